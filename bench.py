@@ -1,0 +1,418 @@
+"""Benchmark: fused RMSNorm forward + backward, effective HBM GB/s on GB300.
+
+One step = the whole hot path (forward, backward row kernel, dgamma column
+reduce) over the big-M small-N sweep: RMSNorm, M = 65536 rows,
+N in {256, 384, 512, 768, 1024, 2048}, bf16 tensors, eps = 1e-6,
+x, dy ~ N(0,1), gamma = 1 + 0.1 N(0,1) (seeded synthetic data).
+
+value = algorithmic bytes of every timed call / summed CUDA-event time of
+those calls.  Algorithmic bytes per call (b = 2 for bf16):
+    forward  : 2 M N b + N b + 4 M          (x, y, gamma, rstd)
+    backward : 3 M N b + N b + 4 M + 4 N    (dy, x, dx, gamma, rstd, dgamma)
+Workspace traffic counts as time, never as bytes.  L2 is flushed (a 256 MiB
+write, outside the events) before every timed call.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs the same per-GPU workload (weak
+scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rmsnorm_norm_fwd_gb300.inputs import make_inputs  # noqa: E402
+
+M = 65536
+NS = (256, 384, 512, 768, 1024, 2048)
+EPS = 1e-6
+B = 2  # bf16
+METRIC = "norm fwd/bwd effective HBM GB/s and % of GB300 peak, per (M,N,dtype)"
+WORKLOAD = ("RMSNorm fwd+bwd sweep, M=65536 rows, N in {256,384,512,768,1024,2048}, "
+            "bf16 tensors, fp32 rstd and dgamma, eps=1e-6")
+L2_FLUSH_BYTES = 256 << 20
+
+# Measured DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# roofline kernel, from the ncu capture summarised under profiles/, valid only
+# for the kernel sources whose digest is recorded with it.
+NCU_TRAFFIC = {"kernel_digest": None, "variant": None, "N": None, "bytes_per_launch": None}
+
+
+def fwd_bytes(m, n):
+    return 2 * m * n * B + n * B + 4 * m
+
+
+def bwd_bytes(m, n):
+    return 3 * m * n * B + n * B + 4 * m + 4 * n
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rmsnorm_norm_fwd_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h", ".inc")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, throttle reasons)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max_sum(vals_max, vals_sum, ws):
+    """Max over ranks of vals_max, sum over ranks of vals_sum (gloo or nccl)."""
+    if ws == 1:
+        return vals_max, vals_sum
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    a = torch.tensor(vals_max, dtype=torch.float64, device=dev)
+    b = torch.tensor(vals_sum, dtype=torch.float64, device=dev)
+    dist.all_reduce(a, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return a.tolist(), b.tolist()
+
+
+# ---------------------------------------------------------------------------- oracle on the host
+def oracle_sample(rows_per_n: int, seed: int = 20261202):
+    """Time the fp64 oracle (as it stands) on `rows_per_n` rows of every N of
+    the workload: forward plus backward (dx and dgamma).  Returns
+    (bytes, seconds, threads)."""
+    import numpy as np
+
+    import oracle
+    tot_b, tot_t = 0, 0.0
+    for n in NS:
+        inp = make_inputs(rows_per_n, n, dtype="bf16", dist="rms", op="rms", seed=seed)
+        x = np.ascontiguousarray(inp.x.double().numpy())
+        dy = np.ascontiguousarray(inp.dy.double().numpy())
+        g = np.ascontiguousarray(inp.gamma.double().numpy())
+        t0 = time.perf_counter()
+        oracle.rmsnorm_fwd(x, g, EPS)
+        oracle.rmsnorm_bwd(dy, x, g, EPS)
+        tot_t += time.perf_counter() - t0
+        tot_b += fwd_bytes(rows_per_n, n) + bwd_bytes(rows_per_n, n)
+    return tot_b, tot_t, oracle.threads()
+
+
+def cpu_baseline(target_s: float = 10.0):
+    rows = 512
+    b, t, th = oracle_sample(rows)
+    if t < target_s:
+        rows = int(min(M, rows * max(1.0, target_s / max(t, 1e-3))))
+        b, t, th = oracle_sample(rows)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": th, "kind": "oracle",
+            "sample": f"{rows} of {M} rows at each N of the sweep, fwd+bwd, bf16 inputs "
+                      f"promoted to fp64 ({t:.1f} s of CPU work)"}
+
+
+def run_reference(args, ws, rank):
+    """The oracle arm: the fp64 CPU oracle on the host cores, same workload,
+    each step a bounded row sample of it."""
+    if rank != 0:
+        return
+    rows = 4096
+    for _ in range(args.warmup):
+        oracle_sample(rows // 8)
+    tb, tt, th = 0, 0.0, 1
+    for _ in range(args.steps):
+        b, t, th = oracle_sample(rows)
+        tb += b
+        tt += t
+    v = tb / tt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": list(NS), "sample_rows_per_N": rows},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": th, "kind": "oracle",
+                             "sample": f"{rows} of {M} rows at each N per step, fwd+bwd"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- GPU arm
+def run_ours(args, ws, rank, local):
+    import rmsnorm_norm_fwd_gb300 as gb
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    # Inputs resident in HBM before timing.
+    data = []
+    for n in NS:
+        inp = make_inputs(M, n, dtype="bf16", dist="rms", op="rms", seed=20261202 + rank)
+        d = {"n": n, "x": inp.x.to(dev), "dy": inp.dy.to(dev), "gamma": inp.gamma.to(dev)}
+        d["y"] = torch.empty_like(d["x"])
+        d["dx"] = torch.empty_like(d["x"])
+        d["rstd"] = torch.empty(M, device=dev, dtype=torch.float32)
+        d["dgamma"] = torch.empty(n, device=dev, dtype=torch.float32)
+        d["ws"] = torch.empty(gb.norm_bwd_workspace_size(False, M, n, torch.bfloat16), device=dev,
+                              dtype=torch.uint8)
+        d["host"] = inp
+        data.append(d)
+    scrub = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+
+    def call_fwd(d):
+        gb.rmsnorm_fwd(d["x"], d["gamma"], EPS, y=d["y"], rstd=d["rstd"])
+
+    def call_bwd(d):
+        gb.rmsnorm_bwd(d["dy"], d["x"], d["gamma"], d["rstd"], dx=d["dx"], dgamma=d["dgamma"],
+                       workspace=d["ws"])
+
+    def one_step(record):
+        for d in data:
+            scrub.zero_()
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            call_fwd(d)
+            e1.record(stream)
+            scrub.zero_()
+            e1b = torch.cuda.Event(enable_timing=True)
+            e1b.record(stream)
+            call_bwd(d)
+            e2.record(stream)
+            if record is not None:
+                record.append((d["n"], e0, e1, e1b, e2))
+
+    for _ in range(max(3, args.warmup)):
+        one_step(None)
+    torch.cuda.synchronize()
+
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    torch.cuda.synchronize()
+    recs = []
+    for _ in range(args.steps):
+        one_step(recs)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+
+    per = {}
+    for n, e0, e1, e1b, e2 in recs:
+        p = per.setdefault(n, {"fwd_ms": [], "bwd_ms": []})
+        p["fwd_ms"].append(e0.elapsed_time(e1))
+        p["bwd_ms"].append(e1b.elapsed_time(e2))
+    t_local = sum(sum(p["fwd_ms"]) + sum(p["bwd_ms"]) for p in per.values())  # ms, all steps
+    b_local = float(args.steps * sum(fwd_bytes(M, n) + bwd_bytes(M, n) for n in NS))
+    (t_max,), (b_sum,) = reduce_max_sum([t_local], [b_local], ws)
+    value = b_sum / (t_max * 1e-3) / 1e9
+
+    # Dominant call: the largest share of the timed region.
+    shares = []
+    for n, p in per.items():
+        for direction, key, nbytes in ((0, "fwd_ms", fwd_bytes(M, n)), (1, "bwd_ms", bwd_bytes(M, n))):
+            shares.append((sum(p[key]), n, direction, nbytes, statistics.mean(p[key])))
+    shares.sort(reverse=True)
+    tot, n_dom, dir_dom, bytes_dom, avg_ms = shares[0]
+    peak, peak_kind = peak_hbm()
+    achieved = bytes_dom / (avg_ms * 1e-3) / 1e9
+    vname = gb.variant_name(False, dir_dom, M, n_dom, torch.bfloat16)
+    digest = kernel_digest()
+    traffic = None
+    if (NCU_TRAFFIC["kernel_digest"] == digest and NCU_TRAFFIC["N"] == n_dom
+            and NCU_TRAFFIC["variant"] == vname):
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+
+    # End to end through the public API from pinned host memory, per step:
+    # H2D of x, dy, gamma; forward; backward; D2H of y, rstd, dx, dgamma.
+    e2e = None
+    if not args.no_e2e:
+        hb = []
+        for d in data:
+            h = d["host"]
+            hb.append({"x": h.x.pin_memory(), "dy": h.dy.pin_memory(), "gamma": h.gamma.pin_memory(),
+                       "y": torch.empty_like(h.x).pin_memory(), "dx": torch.empty_like(h.x).pin_memory(),
+                       "rstd": torch.empty(M, dtype=torch.float32).pin_memory(),
+                       "dgamma": torch.empty(d["n"], dtype=torch.float32).pin_memory()})
+        h2d = sum(h["x"].nbytes + h["dy"].nbytes + h["gamma"].nbytes for h in hb)
+        d2h = sum(h["y"].nbytes + h["dx"].nbytes + h["rstd"].nbytes + h["dgamma"].nbytes for h in hb)
+
+        def e2e_step():
+            for d, h in zip(data, hb):
+                d["x"].copy_(h["x"], non_blocking=True)
+                d["dy"].copy_(h["dy"], non_blocking=True)
+                d["gamma"].copy_(h["gamma"], non_blocking=True)
+                call_fwd(d)
+                call_bwd(d)
+                h["y"].copy_(d["y"], non_blocking=True)
+                h["dx"].copy_(d["dx"], non_blocking=True)
+                h["rstd"].copy_(d["rstd"], non_blocking=True)
+                h["dgamma"].copy_(d["dgamma"], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        k2 = max(1, min(args.steps, 5))
+        if dist:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        (te,), (be,) = reduce_max_sum([a.elapsed_time(b)], [float(k2 * sum(
+            fwd_bytes(M, n) + bwd_bytes(M, n) for n in NS))], ws)
+        e2e = {"value": be / (te * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank == 0:
+        breakdown = {str(n): {"fwd_gbs": round(fwd_bytes(M, n) / (statistics.median(p["fwd_ms"]) * 1e-3) / 1e9, 1),
+                              "bwd_gbs": round(bwd_bytes(M, n) / (statistics.median(p["bwd_ms"]) * 1e-3) / 1e9, 1),
+                              "fwd_variant": gb.variant_name(False, 0, M, n, torch.bfloat16),
+                              "bwd_variant": gb.variant_name(False, 1, M, n, torch.bfloat16)}
+                     for n, p in sorted(per.items())}
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": list(NS), "io_dtype": "bf16",
+                       "l2": "flushed before every timed call (256 MiB write outside the events)",
+                       "timing": "CUDA events on the launching stream around each C-ABI call"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": peak_kind,
+                         "kernel": {"dir": "bwd" if dir_dom else "fwd", "N": n_dom, "variant": vname,
+                                    "share_of_timed": tot / t_local,
+                                    "note": ("backward time covers the row kernel and the column "
+                                             "reduce of one call") if dir_dom else "one kernel"}},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * len(NS) * 3,
+            "clocks": clocks,
+            "breakdown": breakdown,
+            "kernel_digest": digest,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank)
+        else:
+            if not torch.cuda.is_available():
+                raise SystemExit("bench.py: no CUDA device; the GPU arm needs one")
+            run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

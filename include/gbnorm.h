@@ -1,0 +1,178 @@
+/*
+ * gbnorm.h -- C ABI of the fused row-wise RMSNorm / LayerNorm library for
+ * GB300 (sm_103a): forward and backward over [M, N] row-major tensors.
+ *
+ * What is computed (per row i of M, over its N contiguous elements):
+ *
+ *   RMSNorm ("SOTA normalization performance with torch.compile", section
+ *   "How Did Torch.compile Catch Quack?"; "Fused RMSNorm", section
+ *   "What it is": a square, a mean, an add of eps, a reciprocal square root,
+ *   a multiply and another multiply):
+ *       rstd_i = 1 / sqrt((1/N) sum_j x_ij^2 + eps)
+ *       y_ij   = (x_ij * rstd_i) * gamma_j
+ *
+ *   LayerNorm (same page and section: subtract the mean, divide by the
+ *   standard deviation, scale by gamma, add beta; biased variance):
+ *       mean_i = (1/N) sum_j x_ij
+ *       rstd_i = 1 / sqrt((1/N) sum_j (x_ij - mean_i)^2 + eps)
+ *       y_ij   = ((x_ij - mean_i) * rstd_i) * gamma_j + beta_j
+ *
+ *   Backward (the outputs dX, dW and dB that the torch.compile page's
+ *   backward paragraph names; the formulas are the analytic gradients):
+ *       xhat_ij = (x_ij - mean_i) * rstd_i         (mean_i = 0 for RMSNorm)
+ *       g_ij    = dy_ij * gamma_j
+ *       RMSNorm:   dx_ij = rstd_i * (g_ij - xhat_ij * (1/N) sum_k g_ik xhat_ik)
+ *       LayerNorm: dx_ij = rstd_i * (g_ij - (1/N) sum_k g_ik
+ *                                         - xhat_ij * (1/N) sum_k g_ik xhat_ik)
+ *       dgamma_j = sum_i dy_ij * xhat_ij,     dbeta_j = sum_i dy_ij
+ *   dgamma/dbeta are reduced in two stages without atomics, as the "Fused
+ *   RMSNorm" page's "What didn't work" and "Next" sections describe: per-block
+ *   partial rows into a caller-provided workspace, then a second kernel that
+ *   sums the workspace column by column in a fixed order (deterministic).
+ *
+ * Conventions shared by every entry point:
+ *   - Layout: x, y, dy, dx are [M, N] row-major and contiguous (row stride N
+ *     elements).  gamma and beta are [N].  mean and rstd are [M] float32.
+ *     dgamma and dbeta are [N] float32.  All are DEVICE pointers on the
+ *     current CUDA device.
+ *   - dtype selects the element type of x, y, dy, dx, gamma and beta; all of
+ *     them share it.  Arithmetic is float32 throughout; each output element
+ *     is rounded once to dtype, round-to-nearest-even.
+ *   - Ownership: the caller allocates and owns every buffer.  The library
+ *     never allocates device memory, never frees, and never synchronises.
+ *     All work is enqueued on `stream` (NULL = the legacy default stream) and
+ *     completes asynchronously.
+ *   - Alignment: with 16-byte-aligned pointers and N * sizeof(dtype) a
+ *     multiple of 16, rows move as 128-bit vectors; anything else takes a
+ *     correct element-wise path.
+ *   - Aliasing: y may equal x exactly (in place) and dx may equal dy exactly;
+ *     any other overlap between an output and an input is rejected.
+ *   - Shapes: M >= 0 (M == 0 launches nothing in the forward and writes zero
+ *     dgamma/dbeta in the backward), 1 <= N <= GBNORM_MAX_N.
+ *   - Errors: every function returns a gbnorm_status_t.  Arguments are
+ *     checked before anything is enqueued; a rejected call enqueues nothing.
+ *     GBNORM_ERR_CUDA reports a failed launch (cudaGetLastError right after
+ *     it).  No C++ exception crosses this interface.
+ *   - Thread safety: all entry points may be called concurrently from several
+ *     host threads; the only shared state is a per-device cache of device
+ *     attributes and occupancy filled once.
+ */
+#ifndef GBNORM_H
+#define GBNORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header needs no CUDA headers. */
+typedef struct CUstream_st *gbnorm_stream_t;
+
+typedef enum {
+    GBNORM_F32 = 0,
+    GBNORM_F16 = 1,
+    GBNORM_BF16 = 2
+} gbnorm_dtype_t;
+
+typedef enum {
+    GBNORM_OK = 0,
+    GBNORM_ERR_INVALID_ARG = 1, /* null pointer, bad shape or dtype, overlapping buffers, bad eps */
+    GBNORM_ERR_UNSUPPORTED = 2, /* a valid request this build cannot serve (e.g. no sm_103a device) */
+    GBNORM_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than norm_bwd_workspace_size */
+    GBNORM_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+} gbnorm_status_t;
+
+/* Largest row length N accepted by every entry point. */
+#define GBNORM_MAX_N ((int64_t)1 << 24)
+
+/*
+ * RMSNorm forward.
+ *   x      [M, N] dtype, read only.
+ *   gamma  [N] dtype, read only.
+ *   y      [M, N] dtype, written (may equal x).
+ *   rstd   [M] float32, written; may be NULL (nothing stored, e.g. inference).
+ *   eps    added to the mean square under the root; finite and >= 0.
+ */
+int rmsnorm_fwd(const void *x, const void *gamma, void *y, float *rstd, int64_t M, int64_t N,
+                int dtype, float eps, gbnorm_stream_t stream);
+
+/*
+ * LayerNorm forward.
+ *   x, gamma, y, rstd as for rmsnorm_fwd; beta [N] dtype, read only.
+ *   mean   [M] float32, written; may be NULL.  rstd may be NULL.
+ *   eps    added to the biased variance under the root; finite and >= 0.
+ */
+int layernorm_fwd(const void *x, const void *gamma, const void *beta, void *y, float *mean,
+                  float *rstd, int64_t M, int64_t N, int dtype, float eps,
+                  gbnorm_stream_t stream);
+
+/*
+ * Bytes of device workspace the backward of this shape needs on the current
+ * device (the per-block partial rows of dgamma, and of dbeta for LayerNorm).
+ * Returns 0 if the arguments are invalid or no CUDA device is usable.
+ */
+size_t norm_bwd_workspace_size(int is_layernorm, int64_t M, int64_t N, int dtype);
+
+/*
+ * RMSNorm backward.
+ *   dy, x  [M, N] dtype, read only.   gamma [N] dtype, read only.
+ *   rstd   [M] float32 as saved by rmsnorm_fwd, read only.
+ *   dx     [M, N] dtype, written (may equal dy).
+ *   dgamma [N] float32, written (overwritten, not accumulated).
+ *   workspace / workspace_bytes: device scratch of at least
+ *          norm_bwd_workspace_size(0, M, N, dtype) bytes, 16-byte aligned;
+ *          its contents on entry are ignored and on exit are unspecified.
+ *          It must not be used by another call that may run concurrently.
+ */
+int rmsnorm_bwd(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx,
+                float *dgamma, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                int dtype, gbnorm_stream_t stream);
+
+/*
+ * LayerNorm backward.
+ *   as rmsnorm_bwd, plus mean [M] float32 as saved by layernorm_fwd (read
+ *   only) and dbeta [N] float32 (written).  Workspace of at least
+ *   norm_bwd_workspace_size(1, M, N, dtype) bytes.
+ */
+int layernorm_bwd(const void *dy, const void *x, const void *gamma, const float *mean,
+                  const float *rstd, void *dx, float *dgamma, float *dbeta, void *workspace,
+                  size_t workspace_bytes, int64_t M, int64_t N, int dtype,
+                  gbnorm_stream_t stream);
+
+/* Static, human-readable text for a status code. */
+const char *gbnorm_status_string(int status);
+
+/*
+ * Dispatch introspection and tuning (not needed for normal use).
+ *
+ * gbnorm_variant_name writes into buf (NUL-terminated, at most len bytes) the
+ * name of the kernel variant that a call with these arguments would launch on
+ * the current device, and returns GBNORM_OK; `aligned` says whether every
+ * pointer of the call would be 16-byte aligned.  dir is 0 for the forward, 1
+ * for the backward.
+ *
+ * gbnorm_force_variant makes every later call of (is_layernorm, dir, dtype)
+ * in this process launch the named variant whenever it can serve the shape
+ * (otherwise dispatch proceeds as usual); name NULL or "" removes the
+ * override.  Returns GBNORM_ERR_INVALID_ARG for an unknown name.  Meant for
+ * tests and tuning sweeps; not to be changed while another host thread is
+ * calling the library.
+ */
+int gbnorm_variant_name(int is_layernorm, int dir, int64_t M, int64_t N, int dtype, int aligned,
+                        char *buf, size_t len);
+int gbnorm_force_variant(int is_layernorm, int dir, int dtype, const char *name);
+
+/*
+ * Number of kernel variants built for (is_layernorm, dir, dtype), and the
+ * name of the index-th one (NULL if out of range).  For tests and tuning.
+ */
+int gbnorm_variant_count(int is_layernorm, int dir, int dtype);
+const char *gbnorm_variant_at(int is_layernorm, int dir, int dtype, int index);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBNORM_H */

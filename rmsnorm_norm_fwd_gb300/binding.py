@@ -1,0 +1,181 @@
+"""Thin Python binding over libgbnorm.so (include/gbnorm.h).
+
+Argument marshalling only: tensors are checked (CUDA, contiguous, matching
+dtype and shape), outputs and the backward workspace are allocated with torch's
+caching allocator when the caller does not pass them, and the call goes to the
+C ABI on torch's current stream.  Every step of the computation runs in the
+library's CUDA kernels; there is no other implementation to fall back to, and
+importing this module fails if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.environ.get("GBNORM_LIB", os.path.join(_HERE, "libgbnorm.so"))
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libgbnorm.so not found at {LIB_PATH}: build it first "
+        "(python -m rmsnorm_norm_fwd_gb300.build, or __graft_entry__.build()).")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_vp, _i64, _int, _f, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+lib.rmsnorm_fwd.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _int, _f, _vp]
+lib.layernorm_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _f, _vp]
+lib.norm_bwd_workspace_size.argtypes = [_int, _i64, _i64, _int]
+lib.norm_bwd_workspace_size.restype = _sz
+lib.rmsnorm_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _int, _vp]
+lib.layernorm_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _int, _vp]
+lib.gbnorm_status_string.argtypes = [_int]
+lib.gbnorm_status_string.restype = ctypes.c_char_p
+lib.gbnorm_variant_name.argtypes = [_int, _int, _i64, _i64, _int, _int, ctypes.c_char_p, _sz]
+lib.gbnorm_force_variant.argtypes = [_int, _int, _int, ctypes.c_char_p]
+lib.gbnorm_variant_count.argtypes = [_int, _int, _int]
+lib.gbnorm_variant_at.argtypes = [_int, _int, _int, _int]
+lib.gbnorm_variant_at.restype = ctypes.c_char_p
+for _fn in ("rmsnorm_fwd", "layernorm_fwd", "rmsnorm_bwd", "layernorm_bwd", "gbnorm_variant_name",
+            "gbnorm_force_variant", "gbnorm_variant_count"):
+    getattr(lib, _fn).restype = _int
+
+GBNORM_OK = 0
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+DTYPE_NAME = {"fp32": 0, "fp16": 1, "bf16": 2}
+
+
+class GbnormError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {lib.gbnorm_status_string(status).decode()} (status {status})")
+        self.status = status
+
+
+def _check(fn: str, status: int) -> None:
+    if status != GBNORM_OK:
+        raise GbnormError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _mat(name, t, dtype=None):
+    if not (t.is_cuda and t.dim() == 2 and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous 2-D CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}")
+    return t
+
+
+def _vec(name, t, n, dtype):
+    if not (t.is_cuda and t.dim() == 1 and t.is_contiguous() and t.numel() == n and t.dtype == dtype):
+        raise ValueError(f"{name} must be a contiguous 1-D CUDA {dtype} tensor of {n} elements")
+    return t
+
+
+def rmsnorm_fwd(x, gamma, eps: float, y=None, rstd=None, save_stats: bool = True, stream=None):
+    """y = x * rstd * gamma per row; returns (y, rstd) (rstd None if not saved)."""
+    _mat("x", x)
+    M, N = x.shape
+    _vec("gamma", gamma, N, x.dtype)
+    y = torch.empty_like(x) if y is None else _mat("y", y, x.dtype)
+    if rstd is None and save_stats:
+        rstd = torch.empty(M, device=x.device, dtype=torch.float32)
+    _check("rmsnorm_fwd", lib.rmsnorm_fwd(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), M, N,
+                                          DTYPE_CODE[x.dtype], float(eps), _stream(stream)))
+    return y, rstd
+
+
+def layernorm_fwd(x, gamma, beta, eps: float, y=None, mean=None, rstd=None, save_stats: bool = True,
+                  stream=None):
+    """y = (x - mean) * rstd * gamma + beta per row; returns (y, mean, rstd)."""
+    _mat("x", x)
+    M, N = x.shape
+    _vec("gamma", gamma, N, x.dtype)
+    _vec("beta", beta, N, x.dtype)
+    y = torch.empty_like(x) if y is None else _mat("y", y, x.dtype)
+    if save_stats:
+        mean = torch.empty(M, device=x.device, dtype=torch.float32) if mean is None else mean
+        rstd = torch.empty(M, device=x.device, dtype=torch.float32) if rstd is None else rstd
+    _check("layernorm_fwd", lib.layernorm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean),
+                                              _ptr(rstd), M, N, DTYPE_CODE[x.dtype], float(eps),
+                                              _stream(stream)))
+    return y, mean, rstd
+
+
+def norm_bwd_workspace_size(is_layernorm: bool, M: int, N: int, dtype) -> int:
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else DTYPE_NAME.get(dtype, dtype)
+    return int(lib.norm_bwd_workspace_size(int(bool(is_layernorm)), M, N, code))
+
+
+def _workspace(is_ln, x, workspace):
+    M, N = x.shape
+    need = norm_bwd_workspace_size(is_ln, M, N, x.dtype)
+    if need == 0:
+        raise GbnormError("norm_bwd_workspace_size", 2)
+    if workspace is None:
+        workspace = torch.empty(need, device=x.device, dtype=torch.uint8)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def rmsnorm_bwd(dy, x, gamma, rstd, dx=None, dgamma=None, workspace=None, stream=None):
+    """Returns (dx, dgamma) with dgamma in float32."""
+    _mat("x", x)
+    M, N = x.shape
+    _mat("dy", dy, x.dtype)
+    _vec("gamma", gamma, N, x.dtype)
+    _vec("rstd", rstd, M, torch.float32)
+    dx = torch.empty_like(x) if dx is None else _mat("dx", dx, x.dtype)
+    dgamma = torch.empty(N, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
+    ws, wsb = _workspace(False, x, workspace)
+    _check("rmsnorm_bwd", lib.rmsnorm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx),
+                                          _ptr(dgamma), _ptr(ws), wsb, M, N, DTYPE_CODE[x.dtype],
+                                          _stream(stream)))
+    return dx, dgamma
+
+
+def layernorm_bwd(dy, x, gamma, mean, rstd, dx=None, dgamma=None, dbeta=None, workspace=None,
+                  stream=None):
+    """Returns (dx, dgamma, dbeta) with dgamma and dbeta in float32."""
+    _mat("x", x)
+    M, N = x.shape
+    _mat("dy", dy, x.dtype)
+    _vec("gamma", gamma, N, x.dtype)
+    _vec("mean", mean, M, torch.float32)
+    _vec("rstd", rstd, M, torch.float32)
+    dx = torch.empty_like(x) if dx is None else _mat("dx", dx, x.dtype)
+    dgamma = torch.empty(N, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
+    dbeta = torch.empty(N, device=x.device, dtype=torch.float32) if dbeta is None else dbeta
+    ws, wsb = _workspace(True, x, workspace)
+    _check("layernorm_bwd", lib.layernorm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd),
+                                              _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(ws), wsb, M, N,
+                                              DTYPE_CODE[x.dtype], _stream(stream)))
+    return dx, dgamma, dbeta
+
+
+def variant_name(is_layernorm: bool, direction: int, M: int, N: int, dtype, aligned: bool = True) -> str:
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else DTYPE_NAME.get(dtype, dtype)
+    buf = ctypes.create_string_buffer(64)
+    _check("gbnorm_variant_name", lib.gbnorm_variant_name(int(bool(is_layernorm)), direction, M, N,
+                                                          code, int(aligned), buf, 64))
+    return buf.value.decode()
+
+
+def force_variant(is_layernorm: bool, direction: int, dtype, name: str | None) -> None:
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else DTYPE_NAME.get(dtype, dtype)
+    _check("gbnorm_force_variant", lib.gbnorm_force_variant(
+        int(bool(is_layernorm)), direction, code, None if not name else name.encode()))
+
+
+def variants(is_layernorm: bool, direction: int, dtype) -> list[str]:
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else DTYPE_NAME.get(dtype, dtype)
+    n = lib.gbnorm_variant_count(int(bool(is_layernorm)), direction, code)
+    return [lib.gbnorm_variant_at(int(bool(is_layernorm)), direction, code, i).decode() for i in range(n)]

@@ -1,0 +1,418 @@
+// api.cu -- the C ABI declared in include/gbnorm.h: argument checks, dispatch
+// to a kernel variant, grid sizing from measured occupancy, launches.
+//
+// Nothing here allocates device memory or synchronises; every launch goes on
+// the caller's stream.  The only shared state is a per-device cache (SM count,
+// compute capability, occupancy per variant), filled once, read lock-free.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/gbnorm.h"
+#include "params.h"
+
+namespace gbn {
+namespace {
+
+constexpr int kMaxDev = 64;
+constexpr int kMaxVariants = 64;
+
+struct DispatchRow {
+    int is_ln, dir, dtype;
+    int64_t nv_max;
+    const char *variant;
+};
+const DispatchRow kDispatch[] = {
+#include "dispatch_table.inc"
+};
+
+// [is_ln][dir][dtype]
+const VariantTable *const kTables[2][2][3] = {
+    {{&kFwdRms_f32, &kFwdRms_f16, &kFwdRms_bf16}, {&kBwdRms_f32, &kBwdRms_f16, &kBwdRms_bf16}},
+    {{&kFwdLn_f32, &kFwdLn_f16, &kFwdLn_bf16}, {&kBwdLn_f32, &kBwdLn_f16, &kBwdLn_bf16}},
+};
+
+int elem_size(int dtype) { return dtype == GBNORM_F32 ? 4 : 2; }
+
+// ------------------------------------------------------------------ device cache
+struct DevInfo {
+    std::atomic<int> state{0};  // 0 unknown, 1 usable, 2 unusable
+    int sms = 0;
+};
+DevInfo g_dev[kMaxDev];
+std::mutex g_dev_mu;
+// Occupancy per (device, table, variant): blocks per SM (CL == 1) or active
+// clusters on the whole GPU (CL > 1); 0 = not yet measured.
+std::atomic<int> g_occ[kMaxDev][2][2][3][kMaxVariants];
+
+// Forced variant per (is_ln, dir, dtype): index + 1, 0 = none.
+std::atomic<int> g_force[2][2][3];
+
+int current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return GBNORM_ERR_CUDA;
+    if (*dev < 0 || *dev >= kMaxDev) return GBNORM_ERR_UNSUPPORTED;
+    DevInfo &d = g_dev[*dev];
+    int st = d.state.load(std::memory_order_acquire);
+    if (st == 0) {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        st = d.state.load(std::memory_order_relaxed);
+        if (st == 0) {
+            int major = 0, minor = 0, sms = 0;
+            bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) == cudaSuccess &&
+                      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) == cudaSuccess &&
+                      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *dev) == cudaSuccess;
+            if (!ok) return GBNORM_ERR_CUDA;
+            // The kernels are compiled for sm_103a only.
+            st = (major == 10 && minor == 3 && sms > 0) ? 1 : 2;
+            d.sms = sms;
+            d.state.store(st, std::memory_order_release);
+        }
+    }
+    return st == 1 ? GBNORM_OK : GBNORM_ERR_UNSUPPORTED;
+}
+
+bool is_vector_variant(const Variant &v) { return v.vpt > 0; }
+
+// Can variant v hold a row of N elements of a dtype whose 16-byte vector has E elements?
+bool can_serve(const Variant &v, int64_t N, bool vec_ok) {
+    if (!is_vector_variant(v)) return true;
+    return vec_ok && N <= v.max_n();
+}
+
+int find_variant(const VariantTable &t, const char *name) {
+    for (int i = 0; i < t.count; ++i)
+        if (std::strcmp(t.v[i].name, name) == 0) return i;
+    return -1;
+}
+
+// Index of the variant that serves (is_ln, dir, dtype, N); vec_ok says whether
+// the 16-byte-vector kernels may be used for this call.
+int select_variant(int is_ln, int dir, int dtype, int64_t N, bool vec_ok) {
+    const VariantTable &t = *kTables[is_ln][dir][dtype];
+    const int forced = g_force[is_ln][dir][dtype].load(std::memory_order_relaxed) - 1;
+    if (forced >= 0 && forced < t.count && can_serve(t.v[forced], N, vec_ok)) return forced;
+    const int elem = find_variant(t, "elem");
+    if (!vec_ok) return elem;
+    const int E = 16 / elem_size(dtype);
+    const int64_t nv = N / E;
+    for (const DispatchRow &r : kDispatch) {
+        if ((r.is_ln >= 0 && r.is_ln != is_ln) || r.dir != dir || (r.dtype >= 0 && r.dtype != dtype))
+            continue;
+        if (nv > r.nv_max) continue;
+        const int i = find_variant(t, r.variant);
+        if (i >= 0 && can_serve(t.v[i], N, vec_ok)) return i;
+    }
+    return elem;
+}
+
+// Occupancy of a variant on device dev (cached).
+int occupancy(int is_ln, int dir, int dtype, int idx, int dev, int *out) {
+    std::atomic<int> &slot = g_occ[dev][is_ln][dir][dtype][idx];
+    int o = slot.load(std::memory_order_relaxed);
+    if (o > 0) {
+        *out = o;
+        return GBNORM_OK;
+    }
+    const Variant &v = kTables[is_ln][dir][dtype]->v[idx];
+    if (v.cl == 1) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.kernel, v.cta, 0) != cudaSuccess)
+            return GBNORM_ERR_CUDA;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = v.cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(v.cl * g_dev[dev].sms);
+        cfg.blockDim = dim3(v.cta);
+        cfg.dynamicSmemBytes = 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&o, v.kernel, &cfg) != cudaSuccess) return GBNORM_ERR_CUDA;
+    }
+    if (o <= 0) return GBNORM_ERR_UNSUPPORTED;
+    slot.store(o, std::memory_order_relaxed);
+    *out = o;
+    return GBNORM_OK;
+}
+
+// Launch geometry: number of CTAs, and the number of blocks P that each write
+// one partial row in the backward (CTAs, or clusters for cluster variants).
+int plan_grid(int is_ln, int dir, int dtype, int idx, int64_t M, int dev, int64_t *grid,
+              int64_t *P) {
+    const Variant &v = kTables[is_ln][dir][dtype]->v[idx];
+    const int sms = g_dev[dev].sms;
+    if (M <= 0) {
+        *grid = 0;
+        *P = 0;
+        return GBNORM_OK;
+    }
+    int occ = 0;
+    int st = occupancy(is_ln, dir, dtype, idx, dev, &occ);
+    if (st != GBNORM_OK) return st;
+    if (!is_vector_variant(v)) {
+        // Element-wise kernels: one CTA per row at a time.  The backward keeps
+        // one partial row per CTA, so it is held to one CTA per SM.
+        const int64_t cap = dir == 0 ? (int64_t)occ * sms : (int64_t)sms;
+        *grid = M < cap ? M : cap;
+        *P = *grid;
+        return GBNORM_OK;
+    }
+    const int64_t rows_per_unit = v.cl > 1 ? v.rows : v.rows_per_cta_iter();
+    const int64_t units = (M + rows_per_unit - 1) / rows_per_unit;
+    const int64_t cap = v.cl > 1 ? (int64_t)occ : (int64_t)occ * sms;
+    const int64_t n_units = units < cap ? units : cap;
+    *grid = n_units * v.cl;
+    *P = n_units;
+    return GBNORM_OK;
+}
+
+int launch_kernel(const Variant &v, int64_t grid, void *params, cudaStream_t s) {
+    void *args[1] = {params};
+    cudaError_t e;
+    if (v.cl == 1) {
+        e = cudaLaunchKernel(v.kernel, dim3((unsigned)grid), dim3(v.cta), args, 0, s);
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = v.cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(v.cta);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelExC(&cfg, v.kernel, args);
+    }
+    if (e != cudaSuccess) return GBNORM_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? GBNORM_OK : GBNORM_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ argument checks
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool valid_shape(int64_t M, int64_t N, int dtype) {
+    if (dtype != GBNORM_F32 && dtype != GBNORM_F16 && dtype != GBNORM_BF16) return false;
+    if (M < 0 || N < 1 || N > GBNORM_MAX_N) return false;
+    // Byte offsets must fit comfortably in int64.
+    if (M > 0 && M > (INT64_MAX / 16) / N) return false;
+    return true;
+}
+
+struct Buf {
+    const void *p;
+    size_t bytes;
+};
+
+// Any output overlapping any input, or another output, is rejected; an
+// output may coincide exactly with the one input named as its in-place pair.
+bool bad_aliasing(const Buf *outs, int no, const Buf *ins, int ni, const void *inplace_out,
+                  const void *inplace_in) {
+    for (int i = 0; i < no; ++i) {
+        for (int j = 0; j < ni; ++j) {
+            if (outs[i].p == inplace_out && ins[j].p == inplace_in && inplace_out == inplace_in &&
+                outs[i].bytes == ins[j].bytes)
+                continue;
+            if (overlap(outs[i].p, outs[i].bytes, ins[j].p, ins[j].bytes)) return true;
+        }
+        for (int j = i + 1; j < no; ++j)
+            if (overlap(outs[i].p, outs[i].bytes, outs[j].p, outs[j].bytes)) return true;
+    }
+    return false;
+}
+
+int do_fwd(int is_ln, const void *x, const void *gamma, const void *beta, void *y, float *mean,
+           float *rstd, int64_t M, int64_t N, int dtype, float eps, cudaStream_t stream) {
+    if (!valid_shape(M, N, dtype)) return GBNORM_ERR_INVALID_ARG;
+    if (!gamma || (is_ln && !beta)) return GBNORM_ERR_INVALID_ARG;
+    if (M > 0 && (!x || !y)) return GBNORM_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f) return GBNORM_ERR_INVALID_ARG;
+    const size_t b = (size_t)elem_size(dtype);
+    const size_t mat = (size_t)M * (size_t)N * b, vec = (size_t)N * b, st = (size_t)M * 4;
+    const Buf outs[3] = {{y, mat}, {rstd, st}, {is_ln ? mean : nullptr, st}};
+    const Buf ins[3] = {{x, mat}, {gamma, vec}, {is_ln ? beta : nullptr, vec}};
+    if (bad_aliasing(outs, 3, ins, 3, y, x)) return GBNORM_ERR_INVALID_ARG;
+    int dev;
+    int s = current_device(&dev);
+    if (s != GBNORM_OK) return s;
+    if (M == 0) return GBNORM_OK;
+    const bool vec_ok = (vec % 16) == 0 && aligned16(x) && aligned16(y) && aligned16(gamma) &&
+                        (!is_ln || aligned16(beta));
+    const int idx = select_variant(is_ln, 0, dtype, N, vec_ok);
+    int64_t grid, P;
+    s = plan_grid(is_ln, 0, dtype, idx, M, dev, &grid, &P);
+    if (s != GBNORM_OK) return s;
+    FwdParams p{x, gamma, is_ln ? beta : nullptr, y, is_ln ? mean : nullptr, rstd, M, N, eps};
+    return launch_kernel(kTables[is_ln][0][dtype]->v[idx], grid, &p, stream);
+}
+
+size_t ws_bytes_for(int is_ln, int64_t M, int64_t N, int dtype, int dev, int *status) {
+    const int E = 16 / elem_size(dtype);
+    size_t best = 0;
+    // The call may take either the vector path or the element-wise path
+    // (that depends on pointer alignment), so size for the larger.
+    for (int vec_ok = 0; vec_ok < 2; ++vec_ok) {
+        if (vec_ok && (N % E) != 0) continue;
+        const int idx = select_variant(is_ln, 1, dtype, N, vec_ok != 0);
+        int64_t grid, P;
+        *status = plan_grid(is_ln, 1, dtype, idx, M, dev, &grid, &P);
+        if (*status != GBNORM_OK) return 0;
+        const size_t need = (size_t)P * (size_t)N * 4u * (is_ln ? 2u : 1u);
+        if (need > best) best = need;
+    }
+    return (best + 255u) & ~(size_t)255u;
+}
+
+int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const float *mean,
+           const float *rstd, void *dx, float *dgamma, float *dbeta, void *ws, size_t ws_bytes,
+           int64_t M, int64_t N, int dtype, cudaStream_t stream) {
+    if (!valid_shape(M, N, dtype)) return GBNORM_ERR_INVALID_ARG;
+    if (!gamma || !dgamma || (is_ln && !dbeta)) return GBNORM_ERR_INVALID_ARG;
+    if (M > 0 && (!dy || !x || !rstd || !dx || (is_ln && !mean))) return GBNORM_ERR_INVALID_ARG;
+    const size_t b = (size_t)elem_size(dtype);
+    const size_t mat = (size_t)M * (size_t)N * b, vec = (size_t)N * b, st = (size_t)M * 4,
+                 pv = (size_t)N * 4;
+    const Buf outs[4] = {{dx, mat}, {dgamma, pv}, {is_ln ? dbeta : nullptr, pv}, {nullptr, 0}};
+    const Buf ins[5] = {{dy, mat}, {x, mat}, {gamma, vec}, {rstd, st}, {is_ln ? mean : nullptr, st}};
+    if (bad_aliasing(outs, 3, ins, 5, dx, dy)) return GBNORM_ERR_INVALID_ARG;
+    int dev;
+    int s = current_device(&dev);
+    if (s != GBNORM_OK) return s;
+    const size_t need = ws_bytes_for(is_ln, M, N, dtype, dev, &s);
+    if (s != GBNORM_OK) return s;
+    if (M > 0) {
+        if (!ws || ws_bytes < need || !aligned16(ws)) return GBNORM_ERR_WORKSPACE;
+        const Buf all_out[4] = {outs[0], outs[1], outs[2], {ws, need}};
+        if (bad_aliasing(all_out, 4, ins, 5, dx, dy)) return GBNORM_ERR_INVALID_ARG;
+    }
+
+    const bool vec_ok = (vec % 16) == 0 && aligned16(dy) && aligned16(x) && aligned16(dx) &&
+                        aligned16(gamma);
+    int64_t P = 0;
+    if (M > 0) {
+        const int idx = select_variant(is_ln, 1, dtype, N, vec_ok);
+        int64_t grid;
+        s = plan_grid(is_ln, 1, dtype, idx, M, dev, &grid, &P);
+        if (s != GBNORM_OK) return s;
+        BwdParams p{dy, x, gamma, is_ln ? mean : nullptr, rstd, dx, static_cast<float *>(ws), M, N};
+        s = launch_kernel(kTables[is_ln][1][dtype]->v[idx], grid, &p, stream);
+        if (s != GBNORM_OK) return s;
+    }
+    // Stage two: column sums of the P partial rows (P = 0 writes zeros).
+    const bool v4 = (N % 4) == 0;
+    const int64_t cols_per_cta = 32 * (v4 ? 4 : 1);
+    const dim3 grid2((unsigned)((N + cols_per_cta - 1) / cols_per_cta), is_ln ? 2u : 1u);
+    const float *wsc = static_cast<const float *>(ws);
+    void *args[5] = {&wsc, &P, &N, &dgamma, &dbeta};
+    if (cudaLaunchKernel(v4 ? kColReduceVec4 : kColReduceScalar, grid2, dim3(kColCTA), args, 0,
+                         stream) != cudaSuccess)
+        return GBNORM_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? GBNORM_OK : GBNORM_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gbn
+
+using namespace gbn;
+
+extern "C" {
+
+int rmsnorm_fwd(const void *x, const void *gamma, void *y, float *rstd, int64_t M, int64_t N,
+                int dtype, float eps, gbnorm_stream_t stream) {
+    return do_fwd(0, x, gamma, nullptr, y, nullptr, rstd, M, N, dtype, eps,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+int layernorm_fwd(const void *x, const void *gamma, const void *beta, void *y, float *mean,
+                  float *rstd, int64_t M, int64_t N, int dtype, float eps,
+                  gbnorm_stream_t stream) {
+    return do_fwd(1, x, gamma, beta, y, mean, rstd, M, N, dtype, eps,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t norm_bwd_workspace_size(int is_layernorm, int64_t M, int64_t N, int dtype) {
+    if (!valid_shape(M, N, dtype)) return 0;
+    int dev;
+    if (current_device(&dev) != GBNORM_OK) return 0;
+    int st = GBNORM_OK;
+    const size_t b = ws_bytes_for(is_layernorm ? 1 : 0, M, N, dtype, dev, &st);
+    if (st != GBNORM_OK) return 0;
+    return b > 256 ? b : 256;
+}
+
+int rmsnorm_bwd(const void *dy, const void *x, const void *gamma, const float *rstd, void *dx,
+                float *dgamma, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                int dtype, gbnorm_stream_t stream) {
+    return do_bwd(0, dy, x, gamma, nullptr, rstd, dx, dgamma, nullptr, workspace, workspace_bytes,
+                  M, N, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int layernorm_bwd(const void *dy, const void *x, const void *gamma, const float *mean,
+                  const float *rstd, void *dx, float *dgamma, float *dbeta, void *workspace,
+                  size_t workspace_bytes, int64_t M, int64_t N, int dtype,
+                  gbnorm_stream_t stream) {
+    return do_bwd(1, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, workspace, workspace_bytes, M, N,
+                  dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *gbnorm_status_string(int status) {
+    switch (status) {
+    case GBNORM_OK: return "ok";
+    case GBNORM_ERR_INVALID_ARG: return "invalid argument";
+    case GBNORM_ERR_UNSUPPORTED: return "unsupported (needs an sm_103a device)";
+    case GBNORM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case GBNORM_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+    }
+}
+
+int gbnorm_variant_name(int is_layernorm, int dir, int64_t M, int64_t N, int dtype, int aligned,
+                        char *buf, size_t len) {
+    if (!valid_shape(M, N, dtype) || (dir != 0 && dir != 1) || !buf || len == 0)
+        return GBNORM_ERR_INVALID_ARG;
+    const int E = 16 / elem_size(dtype);
+    const bool vec_ok = aligned && (N % E) == 0;
+    const int idx = select_variant(is_layernorm ? 1 : 0, dir, dtype, N, vec_ok);
+    std::snprintf(buf, len, "%s", kTables[is_layernorm ? 1 : 0][dir][dtype]->v[idx].name);
+    return GBNORM_OK;
+}
+
+int gbnorm_force_variant(int is_layernorm, int dir, int dtype, const char *name) {
+    if ((dir != 0 && dir != 1) || dtype < 0 || dtype > 2) return GBNORM_ERR_INVALID_ARG;
+    const int ln = is_layernorm ? 1 : 0;
+    if (!name || !name[0]) {
+        g_force[ln][dir][dtype].store(0);
+        return GBNORM_OK;
+    }
+    const int i = find_variant(*kTables[ln][dir][dtype], name);
+    if (i < 0) return GBNORM_ERR_INVALID_ARG;
+    g_force[ln][dir][dtype].store(i + 1);
+    return GBNORM_OK;
+}
+
+int gbnorm_variant_count(int is_layernorm, int dir, int dtype) {
+    if ((dir != 0 && dir != 1) || dtype < 0 || dtype > 2) return 0;
+    return kTables[is_layernorm ? 1 : 0][dir][dtype]->count;
+}
+
+const char *gbnorm_variant_at(int is_layernorm, int dir, int dtype, int index) {
+    if ((dir != 0 && dir != 1) || dtype < 0 || dtype > 2) return nullptr;
+    const VariantTable &t = *kTables[is_layernorm ? 1 : 0][dir][dtype];
+    return (index >= 0 && index < t.count) ? t.v[index].name : nullptr;
+}
+
+}  // extern "C"

@@ -1,0 +1,214 @@
+// device_common.cuh -- device-side building blocks shared by the norm kernels:
+// 128-bit vector packing for bf16/fp16/fp32, row reductions at warp, CTA and
+// thread-block-cluster level (the last through distributed shared memory),
+// and the few PTX wrappers the cluster path needs.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbn {
+
+// Elements of T carried by one 16-byte vector.
+template <typename T> struct VecTraits;
+template <> struct VecTraits<float> { static constexpr int E = 4; };
+template <> struct VecTraits<__half> { static constexpr int E = 8; };
+template <> struct VecTraits<__nv_bfloat16> { static constexpr int E = 8; };
+
+// ---------------------------------------------------------------- 16-byte vectors
+__device__ __forceinline__ uint32_t word(const uint4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Element e of a 16-byte vector, widened to float (exact for all three types).
+template <typename T> __device__ __forceinline__ float vget(const uint4 &v, int e);
+
+template <> __device__ __forceinline__ float vget<float>(const uint4 &v, int e) {
+    return __uint_as_float(word(v, e));
+}
+template <> __device__ __forceinline__ float vget<__nv_bfloat16>(const uint4 &v, int e) {
+    const uint32_t w = word(v, e >> 1);
+    return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+template <> __device__ __forceinline__ float vget<__half>(const uint4 &v, int e) {
+    const uint32_t w = word(v, e >> 1);
+    __half2 h = *reinterpret_cast<const __half2 *>(&w);
+    return (e & 1) ? __high2float(h) : __low2float(h);
+}
+
+// Pack E floats into one 16-byte vector of T, each rounded to nearest even.
+template <typename T> __device__ __forceinline__ uint4 vpack(const float *f);
+
+template <> __device__ __forceinline__ uint4 vpack<float>(const float *f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+}
+template <> __device__ __forceinline__ uint4 vpack<__nv_bfloat16>(const float *f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <> __device__ __forceinline__ uint4 vpack<__half>(const float *f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Scalar element conversions for the element-wise (any-alignment) path.
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Read-only 16-byte load through the non-coherent path; p must be 16-byte aligned.
+__device__ __forceinline__ uint4 ld_vec(const void *base, int64_t idx) {
+    return __ldg(reinterpret_cast<const uint4 *>(base) + idx);
+}
+__device__ __forceinline__ void st_vec(void *base, int64_t idx, const uint4 &v) {
+    reinterpret_cast<uint4 *>(base)[idx] = v;
+}
+
+// ---------------------------------------------------------------- cluster PTX
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Full cluster barrier: every thread of every CTA arrives (release) and waits
+// (acquire), so shared::cluster stores issued before it are visible after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- reductions
+// Butterfly sum over aligned groups of G lanes (G a power of two <= 32).  Every
+// lane of a group ends with the same bits: each step adds the same two
+// operands on both partner lanes, and float addition is commutative.
+template <int G, int R>
+__device__ __forceinline__ void group_sum(float (&v)[R]) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
+    }
+}
+
+// Shared-memory scratch of one row reducer (two parity copies, so that one
+// barrier per reduction suffices: the barrier of call k+1 proves every thread
+// has finished reading the copy that call k+2 overwrites).
+template <int TPR, int RPC, int CL, int R> struct RowReduceSmem {
+    static constexpr int WPR = TPR > 32 ? TPR / 32 : 1;
+    float warp_part[TPR > 32 ? 2 * RPC * R * WPR : 1];
+    float cta_part[CL > 1 ? 2 * R * CL : 1];
+};
+
+// All-reduce R independent sums over the TPR threads of a row group, and over
+// the CL CTAs of the cluster when CL > 1.  Every thread of the row (in every
+// CTA of the cluster) receives identical bits: partials are combined in a
+// fixed order (lane butterfly, then warps in index order, then CTAs in rank
+// order).  All threads of the CTA must call it together.
+template <int TPR, int RPC, int CL, int R>
+__device__ __forceinline__ void row_allreduce(float (&v)[R], RowReduceSmem<TPR, RPC, CL, R> &sm,
+                                              int &parity) {
+    group_sum<(TPR < 32 ? TPR : 32), R>(v);
+    if constexpr (TPR > 32) {
+        constexpr int WPR = TPR / 32;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int grp = threadIdx.x / TPR, wig = warp % WPR;
+        float *buf = sm.warp_part + parity * (RPC * R * WPR);
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) buf[(grp * R + r) * WPR + wig] = v[r];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPR; ++w) s += buf[(grp * R + r) * WPR + w];
+            v[r] = s;
+        }
+    }
+    if constexpr (CL > 1) {
+        float *buf = sm.cta_part + parity * (R * CL);
+        const uint32_t me = cluster_ctarank();
+        if (threadIdx.x < CL) {
+            const uint32_t remote = map_to_rank(smem_u32(buf), threadIdx.x);
+#pragma unroll
+            for (int r = 0; r < R; ++r) st_cluster_f32(remote + 4u * (r * CL + me), v[r]);
+        }
+        cluster_sync_all();
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float s = 0.f;
+#pragma unroll
+            for (int c = 0; c < CL; ++c) s += buf[r * CL + c];
+            v[r] = s;
+        }
+    }
+    parity ^= 1;
+}
+
+// Sum over all threads of a CTA of NT threads (NT a multiple of 32), same
+// determinism guarantees; used by the element-wise path.
+template <int NT, int R>
+__device__ __forceinline__ void cta_allreduce(float (&v)[R], float *buf2 /* [2][R][NT/32] */,
+                                              int &parity) {
+    constexpr int W = NT / 32;
+    group_sum<32, R>(v);
+    float *buf = buf2 + parity * (R * W);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) buf[r * W + warp] = v[r];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) s += buf[r * W + w];
+        v[r] = s;
+    }
+    parity ^= 1;
+}
+
+}  // namespace gbn

@@ -1,0 +1,5 @@
+// Kernel instantiations: bwdward, element type __nv_bfloat16.
+#define GBN_T __nv_bfloat16
+#define GBN_SFX bf16
+#define GBN_BWD 1
+#include "inst_body.cuh"

@@ -1,0 +1,5 @@
+// Kernel instantiations: fwdward, element type __half.
+#define GBN_T __half
+#define GBN_SFX f16
+#define GBN_FWD 1
+#include "inst_body.cuh"

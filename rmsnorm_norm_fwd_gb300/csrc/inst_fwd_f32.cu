@@ -1,0 +1,5 @@
+// Kernel instantiations: fwdward, element type float.
+#define GBN_T float
+#define GBN_SFX f32
+#define GBN_FWD 1
+#include "inst_body.cuh"

@@ -1,0 +1,136 @@
+"""The C-ABI library: loads, exports every declared symbol, and rejects bad
+arguments before touching a device (CPU only; nothing here launches)."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+LIB = os.path.join(ROOT, "rmsnorm_norm_fwd_gb300", "libgbnorm.so")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from rmsnorm_norm_fwd_gb300 import build
+        build.build()
+    from rmsnorm_norm_fwd_gb300 import binding
+    return binding.lib
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(HEADER_DIR)):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\([^;{]*\)\s*;", text, re.M):
+            names.append(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for want in ("rmsnorm_fwd", "rmsnorm_bwd", "layernorm_fwd", "layernorm_bwd",
+                 "norm_bwd_workspace_size", "gbnorm_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_exported_symbols_are_c_names():
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for n in declared_functions():
+        assert n in syms, f"{n} not exported with C linkage"
+
+
+def test_status_strings(lib):
+    for s, want in ((0, "ok"), (1, "invalid argument"), (3, "workspace")):
+        assert want in lib.gbnorm_status_string(s).decode()
+    assert lib.gbnorm_status_string(99) == b"unknown status"
+
+
+def test_variant_tables(lib):
+    from rmsnorm_norm_fwd_gb300 import binding as b
+    for ln in (False, True):
+        for d in (0, 1):
+            for dt in ("fp32", "fp16", "bf16"):
+                names = b.variants(ln, d, dt)
+                assert "elem" in names and len(names) == len(set(names)) >= 10
+    assert lib.gbnorm_force_variant(0, 0, 2, b"no-such-variant") == 1
+    assert lib.gbnorm_force_variant(0, 0, 2, None) == 0
+    assert lib.gbnorm_variant_at(0, 0, 2, 10_000) is None
+
+
+# Fake, never-dereferenced addresses: argument checks run before any device use.
+A, B, C, D, E_, F, G, H = (0x10000 * k for k in range(1, 9))
+V = ctypes.c_void_p
+
+
+def test_forward_rejects_bad_arguments(lib):
+    bf16 = 2
+    f = lib.rmsnorm_fwd
+    assert f(V(A), V(B), V(C), V(D), 4, 0, bf16, 1e-6, None) == 1            # N = 0
+    assert f(V(A), V(B), V(C), V(D), -1, 8, bf16, 1e-6, None) == 1           # M < 0
+    assert f(V(A), V(B), V(C), V(D), 4, 8, 7, 1e-6, None) == 1               # dtype
+    assert f(V(A), None, V(C), V(D), 4, 8, bf16, 1e-6, None) == 1            # gamma null
+    assert f(None, V(B), V(C), V(D), 4, 8, bf16, 1e-6, None) == 1            # x null
+    assert f(V(A), V(B), V(C), V(D), 4, 8, bf16, float("nan"), None) == 1    # eps
+    assert f(V(A), V(B), V(C), V(D), 4, 8, bf16, -1.0, None) == 1            # eps < 0
+    assert f(V(A), V(B), V(A + 2), V(D), 4, 8, bf16, 1e-6, None) == 1        # y overlaps x
+    assert f(V(A), V(B), V(C), V(C + 4), 4, 8, bf16, 1e-6, None) == 1        # rstd overlaps y
+    assert f(V(A), V(B), V(C), V(D), 4, (1 << 24) + 1, bf16, 1e-6, None) == 1  # N too large
+    g = lib.layernorm_fwd
+    assert g(V(A), V(B), None, V(C), V(D), V(E_), 4, 8, bf16, 1e-5, None) == 1  # beta null
+    assert g(V(A), V(B), V(F), V(C), V(D), V(D), 4, 8, bf16, 1e-5, None) == 1   # mean == rstd
+
+
+def test_backward_rejects_bad_arguments(lib):
+    bf16 = 2
+    f = lib.rmsnorm_bwd
+    # dx overlapping x (not the permitted in-place pair dx == dy)
+    assert f(V(A), V(B), V(C), V(D), V(B), V(E_), V(F), 1 << 20, 4, 8, bf16, None) == 1
+    assert f(V(A), V(B), V(C), V(D), V(E_), None, V(F), 1 << 20, 4, 8, bf16, None) == 1  # dgamma
+    assert f(V(A), V(B), V(C), None, V(E_), V(G), V(F), 1 << 20, 4, 8, bf16, None) == 1  # rstd
+    assert f(V(A), V(B), V(C), V(D), V(E_), V(G), V(F), 1 << 20, 4, 0, bf16, None) == 1  # N
+    g = lib.layernorm_bwd
+    assert g(V(A), V(B), V(C), None, V(D), V(E_), V(F), V(G), V(H), 1 << 20, 4, 8, bf16, None) == 1
+    assert g(V(A), V(B), V(C), V(D), V(D + 8), V(E_), V(F), V(F), V(H), 1 << 20, 4, 8, bf16,
+             None) == 1  # dgamma == dbeta
+
+
+def test_valid_call_without_device_reports_cuda_or_unsupported(lib):
+    # A well-formed call on a machine without a usable sm_103a device must not
+    # pretend to succeed.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    st = lib.rmsnorm_fwd(V(A), V(B), V(C), V(D), 4, 8, 2, 1e-6, None)
+    assert st in (2, 4)
+    assert lib.norm_bwd_workspace_size(0, 4, 8, 2) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    env = dict(os.environ, GBNORM_LIB=str(tmp_path / "missing.so"), PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", "import rmsnorm_norm_fwd_gb300 as g; g.rmsnorm_fwd"],
+                       capture_output=True, text=True, env=env, cwd=ROOT)
+    assert r.returncode != 0 and "libgbnorm.so not found" in r.stderr
+
+
+def test_product_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "rmsnorm_norm_fwd_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".inc", ".cpp")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "norm_oracle" not in text, fn

@@ -1,0 +1,184 @@
+"""CUDA path vs the fp64 oracle on small and ragged shapes, every variant,
+and the edge cases (GPU; every call goes through the C ABI)."""
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from parity_util import compare, gpu_run, run_case
+from rmsnorm_norm_fwd_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["bf16", "fp16", "fp32"]
+# Row lengths spanning every dispatch bucket, non-powers of two, and tails
+# that do not fill a vector (element-wise path).
+SMALL_N = [1, 3, 8, 63, 256, 384, 1000, 1024, 2048, 4096, 5120, 8192, 16392, 32768, 65536, 131072]
+
+
+def _rows_for(N):
+    # A few hundred rows for short rows (several CTAs and a ragged last
+    # iteration), fewer for wide rows so that the oracle stays quick.
+    return 301 if N <= 4096 else (37 if N <= 32768 else 9)
+
+
+@pytest.mark.parametrize("N", SMALL_N)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", ["rms", "ln"])
+def test_small_shapes(op, dtype, N):
+    rep, _, _ = run_case(op, dtype, _rows_for(N), N, dist="llm" if N >= 4096 else None)
+    rep.assert_ok()
+
+
+def _geom(name):
+    m = re.fullmatch(r"(\d+)x(\d+)r(\d+)c(\d+)b(\d+)", name)
+    return tuple(int(v) for v in m.groups()) if m else None
+
+
+def _variant_cases():
+    import rmsnorm_norm_fwd_gb300 as g
+    cases = []
+    for op in ("rms", "ln"):
+        for d in (0, 1):
+            for dt in DTYPES:
+                for v in g.variants(op == "ln", d, dt):
+                    cases.append((op, d, dt, v))
+    return cases
+
+
+def _variant_ids():
+    try:
+        return [f"{o}-{'fwd' if d == 0 else 'bwd'}-{t}-{v}" for o, d, t, v in _variant_cases()]
+    except Exception:
+        return None
+
+
+try:
+    _CASES = _variant_cases()
+except Exception:  # library not built (collection on a machine without it)
+    _CASES = []
+
+
+@pytest.mark.parametrize("op,direction,dtype,variant", _CASES, ids=_variant_ids())
+def test_forced_variant(op, direction, dtype, variant):
+    """Each compiled variant, forced, at its full row capacity and at a row
+    one vector short of it, with a ragged number of rows."""
+    import rmsnorm_norm_fwd_gb300 as g
+    E = 4 if dtype == "fp32" else 8
+    geo = _geom(variant)
+    if geo is None:  # the element-wise variant: odd N
+        shapes = [(67, 1), (67, 77), (5, 3001)]
+    else:
+        tpr, vpt, r, cl, cta = geo
+        cap = tpr * vpt * cl * E
+        rows_per_iter = r if cl > 1 else (cta // tpr) * r
+        M = min(2 * rows_per_iter + 3, max(3, (1 << 21) // cap))
+        shapes = [(M, cap), (M, cap - E)]
+    try:
+        g.force_variant(op == "ln", direction, dtype, variant)
+        for (M, N) in shapes:
+            assert g.variant_name(op == "ln", direction, M, N, dtype, aligned=(geo is not None)) == variant
+            rep, _, _ = run_case(op, dtype, M, N, dist="llm")
+            rep.assert_ok()
+    finally:
+        g.force_variant(op == "ln", direction, dtype, None)
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+def test_empty_rows(op):
+    import rmsnorm_norm_fwd_gb300 as g
+    N = 256
+    x = torch.empty(0, N, device="cuda", dtype=torch.bfloat16)
+    gam = torch.ones(N, device="cuda", dtype=torch.bfloat16)
+    dg = torch.full((N,), 7.0, device="cuda")
+    db = torch.full((N,), 7.0, device="cuda")
+    if op == "rms":
+        y, r = g.rmsnorm_fwd(x, gam, 1e-6)
+        dx, dg = g.rmsnorm_bwd(x, x, gam, r, dgamma=dg)
+    else:
+        y, m, r = g.layernorm_fwd(x, gam, gam, 1e-5)
+        dx, dg, db = g.layernorm_bwd(x, x, gam, m, r, dgamma=dg, dbeta=db)
+        assert torch.all(db == 0)
+    torch.cuda.synchronize()
+    assert y.shape == (0, N) and torch.all(dg == 0)
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_misaligned_pointers_take_the_elementwise_path(op, dtype):
+    """Rows starting off a 16-byte boundary: the vector kernels must not be
+    used, and results must still match."""
+    M, N = 97, 1024
+    inp = make_inputs(M, N, dtype=dtype, op=op)
+    xb = torch.empty(M * N + 1, device="cuda", dtype=inp.x.dtype)
+    db = torch.empty(M * N + 1, device="cuda", dtype=inp.x.dtype)
+    x = xb[1:].view(M, N)
+    dy = db[1:].view(M, N)
+    x.copy_(inp.x)
+    dy.copy_(inp.dy)
+    assert x.data_ptr() % 16 != 0
+    out = gpu_run(op, inp, x_dev=x, dy_dev=dy)
+    compare(op, inp, out).assert_ok()
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+def test_in_place(op):
+    import rmsnorm_norm_fwd_gb300 as g
+    M, N = 129, 2048
+    inp = make_inputs(M, N, op=op)
+    ref = gpu_run(op, inp)
+    x = inp.x.cuda()
+    dy = inp.dy.cuda()
+    gam, bet = inp.gamma.cuda(), inp.beta.cuda()
+    if op == "rms":
+        y, r = g.rmsnorm_fwd(x.clone(), gam, inp.eps)
+        xi = x.clone()
+        y2, _ = g.rmsnorm_fwd(xi, gam, inp.eps, y=xi)
+        dyi = dy.clone()
+        dx2, _ = g.rmsnorm_bwd(dyi, x, gam, r, dx=dyi)
+    else:
+        y, m, r = g.layernorm_fwd(x.clone(), gam, bet, inp.eps)
+        xi = x.clone()
+        y2, _, _ = g.layernorm_fwd(xi, gam, bet, inp.eps, y=xi)
+        dyi = dy.clone()
+        dx2, _, _ = g.layernorm_bwd(dyi, x, gam, m, r, dx=dyi)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, ref["y"]) and torch.equal(dx2, ref["dx"])
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("N", [384, 8192, 65536])
+def test_deterministic(op, N):
+    M = 1024 if N <= 8192 else 64
+    inp = make_inputs(M, N, op=op)
+    a = gpu_run(op, inp)
+    b = gpu_run(op, inp)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_rms_scale_equivariance():
+    """x -> 2x with eps -> 4 eps leaves y unchanged and halves rstd (within
+    tolerance: nothing is assumed about the device's rsqrt)."""
+    import rmsnorm_norm_fwd_gb300 as g
+    inp = make_inputs(512, 1024, dtype="fp32")
+    x, gam = inp.x.cuda(), inp.gamma.cuda()
+    y1, r1 = g.rmsnorm_fwd(x, gam, 1e-6)
+    y2, r2 = g.rmsnorm_fwd(2 * x, gam, 4e-6)
+    torch.cuda.synchronize()
+    assert torch.allclose(y1, y2, rtol=1e-6, atol=1e-7)
+    assert torch.allclose(r1, 2 * r2, rtol=1e-6)
+
+
+def test_degenerate_rows():
+    """Zero rows (RMS: y = 0, rstd = 1/sqrt(eps)) and constant rows (LN:
+    y = beta) against the oracle."""
+    M, N = 64, 512
+    for op in ("rms", "ln"):
+        for dtype in DTYPES:
+            inp = make_inputs(M, N, dtype=dtype, op=op)
+            inp.x[::2] = 0
+            inp.x[1::4] = 1.5
+            out = gpu_run(op, inp)
+            compare(op, inp, out).assert_ok()
