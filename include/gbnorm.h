@@ -171,6 +171,25 @@ int gbnorm_force_variant(int is_layernorm, int dir, int dtype, const char *name)
 int gbnorm_variant_count(int is_layernorm, int dir, int dtype);
 const char *gbnorm_variant_at(int is_layernorm, int dir, int dtype, int index);
 
+/*
+ * Caps the persistent grid of every later launch at max_ctas CTAs (0 removes
+ * the cap; negative values are rejected).  Results do not change, only how
+ * many rows each CTA walks through; the backward workspace size follows the
+ * cap.  For tests and tuning; not to be changed while another host thread is
+ * calling the library.
+ */
+int gbnorm_set_grid_limit(int max_ctas);
+
+/*
+ * Device fault word of the current device.  The kernels that stage rows
+ * through shared memory wait on hardware barriers; every such wait gives up
+ * after about two seconds, sets this word to nonzero and lets the kernel run
+ * to its end (its outputs are then meaningless) instead of hanging the GPU.
+ * Writes the word into *value and, if reset is nonzero, clears it.  This call
+ * synchronises with the device (it is a diagnostic, not for the hot path).
+ */
+int gbnorm_read_fault(int reset, int *value);
+
 #ifdef __cplusplus
 }
 #endif

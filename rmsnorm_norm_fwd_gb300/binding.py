@@ -38,8 +38,11 @@ lib.gbnorm_force_variant.argtypes = [_int, _int, _int, ctypes.c_char_p]
 lib.gbnorm_variant_count.argtypes = [_int, _int, _int]
 lib.gbnorm_variant_at.argtypes = [_int, _int, _int, _int]
 lib.gbnorm_variant_at.restype = ctypes.c_char_p
+lib.gbnorm_read_fault.argtypes = [_int, ctypes.POINTER(ctypes.c_int)]
+lib.gbnorm_set_grid_limit.argtypes = [_int]
 for _fn in ("rmsnorm_fwd", "layernorm_fwd", "rmsnorm_bwd", "layernorm_bwd", "gbnorm_variant_name",
-            "gbnorm_force_variant", "gbnorm_variant_count"):
+            "gbnorm_force_variant", "gbnorm_variant_count", "gbnorm_read_fault",
+            "gbnorm_set_grid_limit"):
     getattr(lib, _fn).restype = _int
 
 GBNORM_OK = 0
@@ -179,3 +182,15 @@ def variants(is_layernorm: bool, direction: int, dtype) -> list[str]:
     code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else DTYPE_NAME.get(dtype, dtype)
     n = lib.gbnorm_variant_count(int(bool(is_layernorm)), direction, code)
     return [lib.gbnorm_variant_at(int(bool(is_layernorm)), direction, code, i).decode() for i in range(n)]
+
+
+def read_fault(reset: bool = True) -> int:
+    """The device fault word (nonzero if a kernel's bounded wait gave up)."""
+    v = ctypes.c_int(0)
+    _check("gbnorm_read_fault", lib.gbnorm_read_fault(int(reset), ctypes.byref(v)))
+    return v.value
+
+
+def set_grid_limit(max_ctas: int) -> None:
+    """Cap the persistent grid of later launches (0 removes the cap); tests/tuning."""
+    _check("gbnorm_set_grid_limit", lib.gbnorm_set_grid_limit(int(max_ctas)))

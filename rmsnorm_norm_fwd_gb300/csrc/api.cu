@@ -1,9 +1,11 @@
 // api.cu -- the C ABI declared in include/gbnorm.h: argument checks, dispatch
-// to a kernel variant, grid sizing from measured occupancy, launches.
+// to a kernel variant, launch geometry from the device's SM count, shared
+// memory and measured occupancy, launches.
 //
-// Nothing here allocates device memory or synchronises; every launch goes on
-// the caller's stream.  The only shared state is a per-device cache (SM count,
-// compute capability, occupancy per variant), filled once, read lock-free.
+// Nothing here allocates device memory or synchronises (except the diagnostic
+// gbnorm_read_fault); every launch goes on the caller's stream.  The only
+// shared state is a per-device cache (SM count, shared-memory limit, fault
+// word address, occupancy per variant), filled once, read lock-free.
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -16,6 +18,10 @@
 #include "params.h"
 
 namespace gbn {
+
+// Set to nonzero by a kernel whose bounded wait gave up (see gbnorm_read_fault).
+__device__ int g_fault_word;
+
 namespace {
 
 constexpr int kMaxDev = 64;
@@ -42,15 +48,21 @@ int elem_size(int dtype) { return dtype == GBNORM_F32 ? 4 : 2; }
 struct DevInfo {
     std::atomic<int> state{0};  // 0 unknown, 1 usable, 2 unusable
     int sms = 0;
+    int smem_optin = 0;         // max dynamic shared memory per block (opt-in)
+    int *fault = nullptr;       // device address of g_fault_word
 };
 DevInfo g_dev[kMaxDev];
 std::mutex g_dev_mu;
-// Occupancy per (device, table, variant): blocks per SM (CL == 1) or active
-// clusters on the whole GPU (CL > 1); 0 = not yet measured.
+// Per (device, table, variant): occupancy (blocks per SM, or active clusters
+// on the whole GPU for cluster variants), 0 = not yet measured; and whether
+// the kernel's dynamic shared-memory limit has been raised.
 std::atomic<int> g_occ[kMaxDev][2][2][3][kMaxVariants];
+std::atomic<int> g_smem_set[kMaxDev][2][2][3][kMaxVariants];
 
 // Forced variant per (is_ln, dir, dtype): index + 1, 0 = none.
 std::atomic<int> g_force[2][2][3];
+// Cap on the persistent grid (CTAs), 0 = none (tests and tuning only).
+std::atomic<int> g_grid_limit{0};
 
 int current_device(int *dev) {
     if (cudaGetDevice(dev) != cudaSuccess) return GBNORM_ERR_CUDA;
@@ -61,26 +73,89 @@ int current_device(int *dev) {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         st = d.state.load(std::memory_order_relaxed);
         if (st == 0) {
-            int major = 0, minor = 0, sms = 0;
+            int major = 0, minor = 0, sms = 0, smem = 0;
+            void *fault = nullptr;
             bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) == cudaSuccess &&
                       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) == cudaSuccess &&
-                      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *dev) == cudaSuccess;
+                      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *dev) == cudaSuccess &&
+                      cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev) ==
+                          cudaSuccess;
             if (!ok) return GBNORM_ERR_CUDA;
             // The kernels are compiled for sm_103a only.
             st = (major == 10 && minor == 3 && sms > 0) ? 1 : 2;
+            if (st == 1) {
+                if (cudaGetSymbolAddress(&fault, g_fault_word) != cudaSuccess) return GBNORM_ERR_CUDA;
+            }
             d.sms = sms;
+            d.smem_optin = smem;
+            d.fault = static_cast<int *>(fault);
             d.state.store(st, std::memory_order_release);
         }
     }
     return st == 1 ? GBNORM_OK : GBNORM_ERR_UNSUPPORTED;
 }
 
-bool is_vector_variant(const Variant &v) { return v.vpt > 0; }
+// What a call allows: 16-byte vectors for the row tensors and gamma/beta
+// (vec), and 16-byte-aligned saved statistics (stats; backward TMA kernels
+// copy them in bulk).
+struct CallShape {
+    int is_ln, dir, dtype;
+    int64_t M, N;
+    bool vec, stats;
+};
 
-// Can variant v hold a row of N elements of a dtype whose 16-byte vector has E elements?
-bool can_serve(const Variant &v, int64_t N, bool vec_ok) {
-    if (!is_vector_variant(v)) return true;
-    return vec_ok && N <= v.max_n();
+// Pipeline geometry of a TMA variant for a row of N elements; false if two
+// stages of at least one row do not fit.
+bool tma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, size_t *dyn_smem) {
+    const size_t row_bytes = (size_t)c.N * elem_size(c.dtype);
+    const int ntens = c.dir == 0 ? 1 : 2;
+    auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
+    // Header, then gamma (and beta for the LayerNorm forward), then the ring.
+    const size_t params = al(row_bytes) * ((c.dir == 0 && c.is_ln) ? 2 : 1);
+    const size_t budget_all = (size_t)g_dev[dev].smem_optin / (size_t)v.ctas_per_sm;
+    if (budget_all <= (size_t)kTmaHeaderBytes + params + 1024) return false;
+    const size_t budget = budget_all - kTmaHeaderBytes - params;
+    // Statistics window per stage (backward): the tile's rows widened to
+    // 16-byte multiples, (RT + 7) & ~3 floats per statistic.
+    auto stride_of = [&](int64_t rt) {
+        size_t s = ntens * al((size_t)rt * row_bytes);
+        if (c.dir == 1) s += al((size_t)((rt + 7) & ~(int64_t)3) * 4 * (c.is_ln ? 2 : 1));
+        return s;
+    };
+    int64_t rt = (int64_t)(v.stage_target / (ntens * row_bytes));
+    if (rt < 1) rt = 1;
+    if (rt > c.M) rt = c.M > 0 ? c.M : 1;  // never more rows per tile than the problem has
+    while (rt > 1 && 2 * stride_of(rt) > budget) rt /= 2;
+    const size_t stride = stride_of(rt);
+    if (2 * stride > budget) return false;
+    int stages = (int)(budget / stride);
+    if (stages > kTmaMaxStages) stages = kTmaMaxStages;
+    size_t ring = (size_t)stages * stride;
+    // The backward combines its row groups' partials in the idle ring.
+    const int rpp = (v.cta - 32) / v.tpr;
+    if (c.dir == 1 && rpp > 1) {
+        const size_t comb = (size_t)v.tpr * v.vpt * v.elems_per_vec * 4 * (c.is_ln ? 2 : 1);
+        if (comb > ring) ring = comb;
+    }
+    if (ring > budget) return false;
+    tc->rows = (int)rt;
+    tc->stages = stages;
+    tc->stride = (uint32_t)stride;
+    tc->fault = g_dev[dev].fault;
+    *dyn_smem = kTmaHeaderBytes + params + ring;
+    return true;
+}
+
+bool can_serve(const Variant &v, const CallShape &c, int dev) {
+    if (v.kind == kElem) return true;
+    if (!c.vec || c.N > v.max_n()) return false;
+    if (v.kind == kTma) {
+        if (c.dir == 1 && !c.stats) return false;
+        TileCfg tc;
+        size_t dyn;
+        return tma_geometry(v, c, dev, &tc, &dyn);
+    }
+    return true;
 }
 
 int find_variant(const VariantTable &t, const char *name) {
@@ -89,36 +164,55 @@ int find_variant(const VariantTable &t, const char *name) {
     return -1;
 }
 
-// Index of the variant that serves (is_ln, dir, dtype, N); vec_ok says whether
-// the 16-byte-vector kernels may be used for this call.
-int select_variant(int is_ln, int dir, int dtype, int64_t N, bool vec_ok) {
-    const VariantTable &t = *kTables[is_ln][dir][dtype];
-    const int forced = g_force[is_ln][dir][dtype].load(std::memory_order_relaxed) - 1;
-    if (forced >= 0 && forced < t.count && can_serve(t.v[forced], N, vec_ok)) return forced;
+// Index of the variant that serves this call.
+int select_variant(const CallShape &c, int dev) {
+    const VariantTable &t = *kTables[c.is_ln][c.dir][c.dtype];
+    const int forced = g_force[c.is_ln][c.dir][c.dtype].load(std::memory_order_relaxed) - 1;
+    if (forced >= 0 && forced < t.count && can_serve(t.v[forced], c, dev)) return forced;
     const int elem = find_variant(t, "elem");
-    if (!vec_ok) return elem;
-    const int E = 16 / elem_size(dtype);
-    const int64_t nv = N / E;
+    if (!c.vec) return elem;
+    const int E = 16 / elem_size(c.dtype);
+    const int64_t nv = c.N / E;
     for (const DispatchRow &r : kDispatch) {
-        if ((r.is_ln >= 0 && r.is_ln != is_ln) || r.dir != dir || (r.dtype >= 0 && r.dtype != dtype))
+        if ((r.is_ln >= 0 && r.is_ln != c.is_ln) || r.dir != c.dir || (r.dtype >= 0 && r.dtype != c.dtype))
             continue;
         if (nv > r.nv_max) continue;
         const int i = find_variant(t, r.variant);
-        if (i >= 0 && can_serve(t.v[i], N, vec_ok)) return i;
+        if (i >= 0 && can_serve(t.v[i], c, dev)) return i;
     }
     return elem;
 }
 
-// Occupancy of a variant on device dev (cached).
-int occupancy(int is_ln, int dir, int dtype, int idx, int dev, int *out) {
-    std::atomic<int> &slot = g_occ[dev][is_ln][dir][dtype][idx];
+struct Plan {
+    int idx;
+    int64_t grid;      // CTAs
+    int64_t P;         // partial rows the backward writes (CTAs, or clusters)
+    size_t dyn_smem;
+    TileCfg tc;
+};
+
+// Occupancy of a variant on device dev (cached, except for TMA variants whose
+// shared-memory footprint depends on the shape).
+int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
+    std::atomic<int> &slot = g_occ[dev][c.is_ln][c.dir][c.dtype][idx];
     int o = slot.load(std::memory_order_relaxed);
-    if (o > 0) {
+    const Variant &v = kTables[c.is_ln][c.dir][c.dtype]->v[idx];
+    if (o > 0 && v.kind != kTma) {
         *out = o;
         return GBNORM_OK;
     }
-    const Variant &v = kTables[is_ln][dir][dtype]->v[idx];
-    if (v.cl == 1) {
+    if (v.kind == kTma) {
+        std::atomic<int> &set = g_smem_set[dev][c.is_ln][c.dir][c.dtype][idx];
+        if (!set.load(std::memory_order_acquire)) {
+            const int lim = g_dev[dev].smem_optin / v.ctas_per_sm;
+            if (cudaFuncSetAttribute(v.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim) !=
+                cudaSuccess)
+                return GBNORM_ERR_CUDA;
+            set.store(1, std::memory_order_release);
+        }
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.kernel, v.cta, dyn_smem) != cudaSuccess)
+            return GBNORM_ERR_CUDA;
+    } else if (v.cl == 1) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.kernel, v.cta, 0) != cudaSuccess)
             return GBNORM_ERR_CUDA;
     } else {
@@ -136,47 +230,61 @@ int occupancy(int is_ln, int dir, int dtype, int idx, int dev, int *out) {
         if (cudaOccupancyMaxActiveClusters(&o, v.kernel, &cfg) != cudaSuccess) return GBNORM_ERR_CUDA;
     }
     if (o <= 0) return GBNORM_ERR_UNSUPPORTED;
-    slot.store(o, std::memory_order_relaxed);
+    if (v.kind != kTma) slot.store(o, std::memory_order_relaxed);
     *out = o;
     return GBNORM_OK;
 }
 
-// Launch geometry: number of CTAs, and the number of blocks P that each write
-// one partial row in the backward (CTAs, or clusters for cluster variants).
-int plan_grid(int is_ln, int dir, int dtype, int idx, int64_t M, int dev, int64_t *grid,
-              int64_t *P) {
-    const Variant &v = kTables[is_ln][dir][dtype]->v[idx];
+// Launch geometry for variant idx.
+int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
+    const Variant &v = kTables[c.is_ln][c.dir][c.dtype]->v[idx];
     const int sms = g_dev[dev].sms;
-    if (M <= 0) {
-        *grid = 0;
-        *P = 0;
-        return GBNORM_OK;
-    }
+    pl->idx = idx;
+    pl->grid = 0;
+    pl->P = 0;
+    pl->dyn_smem = 0;
+    pl->tc = TileCfg{0, 0, 0, g_dev[dev].fault};
+    if (c.M <= 0) return GBNORM_OK;
+    if (v.kind == kTma && !tma_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     int occ = 0;
-    int st = occupancy(is_ln, dir, dtype, idx, dev, &occ);
+    int st = occupancy(c, idx, dev, pl->dyn_smem, &occ);
     if (st != GBNORM_OK) return st;
-    if (!is_vector_variant(v)) {
+    const int64_t limit = g_grid_limit.load(std::memory_order_relaxed);
+    if (v.kind == kElem) {
         // Element-wise kernels: one CTA per row at a time.  The backward keeps
         // one partial row per CTA, so it is held to one CTA per SM.
-        const int64_t cap = dir == 0 ? (int64_t)occ * sms : (int64_t)sms;
-        *grid = M < cap ? M : cap;
-        *P = *grid;
+        int64_t cap = c.dir == 0 ? (int64_t)occ * sms : (int64_t)sms;
+        if (limit > 0 && limit < cap) cap = limit;
+        pl->grid = c.M < cap ? c.M : cap;
+        pl->P = pl->grid;
+        return GBNORM_OK;
+    }
+    if (v.kind == kTma) {
+        const int64_t ntiles = (c.M + pl->tc.rows - 1) / pl->tc.rows;
+        int64_t cap = (int64_t)occ * sms;
+        if (limit > 0 && limit < cap) cap = limit;
+        pl->grid = ntiles < cap ? ntiles : cap;
+        pl->P = pl->grid;
         return GBNORM_OK;
     }
     const int64_t rows_per_unit = v.cl > 1 ? v.rows : v.rows_per_cta_iter();
-    const int64_t units = (M + rows_per_unit - 1) / rows_per_unit;
-    const int64_t cap = v.cl > 1 ? (int64_t)occ : (int64_t)occ * sms;
+    const int64_t units = (c.M + rows_per_unit - 1) / rows_per_unit;
+    int64_t cap = v.cl > 1 ? (int64_t)occ : (int64_t)occ * sms;
+    if (limit > 0) {
+        const int64_t lu = limit / v.cl > 0 ? limit / v.cl : 1;
+        if (lu < cap) cap = lu;
+    }
     const int64_t n_units = units < cap ? units : cap;
-    *grid = n_units * v.cl;
-    *P = n_units;
+    pl->grid = n_units * v.cl;
+    pl->P = n_units;
     return GBNORM_OK;
 }
 
-int launch_kernel(const Variant &v, int64_t grid, void *params, cudaStream_t s) {
+int launch_kernel(const Variant &v, const Plan &pl, void *params, cudaStream_t s) {
     void *args[1] = {params};
     cudaError_t e;
     if (v.cl == 1) {
-        e = cudaLaunchKernel(v.kernel, dim3((unsigned)grid), dim3(v.cta), args, 0, s);
+        e = cudaLaunchKernel(v.kernel, dim3((unsigned)pl.grid), dim3(v.cta), args, pl.dyn_smem, s);
     } else {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -184,9 +292,9 @@ int launch_kernel(const Variant &v, int64_t grid, void *params, cudaStream_t s) 
         attr[0].val.clusterDim.x = v.cl;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3((unsigned)grid);
+        cfg.gridDim = dim3((unsigned)pl.grid);
         cfg.blockDim = dim3(v.cta);
-        cfg.dynamicSmemBytes = 0;
+        cfg.dynamicSmemBytes = pl.dyn_smem;
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -250,28 +358,30 @@ int do_fwd(int is_ln, const void *x, const void *gamma, const void *beta, void *
     int s = current_device(&dev);
     if (s != GBNORM_OK) return s;
     if (M == 0) return GBNORM_OK;
-    const bool vec_ok = (vec % 16) == 0 && aligned16(x) && aligned16(y) && aligned16(gamma) &&
-                        (!is_ln || aligned16(beta));
-    const int idx = select_variant(is_ln, 0, dtype, N, vec_ok);
-    int64_t grid, P;
-    s = plan_grid(is_ln, 0, dtype, idx, M, dev, &grid, &P);
+    CallShape c{is_ln, 0, dtype, M, N, false, true};
+    c.vec = (vec % 16) == 0 && aligned16(x) && aligned16(y) && aligned16(gamma) &&
+            (!is_ln || aligned16(beta));
+    Plan pl;
+    s = make_plan(c, select_variant(c, dev), dev, &pl);
     if (s != GBNORM_OK) return s;
-    FwdParams p{x, gamma, is_ln ? beta : nullptr, y, is_ln ? mean : nullptr, rstd, M, N, eps};
-    return launch_kernel(kTables[is_ln][0][dtype]->v[idx], grid, &p, stream);
+    FwdParams p{x, gamma, is_ln ? beta : nullptr, y, is_ln ? mean : nullptr, rstd, M, N, eps, pl.tc};
+    return launch_kernel(kTables[is_ln][0][dtype]->v[pl.idx], pl, &p, stream);
 }
 
+// Workspace bytes the backward of this shape needs.  The call may take the
+// TMA, the register or the element-wise path (that depends on pointer
+// alignment), so this sizes for the largest of the three.
 size_t ws_bytes_for(int is_ln, int64_t M, int64_t N, int dtype, int dev, int *status) {
     const int E = 16 / elem_size(dtype);
     size_t best = 0;
-    // The call may take either the vector path or the element-wise path
-    // (that depends on pointer alignment), so size for the larger.
-    for (int vec_ok = 0; vec_ok < 2; ++vec_ok) {
-        if (vec_ok && (N % E) != 0) continue;
-        const int idx = select_variant(is_ln, 1, dtype, N, vec_ok != 0);
-        int64_t grid, P;
-        *status = plan_grid(is_ln, 1, dtype, idx, M, dev, &grid, &P);
+    const bool flags[3][2] = {{false, false}, {true, false}, {true, true}};  // (vec, stats)
+    for (const auto &f : flags) {
+        if (f[0] && (N % E) != 0) continue;
+        CallShape c{is_ln, 1, dtype, M, N, f[0], f[1]};
+        Plan pl;
+        *status = make_plan(c, select_variant(c, dev), dev, &pl);
         if (*status != GBNORM_OK) return 0;
-        const size_t need = (size_t)P * (size_t)N * 4u * (is_ln ? 2u : 1u);
+        const size_t need = (size_t)pl.P * (size_t)N * 4u * (is_ln ? 2u : 1u);
         if (need > best) best = need;
     }
     return (best + 255u) & ~(size_t)255u;
@@ -299,18 +409,18 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
         const Buf all_out[4] = {outs[0], outs[1], outs[2], {ws, need}};
         if (bad_aliasing(all_out, 4, ins, 5, dx, dy)) return GBNORM_ERR_INVALID_ARG;
     }
-
-    const bool vec_ok = (vec % 16) == 0 && aligned16(dy) && aligned16(x) && aligned16(dx) &&
-                        aligned16(gamma);
     int64_t P = 0;
     if (M > 0) {
-        const int idx = select_variant(is_ln, 1, dtype, N, vec_ok);
-        int64_t grid;
-        s = plan_grid(is_ln, 1, dtype, idx, M, dev, &grid, &P);
+        CallShape c{is_ln, 1, dtype, M, N, false, false};
+        c.vec = (vec % 16) == 0 && aligned16(dy) && aligned16(x) && aligned16(dx) && aligned16(gamma);
+        c.stats = aligned16(rstd) && (!is_ln || aligned16(mean));
+        Plan pl;
+        s = make_plan(c, select_variant(c, dev), dev, &pl);
         if (s != GBNORM_OK) return s;
-        BwdParams p{dy, x, gamma, is_ln ? mean : nullptr, rstd, dx, static_cast<float *>(ws), M, N};
-        s = launch_kernel(kTables[is_ln][1][dtype]->v[idx], grid, &p, stream);
+        BwdParams p{dy, x, gamma, is_ln ? mean : nullptr, rstd, dx, static_cast<float *>(ws), M, N, pl.tc};
+        s = launch_kernel(kTables[is_ln][1][dtype]->v[pl.idx], pl, &p, stream);
         if (s != GBNORM_OK) return s;
+        P = pl.P;
     }
     // Stage two: column sums of the P partial rows (P = 0 writes zeros).
     const bool v4 = (N % 4) == 0;
@@ -318,8 +428,8 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
     const dim3 grid2((unsigned)((N + cols_per_cta - 1) / cols_per_cta), is_ln ? 2u : 1u);
     const float *wsc = static_cast<const float *>(ws);
     void *args[5] = {&wsc, &P, &N, &dgamma, &dbeta};
-    if (cudaLaunchKernel(v4 ? kColReduceVec4 : kColReduceScalar, grid2, dim3(kColCTA), args, 0,
-                         stream) != cudaSuccess)
+    if (cudaLaunchKernel(v4 ? kColReduceVec4 : kColReduceScalar, grid2, dim3(kColCTA), args, 0, stream) !=
+        cudaSuccess)
         return GBNORM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GBNORM_OK : GBNORM_ERR_CUDA;
 }
@@ -384,10 +494,13 @@ int gbnorm_variant_name(int is_layernorm, int dir, int64_t M, int64_t N, int dty
                         char *buf, size_t len) {
     if (!valid_shape(M, N, dtype) || (dir != 0 && dir != 1) || !buf || len == 0)
         return GBNORM_ERR_INVALID_ARG;
+    int dev;
+    const int s = current_device(&dev);
+    if (s != GBNORM_OK) return s;
     const int E = 16 / elem_size(dtype);
-    const bool vec_ok = aligned && (N % E) == 0;
-    const int idx = select_variant(is_layernorm ? 1 : 0, dir, dtype, N, vec_ok);
-    std::snprintf(buf, len, "%s", kTables[is_layernorm ? 1 : 0][dir][dtype]->v[idx].name);
+    CallShape c{is_layernorm ? 1 : 0, dir, dtype, M, N, aligned && (N % E) == 0, aligned != 0};
+    const int idx = select_variant(c, dev);
+    std::snprintf(buf, len, "%s", kTables[c.is_ln][dir][dtype]->v[idx].name);
     return GBNORM_OK;
 }
 
@@ -413,6 +526,25 @@ const char *gbnorm_variant_at(int is_layernorm, int dir, int dtype, int index) {
     if ((dir != 0 && dir != 1) || dtype < 0 || dtype > 2) return nullptr;
     const VariantTable &t = *kTables[is_layernorm ? 1 : 0][dir][dtype];
     return (index >= 0 && index < t.count) ? t.v[index].name : nullptr;
+}
+
+int gbnorm_set_grid_limit(int max_ctas) {
+    if (max_ctas < 0) return GBNORM_ERR_INVALID_ARG;
+    g_grid_limit.store(max_ctas);
+    return GBNORM_OK;
+}
+
+int gbnorm_read_fault(int reset, int *value) {
+    if (!value) return GBNORM_ERR_INVALID_ARG;
+    int dev;
+    const int s = current_device(&dev);
+    if (s != GBNORM_OK) return s;
+    if (cudaMemcpyFromSymbol(value, g_fault_word, sizeof(int)) != cudaSuccess) return GBNORM_ERR_CUDA;
+    if (reset) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(int)) != cudaSuccess) return GBNORM_ERR_CUDA;
+    }
+    return GBNORM_OK;
 }
 
 }  // extern "C"

@@ -118,6 +118,84 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// ---------------------------------------------------------------- mbarrier + bulk async copy
+// A wait gives up after this many SM clock cycles (about two seconds at the
+// GB300's top clock); real waits last microseconds.
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+// Makes barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// global to this CTA's shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Waits for phase `parity` of `bar` to complete, at most kWaitLimitCycles.
+// Returns false without waiting once the CTA has aborted (*abort != 0); on a
+// timeout it sets *abort and the device fault word, then returns false.  The
+// caller carries on either way, so that every barrier of the CTA stays
+// matched and the kernel ends in bounded time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort, int *fault) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (*abort) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            if (fault) atomicExch(fault, 1);
+            return false;
+        }
+    }
+}
+
+// 16-byte shared-memory load the compiler may not merge with other loads of
+// the same address: staged rows are re-read on every pass instead of being
+// kept live in registers across the row reductions.
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
+// Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- reductions
 // Butterfly sum over aligned groups of G lanes (G a power of two <= 32).  Every
 // lane of a group ends with the same bits: each step adds the same two
@@ -207,6 +285,39 @@ __device__ __forceinline__ void cta_allreduce(float (&v)[R], float *buf2 /* [2][
 #pragma unroll
         for (int w = 0; w < W; ++w) s += buf[r * W + w];
         v[r] = s;
+    }
+    parity ^= 1;
+}
+
+}  // namespace gbn
+
+namespace gbn {
+
+// All-reduce R sums over a row group of TPR consecutive threads that does not
+// span the whole CTA.  TPR <= 32: lane butterfly only.  TPR > 32: butterfly,
+// then warp partials through shared memory `scratch` ([2][R][TPR/32] floats,
+// private to this group) under named barrier `bar_id` (TPR threads).  Same
+// determinism guarantees as row_allreduce.
+template <int TPR, int R>
+__device__ __forceinline__ void group_allreduce(float (&v)[R], float *scratch, int &parity,
+                                                int bar_id) {
+    group_sum<(TPR < 32 ? TPR : 32), R>(v);
+    if constexpr (TPR > 32) {
+        constexpr int WPR = TPR / 32;
+        const int wig = (threadIdx.x % TPR) >> 5, lane = threadIdx.x & 31;
+        float *buf = scratch + parity * (R * WPR);
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) buf[r * WPR + wig] = v[r];
+        }
+        named_sync(bar_id, TPR);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPR; ++w) s += buf[r * WPR + w];
+            v[r] = s;
+        }
     }
     parity ^= 1;
 }

@@ -2,6 +2,7 @@
 // direction.  The including unit defines GBN_T (element type), GBN_SFX (table
 // name suffix) and exactly one of GBN_FWD / GBN_BWD.
 #include "norm_kernels.cuh"
+#include "tma_kernels.cuh"
 #include "variants.inc"
 
 namespace gbn {
@@ -12,31 +13,51 @@ namespace gbn {
 #ifdef GBN_FWD
 #define GBN_ROW(LN, TPR, VPT, R, CL, CTA)                                                     \
     Variant{GBN_VNAME(TPR, VPT, R, CL, CTA), (const void *)&fwd_rows<GBN_T, LN, TPR, VPT, R, CL, CTA>, \
-            TPR, VPT, R, CL, CTA, VecTraits<GBN_T>::E},
+            kRows, TPR, VPT, R, CL, CTA, VecTraits<GBN_T>::E, 0, 0},
 #define GBN_X_RMS(TPR, VPT, R, CL, CTA) GBN_ROW(false, TPR, VPT, R, CL, CTA)
 #define GBN_X_LN(TPR, VPT, R, CL, CTA) GBN_ROW(true, TPR, VPT, R, CL, CTA)
+#define GBN_TMA(LN, TPR, VPT, CW)                                                              \
+    Variant{GBN_TMA_VNAME(TPR, VPT, CW), (const void *)&fwd_tma<GBN_T, LN, TPR, VPT, CW>, kTma, TPR, \
+            VPT, 0, 1, (CW + 1) * 32, VecTraits<GBN_T>::E, 1, 32768},
+#define GBN_T_RMS(TPR, VPT, CW) GBN_TMA(false, TPR, VPT, CW)
+#define GBN_T_LN(TPR, VPT, CW) GBN_TMA(true, TPR, VPT, CW)
 static const Variant rms_variants[] = {
+    GBN_TMA_FWD_GEOMS(GBN_T_RMS)
     GBN_FWD_GEOMS(GBN_X_RMS)
-    Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElemCTA, 0, 1, 1, kElemCTA, 1}};
+    Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
+    GBN_TMA_FWD_GEOMS(GBN_T_LN)
     GBN_FWD_GEOMS(GBN_X_LN)
-    Variant{"elem", (const void *)&fwd_elem<GBN_T, true>, kElemCTA, 0, 1, 1, kElemCTA, 1}};
+    Variant{"elem", (const void *)&fwd_elem<GBN_T, true>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 const VariantTable GBN_CAT(kFwdRms_, GBN_SFX) = {rms_variants, (int)(sizeof(rms_variants) / sizeof(Variant))};
 const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_variants) / sizeof(Variant))};
+#undef GBN_ROW
+#undef GBN_X_RMS
+#undef GBN_X_LN
+#undef GBN_TMA
+#undef GBN_T_RMS
+#undef GBN_T_LN
 #endif
 
 #ifdef GBN_BWD
 #define GBN_ROW(LN, TPR, VPT, R, CL, CTA)                                                     \
     Variant{GBN_VNAME(TPR, VPT, R, CL, CTA), (const void *)&bwd_rows<GBN_T, LN, TPR, VPT, R, CL, CTA>, \
-            TPR, VPT, R, CL, CTA, VecTraits<GBN_T>::E},
+            kRows, TPR, VPT, R, CL, CTA, VecTraits<GBN_T>::E, 0, 0},
 #define GBN_X_RMS(TPR, VPT, R, CL, CTA) GBN_ROW(false, TPR, VPT, R, CL, CTA)
 #define GBN_X_LN(TPR, VPT, R, CL, CTA) GBN_ROW(true, TPR, VPT, R, CL, CTA)
+#define GBN_TMA(LN, TPR, VPT, CW)                                                              \
+    Variant{GBN_TMA_VNAME(TPR, VPT, CW), (const void *)&bwd_tma<GBN_T, LN, TPR, VPT, CW>, kTma, TPR, \
+            VPT, 0, 1, (CW + 1) * 32, VecTraits<GBN_T>::E, 1, 32768},
+#define GBN_T_RMS(TPR, VPT, CW) GBN_TMA(false, TPR, VPT, CW)
+#define GBN_T_LN(TPR, VPT, CW) GBN_TMA(true, TPR, VPT, CW)
 static const Variant rms_variants[] = {
+    GBN_TMA_BWD_GEOMS(GBN_T_RMS)
     GBN_BWD_GEOMS(GBN_X_RMS)
-    Variant{"elem", (const void *)&bwd_elem<GBN_T, false>, kElemCTA, 0, 1, 1, kElemCTA, 1}};
+    Variant{"elem", (const void *)&bwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
+    GBN_TMA_BWD_GEOMS(GBN_T_LN)
     GBN_BWD_GEOMS(GBN_X_LN)
-    Variant{"elem", (const void *)&bwd_elem<GBN_T, true>, kElemCTA, 0, 1, 1, kElemCTA, 1}};
+    Variant{"elem", (const void *)&bwd_elem<GBN_T, true>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 const VariantTable GBN_CAT(kBwdRms_, GBN_SFX) = {rms_variants, (int)(sizeof(rms_variants) / sizeof(Variant))};
 const VariantTable GBN_CAT(kBwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_variants) / sizeof(Variant))};
 #endif

@@ -9,6 +9,16 @@ namespace gbn {
 
 constexpr int kElemCTA = 256;  // threads per CTA of the element-wise kernels
 constexpr int kColCTA = 512;   // threads per CTA of the column-reduce kernel
+constexpr int kTmaHeaderBytes = 2048;  // TMA kernels: barriers, abort flag, reduction scratch
+constexpr int kTmaMaxStages = 8;       // TMA kernels: deepest shared-memory ring
+
+// Pipeline geometry of the TMA-staged kernels, chosen by the host per call.
+struct TileCfg {
+    int rows;          // rows per tile (one bulk copy per tensor per tile)
+    int stages;        // tiles in flight (shared-memory ring depth)
+    uint32_t stride;   // bytes between consecutive stages in shared memory
+    int *fault;        // device word set to nonzero if a bounded wait gives up
+};
 
 struct FwdParams {
     const void *x;      // [M, N] T
@@ -19,6 +29,7 @@ struct FwdParams {
     float *rstd;        // [M] or null
     int64_t M, N;
     float eps;
+    TileCfg tc;         // used by the TMA-staged kernels only
 };
 
 struct BwdParams {
@@ -30,24 +41,34 @@ struct BwdParams {
     void *dx;           // [M, N] T
     float *ws;          // [2][P][N] float partial rows (second block: dbeta)
     int64_t M, N;
+    TileCfg tc;         // used by the TMA-staged kernels only
+};
+
+enum VariantKind : int {
+    kRows = 0,  // row-resident registers, plain 16-byte loads
+    kElem = 1,  // element-wise, any N and alignment
+    kTma = 2,   // rows staged through a shared-memory ring by bulk async copies
 };
 
 // One compiled kernel and the geometry the host needs to launch it.
 struct Variant {
     const char *name;
     const void *kernel;  // __global__ entry (takes FwdParams or BwdParams by value)
+    int kind;            // VariantKind
     int tpr;             // threads per row group (within one CTA)
-    int vpt;             // 16-byte vectors per thread per row (0: element-wise kernel)
-    int rows;            // rows each row group handles per iteration
+    int vpt;             // 16-byte vectors per thread per row (max)
+    int rows;            // rows each row group handles per iteration (kRows)
     int cl;              // CTAs per row (thread-block cluster size)
     int cta;             // threads per CTA
     int elems_per_vec;   // E (16 bytes / sizeof(T)); 1 for element-wise kernels
+    int ctas_per_sm;     // kTma: CTAs meant to share an SM (shared-memory budget split)
+    int stage_target;    // kTma: bytes of one stage the host aims for
 
     // Longest row (elements) this variant can hold.
     int64_t max_n() const {
-        return vpt == 0 ? INT64_MAX : (int64_t)tpr * vpt * cl * elems_per_vec;
+        return kind == kElem ? INT64_MAX : (int64_t)tpr * vpt * cl * elems_per_vec;
     }
-    int rows_per_cta_iter() const { return vpt == 0 ? 1 : (cta / tpr) * rows; }
+    int rows_per_cta_iter() const { return kind == kRows ? (cta / tpr) * rows : 1; }
 };
 
 struct VariantTable {

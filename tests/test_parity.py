@@ -32,8 +32,24 @@ def test_small_shapes(op, dtype, N):
 
 
 def _geom(name):
+    """(tpr, vpt, rows, cluster, cta, is_tma) of a vector variant, None for 'elem'."""
     m = re.fullmatch(r"(\d+)x(\d+)r(\d+)c(\d+)b(\d+)", name)
-    return tuple(int(v) for v in m.groups()) if m else None
+    if m:
+        return tuple(int(v) for v in m.groups()) + (False,)
+    m = re.fullmatch(r"tma(\d+)x(\d+)w(\d+)", name)
+    if m:
+        tpr, vpt, cw = (int(v) for v in m.groups())
+        return (tpr, vpt, 1, 1, cw * 32, True)
+    return None
+
+
+@pytest.fixture(autouse=True)
+def _no_device_fault():
+    """Every test must leave the device fault word clear (no bounded wait gave up)."""
+    import rmsnorm_norm_fwd_gb300 as g
+    g.read_fault(reset=True)
+    yield
+    assert g.read_fault(reset=True) == 0, "a kernel's bounded wait timed out"
 
 
 def _variant_cases():
@@ -70,13 +86,27 @@ def test_forced_variant(op, direction, dtype, variant):
     if geo is None:  # the element-wise variant: odd N
         shapes = [(67, 1), (67, 77), (5, 3001)]
     else:
-        tpr, vpt, r, cl, cta = geo
+        tpr, vpt, r, cl, cta, tma = geo
         cap = tpr * vpt * cl * E
-        rows_per_iter = r if cl > 1 else (cta // tpr) * r
-        M = min(2 * rows_per_iter + 3, max(3, (1 << 21) // cap))
+        if tma:
+            # several tiles, a ragged last tile (not a multiple of 4 rows)
+            M = max(7, min(1000, (3 << 20) // (cap * (4 if dtype == "fp32" else 2))) | 3)
+        else:
+            rows_per_iter = r if cl > 1 else (cta // tpr) * r
+            M = min(2 * rows_per_iter + 3, max(3, (1 << 21) // cap))
         shapes = [(M, cap), (M, cap - E)]
     try:
         g.force_variant(op == "ln", direction, dtype, variant)
+        if geo is not None and geo[5]:
+            # A staged variant may hold fewer elements than its register
+            # capacity when gamma/beta and two stages must fit in shared
+            # memory: take the widest row it serves, at least a quarter of it.
+            M, cap = shapes[0]
+            n = cap
+            while n >= cap // 4 and g.variant_name(op == "ln", direction, M, n, dtype) != variant:
+                n //= 2
+            assert n >= cap // 4, f"{variant} serves no row of {cap // 4}..{cap} elements"
+            shapes = [(M, n), (M, n - E)]
         for (M, N) in shapes:
             assert g.variant_name(op == "ln", direction, M, N, dtype, aligned=(geo is not None)) == variant
             rep, _, _ = run_case(op, dtype, M, N, dist="llm")
@@ -182,3 +212,59 @@ def test_degenerate_rows():
             inp.x[1::4] = 1.5
             out = gpu_run(op, inp)
             compare(op, inp, out).assert_ok()
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("direction", [0, 1])
+@pytest.mark.parametrize("N", [256, 2048, 8192])
+@pytest.mark.parametrize("limit", [1, 3])
+def test_tma_ring_wraps(op, direction, N, limit):
+    """A capped grid makes each CTA walk many more tiles than the ring has
+    stages, so every stage's barriers go through several phases."""
+    import rmsnorm_norm_fwd_gb300 as g
+    M = 4099 if N <= 2048 else 517
+    name = g.variant_name(op == "ln", direction, M, N, "bf16")
+    assert name.startswith("tma"), name
+    try:
+        g.set_grid_limit(limit)
+        rep, _, _ = run_case(op, "bf16", M, N)
+        rep.assert_ok()
+    finally:
+        g.set_grid_limit(0)
+
+
+def test_grid_limit_changes_nothing():
+    import rmsnorm_norm_fwd_gb300 as g
+    inp = make_inputs(3001, 768, op="ln", dist="ln")
+    a = gpu_run("ln", inp)
+    try:
+        g.set_grid_limit(5)
+        b = gpu_run("ln", inp)
+    finally:
+        g.set_grid_limit(0)
+    for k in ("y", "mean", "rstd", "dx"):
+        assert torch.equal(a[k], b[k]), k
+    # dgamma/dbeta are summed in a different grouping: equal within tolerance
+    for k in ("dgamma", "dbeta"):
+        assert torch.allclose(a[k], b[k], rtol=1e-5, atol=1e-4), k
+
+
+def test_unaligned_stats_fall_back_from_tma():
+    """rstd/mean not 16-byte aligned: the backward must not use the bulk-copy
+    kernels (which copy them in 16-byte units) and must still be right."""
+    import rmsnorm_norm_fwd_gb300 as g
+    M, N = 1029, 1024
+    inp = make_inputs(M, N, op="ln", dist="ln")
+    x, dy = inp.x.cuda(), inp.dy.cuda()
+    gam, bet = inp.gamma.cuda(), inp.beta.cuda()
+    y, mean, rstd = g.layernorm_fwd(x, gam, bet, inp.eps)
+    mb = torch.empty(M + 1, device="cuda")
+    rb = torch.empty(M + 1, device="cuda")
+    mean_u, rstd_u = mb[1:], rb[1:]
+    mean_u.copy_(mean)
+    rstd_u.copy_(rstd)
+    assert rstd_u.data_ptr() % 16 != 0
+    dx, dg, db = g.layernorm_bwd(dy, x, gam, mean_u, rstd_u)
+    torch.cuda.synchronize()
+    out = {"y": y, "mean": mean, "rstd": rstd, "dx": dx, "dgamma": dg, "dbeta": db}
+    compare("ln", inp, out).assert_ok()
