@@ -385,6 +385,54 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """One call shape of the workload, repeated: for profiling a single kernel
+    (e.g. under ncu -k).  Prints one JSON line with the median CUDA-event time."""
+    import rmsnorm_norm_fwd_gb300 as gb
+    op, d, n = args.case.split(":")
+    n, ln, bwd = int(n), op == "ln", d == "bwd"
+    m = args.rows or M
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = make_inputs(m, n, dtype="bf16", dist="ln" if ln else "rms", op=op)
+    x, dy, g, b = (t.to(dev) for t in (inp.x, inp.dy, inp.gamma, inp.beta))
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    mean, rstd = torch.empty(m, device=dev), torch.empty(m, device=dev)
+    dg, db = torch.empty(n, device=dev), torch.empty(n, device=dev)
+    ws = torch.empty(gb.norm_bwd_workspace_size(ln, m, n, torch.bfloat16), device=dev, dtype=torch.uint8)
+
+    def fwd():
+        if ln:
+            gb.layernorm_fwd(x, g, b, inp.eps, y=y, mean=mean, rstd=rstd)
+        else:
+            gb.rmsnorm_fwd(x, g, inp.eps, y=y, rstd=rstd)
+
+    def bwd_():
+        if ln:
+            gb.layernorm_bwd(dy, x, g, mean, rstd, dx=dx, dgamma=dg, dbeta=db, workspace=ws)
+        else:
+            gb.rmsnorm_bwd(dy, x, g, rstd, dx=dx, dgamma=dg, workspace=ws)
+
+    fwd()
+    call = bwd_ if bwd else fwd
+    for _ in range(args.warmup):
+        call()
+    stream = torch.cuda.current_stream(dev)
+    ts = []
+    for _ in range(args.steps):
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        ts.append(a.elapsed_time(e))
+    ms = statistics.median(ts)
+    nbytes = (bwd_bytes(m, n) if bwd else fwd_bytes(m, n)) if not ln else (
+        3 * m * n * B + n * B + 8 * m + 8 * n if bwd else 2 * m * n * B + 2 * n * B + 8 * m)
+    print(json.dumps({"case": args.case, "M": m, "N": n, "variant": gb.variant_name(ln, int(bwd), m, n, torch.bfloat16),
+                      "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "l2": "not flushed"}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,7 +442,13 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", help="op:dir:N (e.g. rms:bwd:2048): time one call shape of bf16 rows "
+                                   "only, for profiling one kernel")
+    ap.add_argument("--rows", type=int, default=0, help="rows for --case (default 65536)")
     args = ap.parse_args(argv)
+    if args.case:
+        run_case(args)
+        return
     args.warmup = max(3, args.warmup)
 
     ws, rank, local = dist_env()
