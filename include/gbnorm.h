@@ -141,6 +141,40 @@ int layernorm_bwd(const void *dy, const void *x, const void *gamma, const float 
                   size_t workspace_bytes, int64_t M, int64_t N, int dtype,
                   gbnorm_stream_t stream);
 
+/*
+ * RMSNorm backward without a caller-provided workspace.
+ *
+ * No counterpart on the pages: this entry point exists for callers that cannot
+ * allocate device memory at the point where they run the backward -- for
+ * example code inside a framework's allocator or memory-pool callback (which
+ * must not re-enter the allocator), a plugin whose enqueue function runs
+ * under a fixed memory budget, or a runtime that forbids cudaMalloc on its
+ * hot path because it synchronises the device.  It allocates nothing: it calls
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Arguments, layout and results are those of rmsnorm_bwd minus the workspace.
+ * The dgamma partial rows go to a fixed scratch array of
+ * GBNORM_NOALLOC_SCRATCH_BYTES inside the library, one per device, reserved
+ * when the library's device code is loaded on that device and held until the
+ * process exits.  A shape whose partial rows need more than that
+ * (norm_bwd_workspace_size(0, M, N, dtype) > GBNORM_NOALLOC_SCRATCH_BYTES) is
+ * refused with GBNORM_ERR_WORKSPACE before anything is enqueued.
+ *
+ * All calls on a device share that one scratch array, which keeps the last
+ * call's contents (the kernels overwrite every entry they read, so nothing
+ * needs clearing).  Two calls whose work overlaps on the GPU -- on different
+ * streams, or from different host threads -- race on it and give wrong
+ * dgamma; serialise them.
+ *
+ * The first call on each device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.
+ */
+#define GBNORM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int rmsnorm_bwd_noalloc(const void *dy, const void *x, const void *gamma, const float *rstd,
+                        void *dx, float *dgamma, int64_t M, int64_t N, int dtype,
+                        gbnorm_stream_t stream);
+
 /* Static, human-readable text for a status code. */
 const char *gbnorm_status_string(int status);
 
