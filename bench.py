@@ -9,7 +9,7 @@ value = algorithmic bytes of every timed call / summed CUDA-event time of
 those calls.  Algorithmic bytes per call (b = 2 for bf16):
     forward  : 2 M N b + N b + 4 M          (x, y, gamma, rstd)
     backward : 3 M N b + N b + 4 M + 4 N    (dy, x, dx, gamma, rstd, dgamma)
-Workspace traffic counts as time, never as bytes.  L2 is flushed (a 256 MiB
+Workspace traffic counts as time, never as bytes.  L2 is flushed (a 1 GiB
 write, outside the events) before every timed call.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -42,7 +42,10 @@ B = 2  # bf16
 METRIC = "norm fwd/bwd effective HBM GB/s and % of GB300 peak, per (M,N,dtype)"
 WORKLOAD = ("RMSNorm fwd+bwd sweep, M=65536 rows, N in {256,384,512,768,1024,2048}, "
             "bf16 tensors, fp32 rstd and dgamma, eps=1e-6")
-L2_FLUSH_BYTES = 256 << 20
+# A 1 GiB write before every timed call: flushes the 129 MB L2 and keeps the GPU
+# busy long enough that the host has queued the timed call before the GPU
+# reaches its start event (otherwise host launch time would be timed too).
+L2_FLUSH_BYTES = 1 << 30
 
 # Measured DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # roofline kernel, from the ncu capture summarised under profiles/, valid only
@@ -366,7 +369,7 @@ def run_ours(args, ws, rank, local):
             "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "N": list(NS), "io_dtype": "bf16",
-                       "l2": "flushed before every timed call (256 MiB write outside the events)",
+                       "l2": "flushed before every timed call (1 GiB write outside the events)",
                        "timing": "CUDA events on the launching stream around each C-ABI call"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,

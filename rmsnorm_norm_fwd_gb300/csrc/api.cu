@@ -58,6 +58,9 @@ std::mutex g_dev_mu;
 // the kernel's dynamic shared-memory limit has been raised.
 std::atomic<int> g_occ[kMaxDev][2][2][3][kMaxVariants];
 std::atomic<int> g_smem_set[kMaxDev][2][2][3][kMaxVariants];
+// TMA variants: the last (dynamic shared memory, occupancy) pair asked for,
+// packed as (bytes << 16) | blocks; their footprint depends on the shape.
+std::atomic<uint64_t> g_occ_tma[kMaxDev][2][2][3][kMaxVariants];
 
 // Forced variant per (is_ln, dir, dtype): index + 1, 0 = none.
 std::atomic<int> g_force[2][2][3];
@@ -164,23 +167,55 @@ int find_variant(const VariantTable &t, const char *name) {
     return -1;
 }
 
+// The dispatch table resolved once to variant indices, per (is_ln, dir, dtype):
+// the rows that apply, in table order, and the element-wise fallback.
+constexpr int kMaxRows = sizeof(kDispatch) / sizeof(kDispatch[0]);
+struct Resolved {
+    int n = 0;
+    int64_t nv_max[kMaxRows];
+    int idx[kMaxRows];
+    int elem = -1;
+};
+struct ResolvedAll {
+    Resolved r[2][2][3];
+    ResolvedAll() {
+        for (int ln = 0; ln < 2; ++ln)
+            for (int dir = 0; dir < 2; ++dir)
+                for (int dt = 0; dt < 3; ++dt) {
+                    Resolved &o = r[ln][dir][dt];
+                    const VariantTable &t = *kTables[ln][dir][dt];
+                    o.elem = find_variant(t, "elem");
+                    for (const DispatchRow &row : kDispatch) {
+                        if ((row.is_ln >= 0 && row.is_ln != ln) || row.dir != dir ||
+                            (row.dtype >= 0 && row.dtype != dt))
+                            continue;
+                        const int i = find_variant(t, row.variant);
+                        if (i < 0) continue;
+                        o.nv_max[o.n] = row.nv_max;
+                        o.idx[o.n] = i;
+                        ++o.n;
+                    }
+                }
+    }
+};
+const Resolved &resolved(int ln, int dir, int dt) {
+    static const ResolvedAll all;  // built on first use (thread-safe)
+    return all.r[ln][dir][dt];
+}
+
 // Index of the variant that serves this call.
 int select_variant(const CallShape &c, int dev) {
     const VariantTable &t = *kTables[c.is_ln][c.dir][c.dtype];
     const int forced = g_force[c.is_ln][c.dir][c.dtype].load(std::memory_order_relaxed) - 1;
     if (forced >= 0 && forced < t.count && can_serve(t.v[forced], c, dev)) return forced;
-    const int elem = find_variant(t, "elem");
-    if (!c.vec) return elem;
-    const int E = 16 / elem_size(c.dtype);
-    const int64_t nv = c.N / E;
-    for (const DispatchRow &r : kDispatch) {
-        if ((r.is_ln >= 0 && r.is_ln != c.is_ln) || r.dir != c.dir || (r.dtype >= 0 && r.dtype != c.dtype))
-            continue;
-        if (nv > r.nv_max) continue;
-        const int i = find_variant(t, r.variant);
-        if (i >= 0 && can_serve(t.v[i], c, dev)) return i;
+    const Resolved &r = resolved(c.is_ln, c.dir, c.dtype);
+    if (!c.vec) return r.elem;
+    const int64_t nv = c.N / (16 / elem_size(c.dtype));
+    for (int k = 0; k < r.n; ++k) {
+        if (nv > r.nv_max[k]) continue;
+        if (can_serve(t.v[r.idx[k]], c, dev)) return r.idx[k];
     }
-    return elem;
+    return r.elem;
 }
 
 struct Plan {
@@ -202,6 +237,12 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
         return GBNORM_OK;
     }
     if (v.kind == kTma) {
+        std::atomic<uint64_t> &cache = g_occ_tma[dev][c.is_ln][c.dir][c.dtype][idx];
+        const uint64_t hit = cache.load(std::memory_order_relaxed);
+        if (hit != 0 && (hit >> 16) == (uint64_t)dyn_smem) {
+            *out = (int)(hit & 0xffff);
+            return GBNORM_OK;
+        }
         std::atomic<int> &set = g_smem_set[dev][c.is_ln][c.dir][c.dtype][idx];
         if (!set.load(std::memory_order_acquire)) {
             const int lim = g_dev[dev].smem_optin / v.ctas_per_sm;
@@ -212,6 +253,7 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
         }
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.kernel, v.cta, dyn_smem) != cudaSuccess)
             return GBNORM_ERR_CUDA;
+        if (o > 0 && o < 0xffff) cache.store(((uint64_t)dyn_smem << 16) | (uint64_t)o, std::memory_order_relaxed);
     } else if (v.cl == 1) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.kernel, v.cta, 0) != cudaSuccess)
             return GBNORM_ERR_CUDA;
@@ -428,8 +470,20 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
     const dim3 grid2((unsigned)((N + cols_per_cta - 1) / cols_per_cta), is_ln ? 2u : 1u);
     const float *wsc = static_cast<const float *>(ws);
     void *args[5] = {&wsc, &P, &N, &dgamma, &dbeta};
-    if (cudaLaunchKernel(v4 ? kColReduceVec4 : kColReduceScalar, grid2, dim3(kColCTA), args, 0, stream) !=
-        cudaSuccess)
+    // Programmatic stream serialization: the column reduce may be scheduled
+    // while the row kernel drains; it waits (griddepcontrol.wait) for that
+    // grid's completion before reading the workspace.
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid2;
+    cfg.blockDim = dim3(kColCTA);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = M > 0 ? 1 : 0;
+    if (cudaLaunchKernelExC(&cfg, v4 ? kColReduceVec4 : kColReduceScalar, args) != cudaSuccess)
         return GBNORM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GBNORM_OK : GBNORM_ERR_CUDA;
 }

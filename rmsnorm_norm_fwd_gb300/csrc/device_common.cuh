@@ -191,6 +191,18 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
     return v;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the
+// stream (launched with programmatic stream serialization) start its CTAs
+// early; wait_primary, in that next kernel, blocks until the previous grid
+// has completed and its memory writes are visible.  Both are hardware
+// operations (no polling loop).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

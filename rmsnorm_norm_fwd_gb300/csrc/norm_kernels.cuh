@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
 template <typename T, bool LN, int TPR, int VPT, int R, int CL, int CTA>
 __global__ void __launch_bounds__(CTA) bwd_rows(const BwdParams p) {
     static_assert(CTA % TPR == 0 && (TPR <= 32 || TPR % 32 == 0), "bad row-group shape");
+    pdl_launch_dependents();  // the column reduce waits for this grid's completion
     static_assert(CL == 1 || TPR == CTA, "a cluster row uses whole CTAs");
     constexpr int E = VecTraits<T>::E;
     constexpr int RPC = CTA / TPR;
@@ -336,6 +337,7 @@ __global__ void __launch_bounds__(kElemCTA) fwd_elem(const FwdParams p) {
 // of the workspace (no other CTA touches it), zeroed first.
 template <typename T, bool LN>
 __global__ void __launch_bounds__(kElemCTA) bwd_elem(const BwdParams p) {
+    pdl_launch_dependents();  // the column reduce waits for this grid's completion
     __shared__ float red[2 * 2 * (kElemCTA / 32)];
     const T *x = static_cast<const T *>(p.x);
     const T *dy = static_cast<const T *>(p.dy);
@@ -387,6 +389,8 @@ __global__ void __launch_bounds__(kColCTA) colreduce(const float *ws, int64_t P,
                                                      float *out0, float *out1) {
     constexpr int W = kColCTA / 32;
     __shared__ float part[W][32 * VW];
+    // Launched right behind the backward row kernel that writes `ws`.
+    pdl_wait_primary();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float *src = ws + (int64_t)blockIdx.y * P * N;
     float *out = blockIdx.y ? out1 : out0;

@@ -245,11 +245,13 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
 // ============================================================================ backward
 template <typename T, bool LN, int TPR, int VPT, int CW>
 __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
+    pdl_launch_dependents();  // the column reduce waits for this grid's completion
     constexpr int E = VecTraits<T>::E;
     constexpr int NT = CW * 32;
     constexpr int RPP = NT / TPR;
     constexpr int WPR = TPR > 32 ? TPR / 32 : 1;
     constexpr int NS = LN ? 2 : 1;
+    constexpr bool HOLD = VPT * E <= 16;  // keep pass-1 values in registers for pass 2
     static_assert(NT % TPR == 0 && (TPR <= 32 || TPR % 32 == 0), "row group shape");
     static_assert(TPR <= 32 || (RPP * 2 * NS * WPR <= (int)(sizeof(TmaHeader::red) / 4) && RPP <= 14),
                   "scratch / named barrier ids");
@@ -317,18 +319,31 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
                 rstd = in_win ? st[row] : __ldg(p.rstd + row);
                 if constexpr (LN) mean = in_win ? st[stat_stride(RT) + row] : __ldg(p.mean + row);
             }
+            // Pass 1: x-hat and g = dy * gamma, their products summed over the
+            // row.  With at most 16 elements per thread (HOLD) x-hat, g and the
+            // raw dy stay in registers for pass 2; otherwise pass 2 re-reads the
+            // staged row.
             float sum[NS];
 #pragma unroll
             for (int i = 0; i < NS; ++i) sum[i] = 0.f;
+            float hx[HOLD ? VPT : 1][E], hg[HOLD ? VPT : 1][E];
+            uint4 hd[HOLD ? VPT : 1];
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * TPR + t;
-                if (!rok || v >= nv) continue;
-                const uint4 q = lds128(xs + v), d = lds128(ds + v), g = lds128(gs + v);
+                const bool ok = rok && v < nv;
+                const uint4 q = ok ? lds128(xs + v) : make_uint4(0, 0, 0, 0);
+                const uint4 d = ok ? lds128(ds + v) : make_uint4(0, 0, 0, 0);
+                const uint4 g = ok ? lds128(gs + v) : make_uint4(0, 0, 0, 0);
+                if constexpr (HOLD) hd[k] = d;
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const float xh = (vget<T>(q, e) - mean) * rstd;
                     const float gg = vget<T>(d, e) * vget<T>(g, e);
+                    if constexpr (HOLD) {
+                        hx[k][e] = xh;
+                        hg[k][e] = gg;
+                    }
                     sum[0] += gg * xh;
                     if constexpr (LN) sum[NS - 1] += gg;
                 }
@@ -341,16 +356,26 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * TPR + t;
                 if (v >= nv) continue;
-                const uint4 q = lds128(xs + v), d = lds128(ds + v), g = lds128(gs + v);
                 float o[E];
+                if constexpr (HOLD) {
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float xh = (vget<T>(q, e) - mean) * rstd;
-                    const float dyv = vget<T>(d, e);
-                    const float gg = dyv * vget<T>(g, e);
-                    o[e] = rstd * (gg - c1 - xh * c2);
-                    accg[k][e] += dyv * xh;
-                    if constexpr (LN) accb[k][e] += dyv;
+                    for (int e = 0; e < E; ++e) {
+                        const float dyv = vget<T>(hd[k], e);
+                        o[e] = rstd * (hg[k][e] - c1 - hx[k][e] * c2);
+                        accg[k][e] += dyv * hx[k][e];
+                        if constexpr (LN) accb[k][e] += dyv;
+                    }
+                } else {
+                    const uint4 q = lds128(xs + v), d = lds128(ds + v), g = lds128(gs + v);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float xh = (vget<T>(q, e) - mean) * rstd;
+                        const float dyv = vget<T>(d, e);
+                        const float gg = dyv * vget<T>(g, e);
+                        o[e] = rstd * (gg - c1 - xh * c2);
+                        accg[k][e] += dyv * xh;
+                        if constexpr (LN) accb[k][e] += dyv;
+                    }
                 }
                 st_vec(p.dx, row * nv + v, vpack<T>(o));
             }

@@ -46,7 +46,7 @@ def sweep(reps: int, only=None):
     import rmsnorm_norm_fwd_gb300 as g
     dt_t = {"fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16}
     dev = torch.device("cuda")
-    scrub = torch.empty(256 << 20, device=dev, dtype=torch.uint8)
+    scrub = torch.empty(1 << 30, device=dev, dtype=torch.uint8)  # flushes L2, covers host launch time
     stream = torch.cuda.current_stream()
     out = []
     for op, dt, M, N in SHAPES:
