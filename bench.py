@@ -10,7 +10,8 @@ those calls.  Algorithmic bytes per call (b = 2 for bf16):
     forward  : 2 M N b + N b + 4 M          (x, y, gamma, rstd)
     backward : 3 M N b + N b + 4 M + 4 N    (dy, x, dx, gamma, rstd, dgamma)
 Workspace traffic counts as time, never as bytes.  L2 is flushed (a 1 GiB
-write, outside the events) before every timed call.
+write, then a 512 MiB read so the lines left are clean; outside the events)
+before every timed call.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs the same per-GPU workload (weak
@@ -42,10 +43,13 @@ B = 2  # bf16
 METRIC = "norm fwd/bwd effective HBM GB/s and % of GB300 peak, per (M,N,dtype)"
 WORKLOAD = ("RMSNorm fwd+bwd sweep, M=65536 rows, N in {256,384,512,768,1024,2048}, "
             "bf16 tensors, fp32 rstd and dgamma, eps=1e-6")
-# A 1 GiB write before every timed call: flushes the 129 MB L2 and keeps the GPU
-# busy long enough that the host has queued the timed call before the GPU
-# reaches its start event (otherwise host launch time would be timed too).
+# Before every timed call: a 1 GiB write (flushes the 129 MB L2 and keeps the
+# GPU busy long enough that the host has queued the timed call before the GPU
+# reaches its start event), then a 512 MiB read, so that L2 holds clean lines
+# of an unrelated buffer instead of dirty ones whose write-back would land in
+# the timed call.
 L2_FLUSH_BYTES = 1 << 30
+L2_CLEAN_BYTES = 512 << 20
 
 # Measured DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # roofline kernel, from the ncu capture summarised under profiles/, valid only
@@ -242,7 +246,12 @@ def run_ours(args, ws, rank, local):
                               dtype=torch.uint8)
         d["host"] = inp
         data.append(d)
-    scrub = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    scrub_w = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    scrub_r = torch.ones(L2_CLEAN_BYTES // 4, device=dev, dtype=torch.float32)
+
+    def flush_l2():
+        scrub_w.zero_()
+        scrub_r.amax()
 
     def call_fwd(d):
         gb.rmsnorm_fwd(d["x"], d["gamma"], EPS, y=d["y"], rstd=d["rstd"])
@@ -253,12 +262,12 @@ def run_ours(args, ws, rank, local):
 
     def one_step(record):
         for d in data:
-            scrub.zero_()
+            flush_l2()
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e0.record(stream)
             call_fwd(d)
             e1.record(stream)
-            scrub.zero_()
+            flush_l2()
             e1b = torch.cuda.Event(enable_timing=True)
             e1b.record(stream)
             call_bwd(d)
@@ -369,7 +378,7 @@ def run_ours(args, ws, rank, local):
             "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "N": list(NS), "io_dtype": "bf16",
-                       "l2": "flushed before every timed call (1 GiB write outside the events)",
+                       "l2": "flushed before every timed call: 1 GiB write then 512 MiB read, outside the events",
                        "timing": "CUDA events on the launching stream around each C-ABI call"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
@@ -416,6 +425,8 @@ def run_case(args):
         else:
             gb.rmsnorm_bwd(dy, x, g, rstd, dx=dx, dgamma=dg, workspace=ws)
 
+    if args.variant:
+        gb.force_variant(ln, int(bwd), torch.bfloat16, args.variant)
     fwd()
     call = bwd_ if bwd else fwd
     for _ in range(args.warmup):
@@ -448,6 +459,7 @@ def main(argv=None):
     ap.add_argument("--case", help="op:dir:N (e.g. rms:bwd:2048): time one call shape of bf16 rows "
                                    "only, for profiling one kernel")
     ap.add_argument("--rows", type=int, default=0, help="rows for --case (default 65536)")
+    ap.add_argument("--variant", help="with --case: force this kernel variant (profiling)")
     args = ap.parse_args(argv)
     if args.case:
         run_case(args)

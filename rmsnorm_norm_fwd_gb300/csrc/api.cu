@@ -135,7 +135,7 @@ bool tma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, si
     if (stages > kTmaMaxStages) stages = kTmaMaxStages;
     size_t ring = (size_t)stages * stride;
     // The backward combines its row groups' partials in the idle ring.
-    const int rpp = (v.cta - 32) / v.tpr;
+    const int rpp = v.consumers() / v.tpr;
     if (c.dir == 1 && rpp > 1) {
         const size_t comb = (size_t)v.tpr * v.vpt * v.elems_per_vec * 4 * (c.is_ln ? 2 : 1);
         if (comb > ring) ring = comb;
@@ -149,14 +149,40 @@ bool tma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, si
     return true;
 }
 
+// Geometry of a cluster TMA variant: each of the CL CTAs stages one column
+// slice of one row per stage.  False if a slice exceeds the variant's
+// per-thread capacity, a CTA would get no columns, or two stages do not fit.
+bool tmac_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, size_t *dyn_smem) {
+    auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
+    const int64_t nv = c.N / (16 / elem_size(c.dtype));
+    const int64_t slice = (nv + v.cl - 1) / v.cl;
+    if (slice > (int64_t)v.tpr * v.vpt || (int64_t)(v.cl - 1) * slice >= nv) return false;
+    const size_t slice_al = al((size_t)slice * 16);
+    const size_t params = slice_al * ((c.dir == 0 && c.is_ln) ? 2 : 1);
+    const size_t stride = (c.dir == 0 ? 1 : 2) * slice_al + (c.dir == 1 ? 128 : 0);
+    const size_t optin = (size_t)g_dev[dev].smem_optin;
+    if (optin <= (size_t)kTmaHeaderBytes + params + 2 * stride) return false;
+    int stages = (int)((optin - kTmaHeaderBytes - params) / stride);
+    if (stages > kTmaMaxStages) stages = kTmaMaxStages;
+    // The consumers hold the rows of two exchange steps (2 * RS stages) at
+    // once; a shallower ring could never refill.
+    if (stages < 2 * v.rows) return false;
+    tc->rows = 1;
+    tc->stages = stages;
+    tc->stride = (uint32_t)stride;
+    tc->fault = g_dev[dev].fault;
+    *dyn_smem = kTmaHeaderBytes + params + (size_t)stages * stride;
+    return true;
+}
+
 bool can_serve(const Variant &v, const CallShape &c, int dev) {
     if (v.kind == kElem) return true;
     if (!c.vec || c.N > v.max_n()) return false;
-    if (v.kind == kTma) {
+    if (v.kind == kTma || v.kind == kTmaCl) {
         if (c.dir == 1 && !c.stats) return false;
         TileCfg tc;
         size_t dyn;
-        return tma_geometry(v, c, dev, &tc, &dyn);
+        return v.kind == kTma ? tma_geometry(v, c, dev, &tc, &dyn) : tmac_geometry(v, c, dev, &tc, &dyn);
     }
     return true;
 }
@@ -236,7 +262,7 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
         *out = o;
         return GBNORM_OK;
     }
-    if (v.kind == kTma) {
+    if (v.kind == kTma || v.kind == kTmaCl) {
         std::atomic<uint64_t> &cache = g_occ_tma[dev][c.is_ln][c.dir][c.dtype][idx];
         const uint64_t hit = cache.load(std::memory_order_relaxed);
         if (hit != 0 && (hit >> 16) == (uint64_t)dyn_smem) {
@@ -249,10 +275,29 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
             if (cudaFuncSetAttribute(v.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim) !=
                 cudaSuccess)
                 return GBNORM_ERR_CUDA;
+            if (v.cl > 8 &&
+                cudaFuncSetAttribute(v.kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                    cudaSuccess)
+                return GBNORM_ERR_CUDA;
             set.store(1, std::memory_order_release);
         }
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.kernel, v.cta, dyn_smem) != cudaSuccess)
-            return GBNORM_ERR_CUDA;
+        if (v.kind == kTma) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.kernel, v.cta, dyn_smem) != cudaSuccess)
+                return GBNORM_ERR_CUDA;
+        } else {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = v.cl;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(v.cl * g_dev[dev].sms);
+            cfg.blockDim = dim3(v.cta);
+            cfg.dynamicSmemBytes = dyn_smem;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&o, v.kernel, &cfg) != cudaSuccess) return GBNORM_ERR_CUDA;
+        }
         if (o > 0 && o < 0xffff) cache.store(((uint64_t)dyn_smem << 16) | (uint64_t)o, std::memory_order_relaxed);
     } else if (v.cl == 1) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.kernel, v.cta, 0) != cudaSuccess)
@@ -288,6 +333,7 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
     pl->tc = TileCfg{0, 0, 0, g_dev[dev].fault};
     if (c.M <= 0) return GBNORM_OK;
     if (v.kind == kTma && !tma_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
+    if (v.kind == kTmaCl && !tmac_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     int occ = 0;
     int st = occupancy(c, idx, dev, pl->dyn_smem, &occ);
     if (st != GBNORM_OK) return st;
@@ -299,6 +345,18 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
         if (limit > 0 && limit < cap) cap = limit;
         pl->grid = c.M < cap ? c.M : cap;
         pl->P = pl->grid;
+        return GBNORM_OK;
+    }
+    if (v.kind == kTmaCl) {
+        // occ = clusters that fit on the GPU at once; one row per cluster at a time.
+        int64_t cap = occ;
+        if (limit > 0) {
+            const int64_t lc = limit / v.cl > 0 ? limit / v.cl : 1;
+            if (lc < cap) cap = lc;
+        }
+        const int64_t ncl = c.M < cap ? c.M : cap;
+        pl->grid = ncl * v.cl;
+        pl->P = ncl;
         return GBNORM_OK;
     }
     if (v.kind == kTma) {
@@ -320,6 +378,17 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
     pl->grid = n_units * v.cl;
     pl->P = n_units;
     return GBNORM_OK;
+}
+
+// Selected variant and its plan; if the GPU cannot host the selected variant
+// (e.g. no cluster of its size fits), the element-wise variant, which always
+// can.
+int plan_call(const CallShape &c, int dev, Plan *pl) {
+    const int idx = select_variant(c, dev);
+    int st = make_plan(c, idx, dev, pl);
+    const int elem = resolved(c.is_ln, c.dir, c.dtype).elem;
+    if (st == GBNORM_ERR_UNSUPPORTED && idx != elem) st = make_plan(c, elem, dev, pl);
+    return st;
 }
 
 int launch_kernel(const Variant &v, const Plan &pl, void *params, cudaStream_t s) {
@@ -404,7 +473,7 @@ int do_fwd(int is_ln, const void *x, const void *gamma, const void *beta, void *
     c.vec = (vec % 16) == 0 && aligned16(x) && aligned16(y) && aligned16(gamma) &&
             (!is_ln || aligned16(beta));
     Plan pl;
-    s = make_plan(c, select_variant(c, dev), dev, &pl);
+    s = plan_call(c, dev, &pl);
     if (s != GBNORM_OK) return s;
     FwdParams p{x, gamma, is_ln ? beta : nullptr, y, is_ln ? mean : nullptr, rstd, M, N, eps, pl.tc};
     return launch_kernel(kTables[is_ln][0][dtype]->v[pl.idx], pl, &p, stream);
@@ -421,7 +490,7 @@ size_t ws_bytes_for(int is_ln, int64_t M, int64_t N, int dtype, int dev, int *st
         if (f[0] && (N % E) != 0) continue;
         CallShape c{is_ln, 1, dtype, M, N, f[0], f[1]};
         Plan pl;
-        *status = make_plan(c, select_variant(c, dev), dev, &pl);
+        *status = plan_call(c, dev, &pl);
         if (*status != GBNORM_OK) return 0;
         const size_t need = (size_t)pl.P * (size_t)N * 4u * (is_ln ? 2u : 1u);
         if (need > best) best = need;
@@ -457,7 +526,7 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
         c.vec = (vec % 16) == 0 && aligned16(dy) && aligned16(x) && aligned16(dx) && aligned16(gamma);
         c.stats = aligned16(rstd) && (!is_ln || aligned16(mean));
         Plan pl;
-        s = make_plan(c, select_variant(c, dev), dev, &pl);
+        s = plan_call(c, dev, &pl);
         if (s != GBNORM_OK) return s;
         BwdParams p{dy, x, gamma, is_ln ? mean : nullptr, rstd, dx, static_cast<float *>(ws), M, N, pl.tc};
         s = launch_kernel(kTables[is_ln][1][dtype]->v[pl.idx], pl, &p, stream);
@@ -553,8 +622,10 @@ int gbnorm_variant_name(int is_layernorm, int dir, int64_t M, int64_t N, int dty
     if (s != GBNORM_OK) return s;
     const int E = 16 / elem_size(dtype);
     CallShape c{is_layernorm ? 1 : 0, dir, dtype, M, N, aligned && (N % E) == 0, aligned != 0};
-    const int idx = select_variant(c, dev);
-    std::snprintf(buf, len, "%s", kTables[c.is_ln][dir][dtype]->v[idx].name);
+    Plan pl;
+    const int st = plan_call(c, dev, &pl);
+    if (st != GBNORM_OK) return st;
+    std::snprintf(buf, len, "%s", kTables[c.is_ln][dir][dtype]->v[pl.idx].name);
     return GBNORM_OK;
 }
 

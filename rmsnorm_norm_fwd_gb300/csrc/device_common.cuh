@@ -203,6 +203,43 @@ __device__ __forceinline__ void pdl_wait_primary() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Arrive (release, cluster scope) on an mbarrier in another CTA of the
+// cluster; `remote` comes from map_to_rank.  Orders this thread's earlier
+// st.shared::cluster stores before the arrival.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
+                 : "memory");
+}
+// try_wait with cluster-scope acquire: after it succeeds, stores that peers
+// made before their release-arrive on this barrier are visible.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait on a cluster-exchange barrier; same abort protocol as
+// mbar_wait_bounded.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity,
+                                                          volatile int *abort, int *fault) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (*abort) return false;
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            if (fault) atomicExch(fault, 1);
+            return false;
+        }
+    }
+}
+
 // Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -3,6 +3,7 @@
 // name suffix) and exactly one of GBN_FWD / GBN_BWD.
 #include "norm_kernels.cuh"
 #include "tma_kernels.cuh"
+#include "tma_cluster_kernels.cuh"
 #include "variants.inc"
 
 namespace gbn {
@@ -21,12 +22,19 @@ namespace gbn {
             VPT, 0, 1, (CW + 1) * 32, VecTraits<GBN_T>::E, 1, 32768},
 #define GBN_T_RMS(TPR, VPT, CW) GBN_TMA(false, TPR, VPT, CW)
 #define GBN_T_LN(TPR, VPT, CW) GBN_TMA(true, TPR, VPT, CW)
+#define GBN_TMAC(LN, CL, VPT, RS)                                                              \
+    Variant{GBN_TMAC_VNAME(CL, VPT, RS), (const void *)&fwd_tmac<GBN_T, LN, VPT, CL, RS>, kTmaCl,  \
+            kTmacNT, VPT, RS, CL, (kTmacCW + 1) * 32, VecTraits<GBN_T>::E, 1, 0},
+#define GBN_C_RMS(CL, VPT, RS) GBN_TMAC(false, CL, VPT, RS)
+#define GBN_C_LN(CL, VPT, RS) GBN_TMAC(true, CL, VPT, RS)
 static const Variant rms_variants[] = {
     GBN_TMA_FWD_GEOMS(GBN_T_RMS)
+    GBN_TMAC_FWD_GEOMS(GBN_C_RMS)
     GBN_FWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
     GBN_TMA_FWD_GEOMS(GBN_T_LN)
+    GBN_TMAC_FWD_GEOMS(GBN_C_LN)
     GBN_FWD_GEOMS(GBN_X_LN)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, true>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 const VariantTable GBN_CAT(kFwdRms_, GBN_SFX) = {rms_variants, (int)(sizeof(rms_variants) / sizeof(Variant))};
@@ -37,6 +45,9 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_TMA
 #undef GBN_T_RMS
 #undef GBN_T_LN
+#undef GBN_TMAC
+#undef GBN_C_RMS
+#undef GBN_C_LN
 #endif
 
 #ifdef GBN_BWD
@@ -50,12 +61,19 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
             VPT, 0, 1, (CW + 1) * 32, VecTraits<GBN_T>::E, 1, 32768},
 #define GBN_T_RMS(TPR, VPT, CW) GBN_TMA(false, TPR, VPT, CW)
 #define GBN_T_LN(TPR, VPT, CW) GBN_TMA(true, TPR, VPT, CW)
+#define GBN_TMAC(LN, CL, VPT, RS)                                                              \
+    Variant{GBN_TMAC_VNAME(CL, VPT, RS), (const void *)&bwd_tmac<GBN_T, LN, VPT, CL, RS>, kTmaCl,  \
+            kTmacNT, VPT, RS, CL, (kTmacCW + 1) * 32, VecTraits<GBN_T>::E, 1, 0},
+#define GBN_C_RMS(CL, VPT, RS) GBN_TMAC(false, CL, VPT, RS)
+#define GBN_C_LN(CL, VPT, RS) GBN_TMAC(true, CL, VPT, RS)
 static const Variant rms_variants[] = {
     GBN_TMA_BWD_GEOMS(GBN_T_RMS)
+    GBN_TMAC_BWD_GEOMS(GBN_C_RMS)
     GBN_BWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&bwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
     GBN_TMA_BWD_GEOMS(GBN_T_LN)
+    GBN_TMAC_BWD_GEOMS(GBN_C_LN)
     GBN_BWD_GEOMS(GBN_X_LN)
     Variant{"elem", (const void *)&bwd_elem<GBN_T, true>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 const VariantTable GBN_CAT(kBwdRms_, GBN_SFX) = {rms_variants, (int)(sizeof(rms_variants) / sizeof(Variant))};

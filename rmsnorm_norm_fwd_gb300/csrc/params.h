@@ -48,6 +48,7 @@ enum VariantKind : int {
     kRows = 0,  // row-resident registers, plain 16-byte loads
     kElem = 1,  // element-wise, any N and alignment
     kTma = 2,   // rows staged through a shared-memory ring by bulk async copies
+    kTmaCl = 3, // as kTma, each row split across a thread-block cluster (column slices)
 };
 
 // One compiled kernel and the geometry the host needs to launch it.
@@ -57,7 +58,7 @@ struct Variant {
     int kind;            // VariantKind
     int tpr;             // threads per row group (within one CTA)
     int vpt;             // 16-byte vectors per thread per row (max)
-    int rows;            // rows each row group handles per iteration (kRows)
+    int rows;            // rows per row group per iteration (kRows); rows per exchange step (kTmaCl)
     int cl;              // CTAs per row (thread-block cluster size)
     int cta;             // threads per CTA
     int elems_per_vec;   // E (16 bytes / sizeof(T)); 1 for element-wise kernels
@@ -68,6 +69,8 @@ struct Variant {
     int64_t max_n() const {
         return kind == kElem ? INT64_MAX : (int64_t)tpr * vpt * cl * elems_per_vec;
     }
+    // Threads of a CTA that work on rows (TMA kinds add one producer warp).
+    int consumers() const { return (kind == kTma || kind == kTmaCl) ? cta - 32 : cta; }
     int rows_per_cta_iter() const { return kind == kRows ? (cta / tpr) * rows : 1; }
 };
 

@@ -35,8 +35,9 @@ constexpr int kTmaBarAll = 15;         // named barrier over all consumer thread
 struct TmaHeader {
     uint64_t full[kTmaMaxStages];
     uint64_t empty[kTmaMaxStages];
+    uint64_t pbar;  // gamma (and beta) landed in shared memory
     int abort;
-    int pad[3];
+    int pad;
     float red[(kTmaHeaderBytes - 16 * kTmaMaxStages - 16) / 4];  // row-group scratch
 };
 static_assert(sizeof(TmaHeader) == kTmaHeaderBytes, "header layout");
@@ -108,17 +109,14 @@ __device__ __forceinline__ void tma_produce(TmaHeader &h, unsigned char *stages,
     }
 }
 
-// Stages gamma (and beta) for the whole row in shared memory once per CTA:
-// every row reads them again, and registers are kept for the backward's
-// dgamma/dbeta partials.  Consumer threads only; ends with a consumer barrier.
-template <int NT>
-__device__ __forceinline__ void stage_params(uint4 *gdst, uint4 *bdst, const void *g, const void *b,
-                                             int64_t nv) {
-    for (int64_t i = threadIdx.x; i < nv; i += NT) {
-        gdst[i] = ld_vec(g, i);
-        if (b) bdst[i] = ld_vec(b, i);
-    }
-    named_sync(kTmaBarAll, NT);
+// gamma (and beta) for the whole row are brought into shared memory once per
+// CTA by the producer's bulk copies, completing h.pbar: every row reads them
+// again, and registers are kept for the backward's dgamma/dbeta partials.
+__device__ __forceinline__ void load_params(uint64_t *pbar, void *gdst, void *bdst, const void *g,
+                                            const void *b, uint32_t bytes) {
+    mbar_arrive_expect_tx(pbar, bytes * (b ? 2u : 1u));
+    bulk_g2s(gdst, g, bytes, pbar);
+    if (b) bulk_g2s(bdst, b, bytes, pbar);
 }
 
 // Bytes of shared memory the TMA kernels keep for gamma (and beta).
@@ -145,24 +143,27 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
     const int S = p.tc.stages, RT = p.tc.rows;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    uint4 *beta_s = par + (tma_param_bytes((int64_t)row_bytes, false) / 16);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&h.full[s], 1);
             mbar_init(&h.empty[s], CW);
         }
+        mbar_init(&h.pbar, 1);
         h.abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == CW) {
-        if (lane == 0)
+        if (lane == 0) {
+            load_params(&h.pbar, par, beta_s, p.gamma, LN ? p.beta : nullptr, (uint32_t)row_bytes);
             tma_produce<false, LN>(h, stages, p.tc, M, row_bytes, p.x, nullptr, nullptr, nullptr, 0);
+        }
         return;
     }
 
-    uint4 *beta_s = par + (tma_param_bytes((int64_t)row_bytes, false) / 16);
-    stage_params<NT>(par, beta_s, p.gamma, LN ? p.beta : nullptr, nv);
+    mbar_wait_bounded(&h.pbar, 0, &h.abort, p.tc.fault);
     const uint4 *gs = par;
     const uint4 *bs = beta_s;
     const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
@@ -270,18 +271,21 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
             mbar_init(&h.full[s], 1);
             mbar_init(&h.empty[s], CW);
         }
+        mbar_init(&h.pbar, 1);
         h.abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == CW) {
-        if (lane == 0)
+        if (lane == 0) {
+            load_params(&h.pbar, par, nullptr, p.gamma, nullptr, (uint32_t)row_bytes);
             tma_produce<true, LN>(h, stages, p.tc, M, row_bytes, p.x, p.dy, p.rstd, p.mean, tile_bytes);
+        }
         return;
     }
 
-    stage_params<NT>(par, nullptr, p.gamma, nullptr, nv);
+    mbar_wait_bounded(&h.pbar, 0, &h.abort, p.tc.fault);
     const uint4 *gs = par;
     const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
     float *scratch = h.red + grp * (2 * NS * WPR);

@@ -6,7 +6,7 @@ measured rows of csrc/dispatch_table.inc.
 
 Each (op, direction, dtype, N, M) is timed for every variant that can serve
 it (forced through gbnorm_force_variant), with L2 flushed before every timed
-call, CUDA events on the launching stream, median of --reps calls.  Effective
+call (1 GiB write, then 512 MiB read), CUDA events on the launching stream, median of --reps calls.  Effective
 bandwidth uses the algorithmic bytes only (b = element size):
     RMS fwd 2MNb + Nb + 4M     LN fwd 2MNb + 2Nb + 8M
     RMS bwd 3MNb + Nb + 4M + 4N   LN bwd 3MNb + Nb + 8M + 8N
@@ -46,7 +46,10 @@ def sweep(reps: int, only=None):
     import rmsnorm_norm_fwd_gb300 as g
     dt_t = {"fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16}
     dev = torch.device("cuda")
-    scrub = torch.empty(1 << 30, device=dev, dtype=torch.uint8)  # flushes L2, covers host launch time
+    # L2 flush before each timed call: a 1 GiB write, then a 512 MiB read so
+    # that the lines left in L2 are clean (no write-back inside the timing).
+    scrub = torch.empty(1 << 30, device=dev, dtype=torch.uint8)
+    clean = torch.ones(128 << 20, device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream()
     out = []
     for op, dt, M, N in SHAPES:
@@ -97,6 +100,7 @@ def sweep(reps: int, only=None):
                     times = []
                     for _ in range(reps):
                         scrub.zero_()
+                        clean.amax()
                         a = torch.cuda.Event(enable_timing=True)
                         b = torch.cuda.Event(enable_timing=True)
                         a.record(stream)

@@ -40,6 +40,10 @@ def _geom(name):
     if m:
         tpr, vpt, cw = (int(v) for v in m.groups())
         return (tpr, vpt, 1, 1, cw * 32, True)
+    m = re.fullmatch(r"tmac(\d+)x(\d+)s(\d+)", name)
+    if m:
+        cl, vpt, rs = (int(v) for v in m.groups())
+        return (256, vpt, rs, cl, 288, True)
     return None
 
 
@@ -88,7 +92,9 @@ def test_forced_variant(op, direction, dtype, variant):
     else:
         tpr, vpt, r, cl, cta, tma = geo
         cap = tpr * vpt * cl * E
-        if tma:
+        if tma and cl > 1:
+            M = 11  # a few rows per cluster; rows not a multiple of 4 (statistics tail)
+        elif tma:
             # several tiles, a ragged last tile (not a multiple of 4 rows)
             M = max(7, min(1000, (3 << 20) // (cap * (4 if dtype == "fp32" else 2))) | 3)
         else:
@@ -214,23 +220,35 @@ def test_degenerate_rows():
             compare(op, inp, out).assert_ok()
 
 
+# A staged variant per (direction, N) that the ring-wrap test forces.
+RING_VARIANTS = {(0, 256): "tma32x1w8", (1, 256): "tma16x2w8", (0, 2048): "tma32x8w8",
+                 (1, 2048): "tma128x2w8", (0, 8192): "tma128x8w8", (1, 8192): "tma256x4w8",
+                 (0, 65536): "tmac8x4s2", (1, 65536): "tmac8x4s2"}
+
+
 @pytest.mark.parametrize("op", ["rms", "ln"])
 @pytest.mark.parametrize("direction", [0, 1])
-@pytest.mark.parametrize("N", [256, 2048, 8192])
+@pytest.mark.parametrize("N", [256, 2048, 8192, 65536])
 @pytest.mark.parametrize("limit", [1, 3])
 def test_tma_ring_wraps(op, direction, N, limit):
-    """A capped grid makes each CTA walk many more tiles than the ring has
-    stages, so every stage's barriers go through several phases."""
+    """A capped grid makes each CTA (or cluster) walk many more tiles than the
+    ring has stages, so every stage's barriers -- and, for wide rows, the
+    cluster's exchange barriers -- go through several phases.  For wide rows
+    the cap is in CTAs: 8 and 24 CTAs leave one and three clusters."""
     import rmsnorm_norm_fwd_gb300 as g
-    M = 4099 if N <= 2048 else 517
-    name = g.variant_name(op == "ln", direction, M, N, "bf16")
-    assert name.startswith("tma"), name
+    M = 4099 if N <= 2048 else (517 if N <= 8192 else 37)
+    variant = RING_VARIANTS[(direction, N)]
+    if N > 8192:
+        limit = limit * 8
     try:
+        g.force_variant(op == "ln", direction, "bf16", variant)
         g.set_grid_limit(limit)
+        assert g.variant_name(op == "ln", direction, M, N, "bf16") == variant
         rep, _, _ = run_case(op, "bf16", M, N)
         rep.assert_ok()
     finally:
         g.set_grid_limit(0)
+        g.force_variant(op == "ln", direction, "bf16", None)
 
 
 def test_grid_limit_changes_nothing():
