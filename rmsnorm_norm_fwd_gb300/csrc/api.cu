@@ -134,10 +134,11 @@ bool tma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, si
     int stages = (int)(budget / stride);
     if (stages > kTmaMaxStages) stages = kTmaMaxStages;
     size_t ring = (size_t)stages * stride;
-    // The backward combines its row groups' partials in the idle ring.
+    // The backward combines its row groups' partials in the idle ring: every
+    // group's row of partials side by side ([NS][groups][TPR * VPT * E]).
     const int rpp = v.consumers() / v.tpr;
     if (c.dir == 1 && rpp > 1) {
-        const size_t comb = (size_t)v.tpr * v.vpt * v.elems_per_vec * 4 * (c.is_ln ? 2 : 1);
+        const size_t comb = (size_t)v.consumers() * v.vpt * v.elems_per_vec * 4 * (c.is_ln ? 2 : 1);
         if (comb > ring) ring = comb;
     }
     if (ring > budget) return false;

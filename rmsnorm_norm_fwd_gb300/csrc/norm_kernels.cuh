@@ -401,20 +401,31 @@ __global__ void __launch_bounds__(kColCTA) colreduce(const float *ws, int64_t P,
 #pragma unroll
     for (int v = 0; v < VW; ++v) acc[v] = 0.f;
     if (ok) {
-        if constexpr (VW == 4) {
-            const float4 *s4 = reinterpret_cast<const float4 *>(src + col);
-            const int64_t stride = N / 4;
-#pragma unroll 4
-            for (int64_t q = p0; q < p1; ++q) {
-                const float4 a = __ldg(s4 + q * stride);
-                acc[0] += a.x;
-                acc[1] += a.y;
-                acc[2] += a.z;
-                acc[3] += a.w;
+        // Bands of up to kColBatch rows: all loads of a batch are issued before
+        // any is added, so a band costs one memory latency, not one per row.
+        constexpr int kColBatch = 16;
+        for (int64_t q0 = p0; q0 < p1; q0 += kColBatch) {
+            if constexpr (VW == 4) {
+                const float4 *s4 = reinterpret_cast<const float4 *>(src + col);
+                const int64_t stride = N / 4;
+                float4 a[kColBatch];
+#pragma unroll
+                for (int i = 0; i < kColBatch; ++i)
+                    a[i] = q0 + i < p1 ? __ldg(s4 + (q0 + i) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < kColBatch; ++i) {
+                    acc[0] += a[i].x;
+                    acc[1] += a[i].y;
+                    acc[2] += a[i].z;
+                    acc[3] += a[i].w;
+                }
+            } else {
+                float a[kColBatch];
+#pragma unroll
+                for (int i = 0; i < kColBatch; ++i) a[i] = q0 + i < p1 ? __ldg(src + (q0 + i) * N + col) : 0.f;
+#pragma unroll
+                for (int i = 0; i < kColBatch; ++i) acc[0] += a[i];
             }
-        } else {
-#pragma unroll 4
-            for (int64_t q = p0; q < p1; ++q) acc[0] += __ldg(src + q * N + col);
         }
     }
 #pragma unroll

@@ -252,7 +252,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
     constexpr int RPP = NT / TPR;
     constexpr int WPR = TPR > 32 ? TPR / 32 : 1;
     constexpr int NS = LN ? 2 : 1;
-    constexpr bool HOLD = VPT * E <= 16;  // keep pass-1 values in registers for pass 2
+    constexpr bool HOLD = VPT * E <= 24;  // keep pass-1 values in registers for pass 2
     static_assert(NT % TPR == 0 && (TPR <= 32 || TPR % 32 == 0), "row group shape");
     static_assert(TPR <= 32 || (RPP * 2 * NS * WPR <= (int)(sizeof(TmaHeader::red) / 4) && RPP <= 14),
                   "scratch / named barrier ids");
@@ -289,6 +289,17 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
     const uint4 *gs = par;
     const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
     float *scratch = h.red + grp * (2 * NS * WPR);
+    // HOLD: this thread's gamma, widened once (its columns never change).
+    float gf[HOLD ? VPT : 1][E];
+    if constexpr (HOLD) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * TPR + t;
+            const uint4 g = v < nv ? lds128(gs + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int e = 0; e < E; ++e) gf[k][e] = vget<T>(g, e);
+        }
+    }
     const float n = (float)p.N;
     float accg[VPT][E], accb[LN ? VPT : 1][E];
 #pragma unroll
@@ -324,7 +335,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
                 if constexpr (LN) mean = in_win ? st[stat_stride(RT) + row] : __ldg(p.mean + row);
             }
             // Pass 1: x-hat and g = dy * gamma, their products summed over the
-            // row.  With at most 16 elements per thread (HOLD) x-hat, g and the
+            // row.  With at most 24 elements per thread (HOLD) x-hat, g and the
             // raw dy stay in registers for pass 2; otherwise pass 2 re-reads the
             // staged row.
             float sum[NS];
@@ -338,12 +349,16 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
                 const bool ok = rok && v < nv;
                 const uint4 q = ok ? lds128(xs + v) : make_uint4(0, 0, 0, 0);
                 const uint4 d = ok ? lds128(ds + v) : make_uint4(0, 0, 0, 0);
-                const uint4 g = ok ? lds128(gs + v) : make_uint4(0, 0, 0, 0);
-                if constexpr (HOLD) hd[k] = d;
+                uint4 g = make_uint4(0, 0, 0, 0);
+                if constexpr (HOLD) {
+                    hd[k] = d;
+                } else {
+                    g = ok ? lds128(gs + v) : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const float xh = (vget<T>(q, e) - mean) * rstd;
-                    const float gg = vget<T>(d, e) * vget<T>(g, e);
+                    const float gg = vget<T>(d, e) * (HOLD ? gf[HOLD ? k : 0][e] : vget<T>(g, e));
                     if constexpr (HOLD) {
                         hx[k][e] = xh;
                         hg[k][e] = gg;
@@ -388,36 +403,35 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
         if (lane == 0) mbar_arrive(&h.empty[s]);
     }
 
-    // Epilogue: the CTA's row groups own the same columns; add them in group
-    // order in shared memory (the stage ring is idle now: every copy issued
-    // was waited for above), then write the CTA's partial row.
+    // Epilogue: the CTA's row groups own the same columns.  Every group writes
+    // its partials to shared memory (the stage ring is idle now: every copy
+    // issued was waited for above), then each thread adds, for its columns,
+    // the groups' values in group order, and writes the CTA's partial row.
     float *wsg = p.ws + (int64_t)blockIdx.x * p.N;
     float *wsb = p.ws + ((int64_t)gridDim.x + blockIdx.x) * p.N;
     if constexpr (RPP > 1) {
-        constexpr int CAP = TPR * VPT * E;
-        float *comb = reinterpret_cast<float *>(stages);
-        named_sync(kTmaBarAll, NT);
-        for (int gi = 0; gi < RPP; ++gi) {
-            if (grp == gi) {
+        constexpr int CAP = TPR * VPT * E;  // columns one row group covers
+        float *comb = reinterpret_cast<float *>(stages);  // [NS][RPP][CAP]
+        named_sync(kTmaBarAll, NT);  // all rows done with the ring
 #pragma unroll
-                for (int k = 0; k < VPT; ++k)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const int c = (k * TPR + t) * E + e;
-                        comb[c] = gi == 0 ? accg[k][e] : comb[c] + accg[k][e];
-                        if constexpr (LN)
-                            comb[CAP + c] = gi == 0 ? accb[k][e] : comb[CAP + c] + accb[k][e];
-                    }
-            }
-            named_sync(kTmaBarAll, NT);
-        }
-        for (int i = threadIdx.x; i < TPR * VPT; i += NT) {
-            if (i >= nv) continue;
+        for (int k = 0; k < VPT; ++k)
 #pragma unroll
             for (int e = 0; e < E; ++e) {
-                wsg[(int64_t)i * E + e] = comb[i * E + e];
-                if constexpr (LN) wsb[(int64_t)i * E + e] = comb[CAP + i * E + e];
+                const int c = (k * TPR + t) * E + e;
+                comb[grp * CAP + c] = accg[k][e];
+                if constexpr (LN) comb[(RPP + grp) * CAP + c] = accb[k][e];
             }
+        named_sync(kTmaBarAll, NT);
+        const int64_t ncol = nv * E < CAP ? nv * E : CAP;
+        for (int c = threadIdx.x; c < ncol; c += NT) {
+            float sg = 0.f, sb = 0.f;
+#pragma unroll 4
+            for (int gi = 0; gi < RPP; ++gi) {
+                sg += comb[gi * CAP + c];
+                if constexpr (LN) sb += comb[(RPP + gi) * CAP + c];
+            }
+            wsg[c] = sg;
+            if constexpr (LN) wsb[c] = sb;
         }
     } else {
 #pragma unroll
