@@ -38,6 +38,11 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
     static_assert(CL == 1 || TPR == CTA, "a cluster row uses whole CTAs");
     constexpr int E = VecTraits<T>::E;
     constexpr int RPC = CTA / TPR;
+    // LayerNorm rows that fill the row group exactly (no cluster) take one
+    // equal-count (mean, M2) merge; otherwise the mean first, then the centred
+    // sum of squares.
+    constexpr bool MERGE = LN && CL == 1;
+    __shared__ RowReduceSmem<TPR, RPC, CL, MERGE ? 2 * R : 1> red2;
     __shared__ RowReduceSmem<TPR, RPC, CL, R> red;
 
     const int t = threadIdx.x % TPR;
@@ -45,6 +50,7 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
     const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
     const int64_t nv = p.N / E;
     const float n = (float)p.N;
+    const bool full = nv == (int64_t)TPR * VPT * CL;  // uniform over the grid
 
     int64_t vid[VPT];
     bool vok[VPT];
@@ -86,8 +92,29 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
                     s[r] += LN ? f : f * f;
                 }
         }
-        row_allreduce<TPR, RPC, CL, R>(s, red, parity);
         float mean[R], rstd[R];
+        if (MERGE && full) {
+            // Every thread holds VPT * E elements of each row: local mean and
+            // M2 from the registers, then one equal-count merge over the row.
+            constexpr float kC = (float)(VPT * E);
+            float m2[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                mean[r] = s[r] * (1.f / kC);
+                m2[r] = 0.f;
+#pragma unroll
+                for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float d = vget<T>(xv[r][k], e) - mean[r];
+                        m2[r] += d * d;
+                    }
+            }
+            if constexpr (MERGE) row_merge_equal<TPR, RPC, R>(mean, m2, kC, red2, parity);
+#pragma unroll
+            for (int r = 0; r < R; ++r) rstd[r] = rsqrtf(m2[r] / n + p.eps);
+        } else {
+        row_allreduce<TPR, RPC, CL, R>(s, red, parity);
         if constexpr (LN) {
             // Pass 2 over the registers: centred sum of squares (no cancellation).
 #pragma unroll
@@ -113,6 +140,7 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
                 mean[r] = 0.f;
                 rstd[r] = rsqrtf(s[r] / n + p.eps);
             }
+        }
         }
         if (t == 0 && rank == 0) {
 #pragma unroll

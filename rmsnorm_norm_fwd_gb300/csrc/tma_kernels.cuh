@@ -132,7 +132,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
     constexpr int RPP = NT / TPR;
     constexpr int WPR = TPR > 32 ? TPR / 32 : 1;
     static_assert(NT % TPR == 0 && (TPR <= 32 || TPR % 32 == 0), "row group shape");
-    static_assert(TPR <= 32 || (RPP * 2 * WPR <= (int)(sizeof(TmaHeader::red) / 4) && RPP <= 14),
+    static_assert(TPR <= 32 || (RPP * 2 * 2 * WPR <= (int)(sizeof(TmaHeader::red) / 4) && RPP <= 14),
                   "scratch / named barrier ids");
     extern __shared__ __align__(128) unsigned char smem[];
     TmaHeader &h = *reinterpret_cast<TmaHeader *>(smem);
@@ -167,8 +167,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
     const uint4 *gs = par;
     const uint4 *bs = beta_s;
     const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
-    float *scratch = h.red + grp * (2 * WPR);
+    float *scratch = h.red + grp * (2 * 2 * WPR);
     const float n = (float)p.N;
+    const bool full = nv == (int64_t)TPR * VPT;  // every thread holds VPT vectors of each row
     volatile int *abort_flag = &h.abort;
     int parity = 0, it = 0;
     const int64_t ntiles = (M + RT - 1) / RT;
@@ -196,8 +197,28 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
                     acc[0] += LN ? f : f * f;
                 }
             }
-            group_allreduce<TPR, 1>(acc, scratch, parity, 1 + grp);
             float mean = 0.f;
+            if (LN && full) {
+                // Every thread holds VPT * E elements of the row: local mean and
+                // M2 from the staged row, then one equal-count merge.
+                constexpr float kC = (float)(VPT * E);
+                mean = acc[0] * (1.f / kC);
+                float m2 = 0.f;
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = k * TPR + t;
+                    if (!rok) continue;
+                    const uint4 q = lds128(xs + v);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float d = vget<T>(q, e) - mean;
+                        m2 += d * d;
+                    }
+                }
+                group_merge_equal<TPR>(mean, m2, kC, scratch, parity, 1 + grp);
+                acc[0] = m2;
+            } else {
+            group_allreduce<TPR, 1>(acc, scratch, parity, 1 + grp);
             if constexpr (LN) {
                 // Second pass over the staged row: centred sum of squares.
                 mean = acc[0] / n;
@@ -214,6 +235,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
                     }
                 }
                 group_allreduce<TPR, 1>(acc, scratch, parity, 1 + grp);
+            }
             }
             const float rstd = rsqrtf(acc[0] / n + p.eps);
             if (!rok) continue;  // uniform per row group: no collective below

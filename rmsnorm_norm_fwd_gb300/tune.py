@@ -40,7 +40,7 @@ def alg_bytes(op, direction, M, N, b):
     return 3 * M * N * b + N * b + (8 if op == "ln" else 4) * M + (8 if op == "ln" else 4) * N
 
 
-def sweep(reps: int, only=None):
+def sweep(reps: int, only=None, dirs=(0, 1)):
     import torch
 
     import rmsnorm_norm_fwd_gb300 as g
@@ -71,7 +71,7 @@ def sweep(reps: int, only=None):
             g.layernorm_fwd(x, gam, bet, 1e-5, y=y, mean=mean, rstd=rstd)
         else:
             g.rmsnorm_fwd(x, gam, 1e-6, y=y, rstd=rstd)
-        for direction in (0, 1):
+        for direction in dirs:
             default = g.variant_name(ln, direction, M, N, dt)
             for v in g.variants(ln, direction, dt):
                 if v == "elem":
@@ -124,24 +124,34 @@ def sweep(reps: int, only=None):
     return out
 
 
+ROW_RE = re.compile(r'^\{(\d+), (\d+), (\d+), (\d+), "[^"]+"\},.*$')
+
+
 def emit(results, table_path):
-    """Rewrite the measured block of the dispatch table from sweep results."""
+    """Merge sweep results into the measured block of the dispatch table: a
+    (op, direction, dtype, N) the sweep measured gets its fastest variant; the
+    other measured rows stay as they are."""
     best = {}
     for r in results:
         key = (r["op"], r["dir"], r["dtype"], r["N"])
         if key not in best or r["gbs"] > best[key]["gbs"]:
             best[key] = r
-    rows = []
-    for (op, d, dt, n), r in sorted(best.items(), key=lambda kv: (kv[0][0], kv[0][1], kv[0][2], kv[0][3])):
-        nv = n * ELEM[dt] // 16
-        rows.append(f'{{{1 if op == "ln" else 0}, {d}, {DTYPE_CODE[dt]}, {nv}, "{r["variant"]}"}},'
-                    f'  // {op} {"fwd" if d == 0 else "bwd"} {dt} M={r["M"]} N={n}: {r["gbs"]:.0f} GB/s')
     text = open(table_path).read()
     start = text.index("// ---- measured rows (tune.py) ----")
     end = text.index("// ---- forward defaults")
-    block = "// ---- measured rows (tune.py) ----\n" + "\n".join(rows) + "\n"
+    rows = {}
+    for line in text[start:end].splitlines()[1:]:
+        m = ROW_RE.match(line)
+        if m:
+            rows[tuple(int(v) for v in m.groups())] = line
+    for (op, d, dt, n), r in best.items():
+        key = (1 if op == "ln" else 0, d, DTYPE_CODE[dt], n * ELEM[dt] // 16)
+        rows[key] = (f'{{{key[0]}, {d}, {key[2]}, {key[3]}, "{r["variant"]}"}},'
+                     f'  // {op} {"fwd" if d == 0 else "bwd"} {dt} M={r["M"]} N={n}: {r["gbs"]:.0f} GB/s')
+    order = sorted(rows, key=lambda k: (-k[0], k[1], -k[2], k[3]))
+    block = "// ---- measured rows (tune.py) ----\n" + "\n".join(rows[k] for k in order) + "\n"
     open(table_path, "w").write(text[:start] + block + text[end:])
-    return rows
+    return [rows[k] for k in order]
 
 
 def main(argv=None):
@@ -150,6 +160,7 @@ def main(argv=None):
     ap.add_argument("--emit", help="read sweep results (JSON) and rewrite the dispatch table")
     ap.add_argument("--reps", type=int, default=7)
     ap.add_argument("--only", help="regex over 'op-dtype-MxN' to restrict the sweep")
+    ap.add_argument("--dir", choices=("fwd", "bwd", "both"), default="both", help="directions to sweep")
     a = ap.parse_args(argv)
     here = os.path.dirname(os.path.abspath(__file__))
     if a.emit:
@@ -157,7 +168,7 @@ def main(argv=None):
             rows = emit(json.load(f), os.path.join(here, "csrc", "dispatch_table.inc"))
         print("\n".join(rows))
         return 0
-    res = sweep(a.reps, a.only)
+    res = sweep(a.reps, a.only, {"fwd": (0,), "bwd": (1,), "both": (0, 1)}[a.dir])
     if a.out:
         with open(a.out, "w") as f:
             json.dump(res, f)
