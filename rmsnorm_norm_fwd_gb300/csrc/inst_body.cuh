@@ -4,6 +4,7 @@
 #include "norm_kernels.cuh"
 #include "tma_kernels.cuh"
 #include "tma_cluster_kernels.cuh"
+#include "wide_kernels.cuh"
 #include "variants.inc"
 
 namespace gbn {
@@ -27,14 +28,21 @@ namespace gbn {
             kTmacNT, VPT, RS, CL, (kTmacCW + 1) * 32, VecTraits<GBN_T>::E, 1, 0},
 #define GBN_C_RMS(CL, VPT, RS) GBN_TMAC(false, CL, VPT, RS)
 #define GBN_C_LN(CL, VPT, RS) GBN_TMAC(true, CL, VPT, RS)
+#define GBN_WIDE(LN, NT, U, MINB, PF)                                                          \
+    Variant{GBN_WIDE_VNAME(NT, U, MINB, PF), (const void *)&fwd_wide<GBN_T, LN, NT, U, MINB, PF>,   \
+            kWide, NT, U, 1, 1, NT, VecTraits<GBN_T>::E, MINB, 0},
+#define GBN_W_RMS(NT, U, MINB, PF) GBN_WIDE(false, NT, U, MINB, PF)
+#define GBN_W_LN(NT, U, MINB, PF) GBN_WIDE(true, NT, U, MINB, PF)
 static const Variant rms_variants[] = {
     GBN_TMA_FWD_GEOMS(GBN_T_RMS)
     GBN_TMAC_FWD_GEOMS(GBN_C_RMS)
+    GBN_WIDE_FWD_GEOMS(GBN_W_RMS)
     GBN_FWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
     GBN_TMA_FWD_GEOMS(GBN_T_LN)
     GBN_TMAC_FWD_GEOMS(GBN_C_LN)
+    GBN_WIDE_FWD_GEOMS(GBN_W_LN)
     GBN_FWD_GEOMS(GBN_X_LN)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, true>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 const VariantTable GBN_CAT(kFwdRms_, GBN_SFX) = {rms_variants, (int)(sizeof(rms_variants) / sizeof(Variant))};
@@ -48,6 +56,9 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_TMAC
 #undef GBN_C_RMS
 #undef GBN_C_LN
+#undef GBN_WIDE
+#undef GBN_W_RMS
+#undef GBN_W_LN
 #endif
 
 #ifdef GBN_BWD

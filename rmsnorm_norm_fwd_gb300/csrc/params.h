@@ -49,6 +49,7 @@ enum VariantKind : int {
     kElem = 1,  // element-wise, any N and alignment
     kTma = 2,   // rows staged through a shared-memory ring by bulk async copies
     kTmaCl = 3, // as kTma, each row split across a thread-block cluster (column slices)
+    kWide = 4,  // one CTA per row, the row streamed twice (DRAM, then L2); any row length
 };
 
 // One compiled kernel and the geometry the host needs to launch it.
@@ -57,17 +58,17 @@ struct Variant {
     const void *kernel;  // __global__ entry (takes FwdParams or BwdParams by value)
     int kind;            // VariantKind
     int tpr;             // threads per row group (within one CTA)
-    int vpt;             // 16-byte vectors per thread per row (max)
+    int vpt;             // 16-byte vectors per thread per row (max); kWide: vectors per batch
     int rows;            // rows per row group per iteration (kRows); rows per exchange step (kTmaCl)
     int cl;              // CTAs per row (thread-block cluster size)
     int cta;             // threads per CTA
     int elems_per_vec;   // E (16 bytes / sizeof(T)); 1 for element-wise kernels
-    int ctas_per_sm;     // kTma: CTAs meant to share an SM (shared-memory budget split)
+    int ctas_per_sm;     // kTma: CTAs meant to share an SM (shared-memory budget split); kWide: launch bound
     int stage_target;    // kTma: bytes of one stage the host aims for
 
     // Longest row (elements) this variant can hold.
     int64_t max_n() const {
-        return kind == kElem ? INT64_MAX : (int64_t)tpr * vpt * cl * elems_per_vec;
+        return (kind == kElem || kind == kWide) ? INT64_MAX : (int64_t)tpr * vpt * cl * elems_per_vec;
     }
     // Threads of a CTA that work on rows (TMA kinds add one producer warp).
     int consumers() const { return (kind == kTma || kind == kTmaCl) ? cta - 32 : cta; }

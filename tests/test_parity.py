@@ -44,6 +44,10 @@ def _geom(name):
     if m:
         cl, vpt, rs = (int(v) for v in m.groups())
         return (256, vpt, rs, cl, 288, True)
+    m = re.fullmatch(r"wide(\d+)u(\d+)b(\d+)p(\d+)", name)
+    if m:
+        nt, u, _, _ = (int(v) for v in m.groups())
+        return ("wide", nt, u)
     return None
 
 
@@ -89,6 +93,12 @@ def test_forced_variant(op, direction, dtype, variant):
     geo = _geom(variant)
     if geo is None:  # the element-wise variant: odd N
         shapes = [(67, 1), (67, 77), (5, 3001)]
+    elif geo[0] == "wide":
+        # any row length: two full load batches per thread, one vector short
+        # of that, a row where only part of the CTA holds a last vector, and a
+        # row shorter than the CTA (threads without elements)
+        nt, u = geo[1], geo[2]
+        shapes = [(9, 2 * nt * u * E), (9, 2 * nt * u * E - E), (7, nt * E + 5 * E), (5, 3 * E)]
     else:
         tpr, vpt, r, cl, cta, tma = geo
         cap = tpr * vpt * cl * E
@@ -103,7 +113,7 @@ def test_forced_variant(op, direction, dtype, variant):
         shapes = [(M, cap), (M, cap - E)]
     try:
         g.force_variant(op == "ln", direction, dtype, variant)
-        if geo is not None and geo[5]:
+        if geo is not None and geo[0] != "wide" and geo[5]:
             # A staged variant may hold fewer elements than its register
             # capacity when gamma/beta and two stages must fit in shared
             # memory: take the widest row it serves, at least a quarter of it.
