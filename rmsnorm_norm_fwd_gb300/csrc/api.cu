@@ -176,9 +176,29 @@ bool tmac_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, s
     return true;
 }
 
+// Shared memory of a wide-row variant: none for the forward; for the
+// backward each CTA's column slice of dgamma (and dbeta) sums in fp32.  False
+// if a CTA of the cluster would get no columns or the sums do not fit.
+bool wide_geometry(const Variant &v, const CallShape &c, int dev, size_t *dyn_smem) {
+    *dyn_smem = 0;
+    if (c.dir == 0) return true;
+    const int64_t nv = c.N / v.elems_per_vec;
+    const int64_t slice = (nv + v.cl - 1) / v.cl;
+    if ((int64_t)(v.cl - 1) * slice >= nv) return false;
+    const size_t bytes = (size_t)slice * v.elems_per_vec * 4u * (c.is_ln ? 2u : 1u);
+    // room for the kernel's static shared memory (reductions, exchange slots)
+    if (bytes + 4096 > (size_t)g_dev[dev].smem_optin) return false;
+    *dyn_smem = bytes;
+    return true;
+}
+
 bool can_serve(const Variant &v, const CallShape &c, int dev) {
     if (v.kind == kElem) return true;
     if (!c.vec || c.N > v.max_n()) return false;
+    if (v.kind == kWide) {
+        size_t dyn;
+        return wide_geometry(v, c, dev, &dyn);
+    }
     if (v.kind == kTma || v.kind == kTmaCl) {
         if (c.dir == 1 && !c.stats) return false;
         TileCfg tc;
@@ -259,11 +279,13 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
     std::atomic<int> &slot = g_occ[dev][c.is_ln][c.dir][c.dtype][idx];
     int o = slot.load(std::memory_order_relaxed);
     const Variant &v = kTables[c.is_ln][c.dir][c.dtype]->v[idx];
-    if (o > 0 && v.kind != kTma) {
+    // Kinds whose shared memory (and so occupancy) depends on the shape.
+    const bool per_shape = v.kind == kTma || (v.kind == kWide && dyn_smem > 0);
+    if (o > 0 && !per_shape) {
         *out = o;
         return GBNORM_OK;
     }
-    if (v.kind == kTma || v.kind == kTmaCl) {
+    if (v.kind == kTma || v.kind == kTmaCl || (v.kind == kWide && dyn_smem > 0)) {
         std::atomic<uint64_t> &cache = g_occ_tma[dev][c.is_ln][c.dir][c.dtype][idx];
         const uint64_t hit = cache.load(std::memory_order_relaxed);
         if (hit != 0 && (hit >> 16) == (uint64_t)dyn_smem) {
@@ -272,7 +294,10 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
         }
         std::atomic<int> &set = g_smem_set[dev][c.is_ln][c.dir][c.dtype][idx];
         if (!set.load(std::memory_order_acquire)) {
-            const int lim = g_dev[dev].smem_optin / v.ctas_per_sm;
+            // Dynamic limit: the per-SM share, less the kernel's static shared memory.
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, v.kernel) != cudaSuccess) return GBNORM_ERR_CUDA;
+            const int lim = g_dev[dev].smem_optin / v.ctas_per_sm - (int)fa.sharedSizeBytes;
             if (cudaFuncSetAttribute(v.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim) !=
                 cudaSuccess)
                 return GBNORM_ERR_CUDA;
@@ -282,7 +307,7 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
                 return GBNORM_ERR_CUDA;
             set.store(1, std::memory_order_release);
         }
-        if (v.kind == kTma) {
+        if (v.cl == 1) {
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, v.kernel, v.cta, dyn_smem) != cudaSuccess)
                 return GBNORM_ERR_CUDA;
         } else {
@@ -318,7 +343,7 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
         if (cudaOccupancyMaxActiveClusters(&o, v.kernel, &cfg) != cudaSuccess) return GBNORM_ERR_CUDA;
     }
     if (o <= 0) return GBNORM_ERR_UNSUPPORTED;
-    if (v.kind != kTma) slot.store(o, std::memory_order_relaxed);
+    if (!per_shape) slot.store(o, std::memory_order_relaxed);
     *out = o;
     return GBNORM_OK;
 }
@@ -335,6 +360,7 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
     if (c.M <= 0) return GBNORM_OK;
     if (v.kind == kTma && !tma_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kTmaCl && !tmac_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
+    if (v.kind == kWide && !wide_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     int occ = 0;
     int st = occupancy(c, idx, dev, pl->dyn_smem, &occ);
     if (st != GBNORM_OK) return st;

@@ -77,18 +77,28 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
             kTmacNT, VPT, RS, CL, (kTmacCW + 1) * 32, VecTraits<GBN_T>::E, 1, 0},
 #define GBN_C_RMS(CL, VPT, RS) GBN_TMAC(false, CL, VPT, RS)
 #define GBN_C_LN(CL, VPT, RS) GBN_TMAC(true, CL, VPT, RS)
+#define GBN_BWIDE(LN, NT, U, CL, PF, F)                                                        \
+    Variant{GBN_BWIDE_VNAME(NT, U, CL, PF, F), (const void *)&bwd_wide<GBN_T, LN, NT, U, CL, PF, F>, \
+            kWide, NT, U, 1, CL, NT, VecTraits<GBN_T>::E, 1, 0},
+#define GBN_W_RMS(NT, U, CL, PF, F) GBN_BWIDE(false, NT, U, CL, PF, F)
+#define GBN_W_LN(NT, U, CL, PF, F) GBN_BWIDE(true, NT, U, CL, PF, F)
 static const Variant rms_variants[] = {
     GBN_TMA_BWD_GEOMS(GBN_T_RMS)
     GBN_TMAC_BWD_GEOMS(GBN_C_RMS)
+    GBN_WIDE_BWD_GEOMS(GBN_W_RMS)
     GBN_BWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&bwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
     GBN_TMA_BWD_GEOMS(GBN_T_LN)
     GBN_TMAC_BWD_GEOMS(GBN_C_LN)
+    GBN_WIDE_BWD_GEOMS(GBN_W_LN)
     GBN_BWD_GEOMS(GBN_X_LN)
     Variant{"elem", (const void *)&bwd_elem<GBN_T, true>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 const VariantTable GBN_CAT(kBwdRms_, GBN_SFX) = {rms_variants, (int)(sizeof(rms_variants) / sizeof(Variant))};
 const VariantTable GBN_CAT(kBwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_variants) / sizeof(Variant))};
+#undef GBN_BWIDE
+#undef GBN_W_RMS
+#undef GBN_W_LN
 #endif
 
 }  // namespace gbn

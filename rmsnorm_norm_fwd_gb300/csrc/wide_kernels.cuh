@@ -282,3 +282,305 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wide(const FwdParams p) {
 }
 
 }  // namespace gbn
+
+namespace gbn {
+
+// ============================================================================ backward
+// Backward for wide rows: a cluster of CL CTAs (CL = 1, 2, 4 or 8) shares each
+// row; CTA `rank` owns a contiguous column slice and keeps its dgamma (and
+// dbeta) partial sums for that slice in shared memory across all the rows it
+// visits.  Per row: pass 1 streams the slice of x and dy from DRAM (L2
+// evict_last) for the partial sums sum g xhat and sum g (g = dy gamma), the
+// CTA reduces them and sends them to every CTA of the cluster through
+// distributed shared memory; pass 2 re-reads the slice from L2, writes
+// dx = rstd (g - c1 - xhat c2) and adds dy xhat (and dy) into the shared
+// accumulators.  At the end each CTA writes its slice of the cluster's
+// partial row; the column-reduce kernel sums the partial rows.
+//
+// Pipeline: iteration j of a CTA sweeps its slice once for both pass 1 of
+// its row j and pass 2 of its row j - 2 (gamma loaded once for both), so each
+// batch has two rows' loads in flight; then it reduces and sends row j's
+// partials and waits for row j - 1's exchange, which has had a whole sweep to
+// complete.
+//
+// Exchange: each CTA stores its partials of row k into slot [k % 4][rank] of
+// every CTA (st.shared::cluster) and arrives with release semantics on that
+// CTA's barrier xch[k % 4]; it waits (acquire, bounded) for CL arrivals,
+// then adds the CL partials in rank order, so every CTA gets identical bits.
+// Reuse is safe with four slots: a peer sends row k + 4 only after it has
+// received this CTA's row k + 2, which this CTA sends after a CTA barrier
+// that follows its reads of row k's slots (and its completed wait for row k).
+
+// One sweep of a CTA over its slice: pass 1 of one row (P1) and pass 2 of
+// another (P2), batch by batch.  v: this thread's pass-1 partial sums.
+template <typename T, bool LN, int NT, int U, bool P1, bool P2>
+__device__ __forceinline__ void wide_bwd_sweep(int t, int cnt, int64_t slice, const uint4 *gr,
+                                               float4 *accs, const uint4 *x1, const uint4 *d1,
+                                               float mean1, float rstd1, float (&v)[LN ? 2 : 1],
+                                               const uint4 *x2, const uint4 *d2, uint4 *dx2,
+                                               float mean2, float rstd2, float c1, float c2,
+                                               uint64_t keep, uint64_t drop) {
+    constexpr int E = VecTraits<T>::E;
+    constexpr int H = E / 4;
+    constexpr int A = U < 2 ? U : 2;  // independent partial-sum chains
+    float a2[A], a1[A];
+#pragma unroll
+    for (int a = 0; a < A; ++a) a2[a] = a1[a] = 0.f;
+    for (int b = t; b < cnt; b += NT * U) {
+        uint4 px[U], pd[U], qx[U], qd[U], g[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int vv = b + u * NT;
+            if (vv < cnt) {
+                g[u] = ld_l2hint(gr + vv, keep);
+                if constexpr (P1) {
+                    px[u] = ld_l2hint(x1 + vv, keep);
+                    pd[u] = ld_l2hint(d1 + vv, keep);
+                }
+                if constexpr (P2) {
+                    qx[u] = ld_l2hint(x2 + vv, drop);
+                    qd[u] = ld_l2hint(d2 + vv, drop);
+                }
+            } else {
+                g[u] = px[u] = pd[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        if constexpr (P2) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int vv = b + u * NT;
+                if (vv < cnt) {
+                    float o[E], dg[E], dyv[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float xh = (vget<T>(qx[u], e) - mean2) * rstd2;
+                        dyv[e] = vget<T>(qd[u], e);
+                        const float gg = dyv[e] * vget<T>(g[u], e);
+                        o[e] = rstd2 * (gg - c1 - xh * c2);
+                        dg[e] = dyv[e] * xh;
+                    }
+                    st_l2hint(dx2 + vv, vpack<T>(o), drop);
+#pragma unroll
+                    for (int h = 0; h < H; ++h) {
+                        float4 &ag = accs[h * slice + vv];
+                        float4 a = ag;
+                        a.x += dg[4 * h];
+                        a.y += dg[4 * h + 1];
+                        a.z += dg[4 * h + 2];
+                        a.w += dg[4 * h + 3];
+                        ag = a;
+                        if constexpr (LN) {
+                            float4 &ab = accs[(H + h) * slice + vv];
+                            float4 q = ab;
+                            q.x += dyv[4 * h];
+                            q.y += dyv[4 * h + 1];
+                            q.z += dyv[4 * h + 2];
+                            q.w += dyv[4 * h + 3];
+                            ab = q;
+                        }
+                    }
+                }
+            }
+        }
+        if constexpr (P1) {
+            // lanes past the slice hold zeros: g = 0 adds nothing
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float xh = (vget<T>(px[u], e) - mean1) * rstd1;
+                    const float gg = vget<T>(pd[u], e) * vget<T>(g[u], e);
+                    a2[u % A] += gg * xh;
+                    if constexpr (LN) a1[u % A] += gg;
+                }
+        }
+    }
+    if constexpr (P1) {
+        v[0] = a2[0];
+#pragma unroll
+        for (int a = 1; a < A; ++a) v[0] += a2[a];
+        if constexpr (LN) {
+            v[1] = a1[0];
+#pragma unroll
+            for (int a = 1; a < A; ++a) v[1] += a1[a];
+        }
+    }
+}
+
+// FUSE: 1 the schedule above; 0 pass 1 of row k + 1 (and its send), then the
+// wait for row k's exchange, then pass 2 of row k (one row's loads per batch,
+// larger batches).
+template <typename T, bool LN, int NT, int U, int CL, int PF, int FUSE>
+__global__ void __launch_bounds__(NT, 1) bwd_wide(const BwdParams p) {
+    pdl_launch_dependents();  // the column reduce waits for this grid's completion
+    constexpr int E = VecTraits<T>::E;
+    constexpr int W = NT / 32;
+    constexpr int H = E / 4;          // float4 accumulators per 16-byte vector
+    constexpr int NVAL = LN ? 2 : 1;  // partial sums per row; accumulator planes
+    constexpr int NS = 4;             // exchange slots
+    static_assert(NT % 32 == 0 && NT <= 1024 && CL >= 1 && CL <= 8, "shape");
+    extern __shared__ __align__(16) float4 accs[];  // [NVAL][H][slice]
+    __shared__ float red[2][NVAL][W];
+    __shared__ float slot[NS][CL][NVAL];
+    __shared__ __align__(8) uint64_t xch[NS];
+    __shared__ int abort_flag;
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+    const int64_t cid = CL > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
+    const int64_t ncl = CL > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
+    const int64_t M = p.M, nv = p.N / E;
+    const int64_t slice = (nv + CL - 1) / CL;
+    const int64_t v0 = rank * slice;
+    const int cnt = (int)(nv - v0 < slice ? nv - v0 : slice);
+    const float n = (float)p.N;
+    const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
+    const uint4 *gr = static_cast<const uint4 *>(p.gamma) + v0;
+    const size_t slice_bytes = (size_t)cnt * 16;
+
+    for (int64_t i = t; i < (int64_t)NVAL * H * slice; i += NT) accs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t == 0) {
+        abort_flag = 0;
+        if (CL > 1) {
+            for (int j = 0; j < NS; ++j) mbar_init(&xch[j], CL);
+            fence_mbar_init();
+        }
+    }
+    // Every CTA's barriers exist before any peer arrives on them.
+    if constexpr (CL > 1) cluster_sync_all();
+    else __syncthreads();
+
+    const int64_t nrows = cid < M ? (M - cid + ncl - 1) / ncl : 0;
+    auto row_of = [&](int64_t k) { return cid + k * ncl; };
+    auto row_x = [&](int64_t k) { return static_cast<const uint4 *>(p.x) + row_of(k) * nv + v0; };
+    auto row_dy = [&](int64_t k) { return static_cast<const uint4 *>(p.dy) + row_of(k) * nv + v0; };
+    auto prefetch = [&](int64_t k) {
+        if (warp == 0 && k < nrows) {
+            prefetch_row(row_x(k), slice_bytes, lane, keep);
+            prefetch_row(row_dy(k), slice_bytes, lane, keep);
+        }
+    };
+    int parity = 0;
+    float cst[3][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // (c1, c2) of row k at [k % 3], once known
+
+    // Row k's pass-1 partials v, summed over the CTA (identical bits in every
+    // thread), then sent to the cluster (or, without one, turned into c1, c2).
+    auto finish_pass1 = [&](int64_t k, float (&v)[NVAL]) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < NVAL; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < NVAL; ++i) red[parity][i][warp] = v[i];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NVAL; ++i) {
+            float s = 0.f;
+#pragma unroll 4
+            for (int w = 0; w < W; ++w) s += red[parity][i][w];
+            v[i] = s;
+        }
+        parity ^= 1;
+        if constexpr (CL > 1) {
+            if (t < CL) {
+                const int sp = (int)(k % NS);
+                const uint32_t dst = map_to_rank(smem_u32(&slot[sp][rank][0]), (uint32_t)t);
+#pragma unroll
+                for (int i = 0; i < NVAL; ++i) st_cluster_f32(dst + 4u * i, v[i]);
+                mbar_arrive_remote(map_to_rank(smem_u32(&xch[sp]), (uint32_t)t));
+            }
+        } else {
+            cst[k % 3][0] = LN ? v[NVAL - 1] / n : 0.f;
+            cst[k % 3][1] = v[0] / n;
+        }
+    };
+    // Row k's exchange: wait for the CL partials, sum them in rank order.
+    auto recv = [&](int64_t k) {
+        if constexpr (CL > 1) {
+            const int sp = (int)(k % NS);
+            mbar_wait_cluster_bounded(&xch[sp], (uint32_t)((k / NS) & 1), &abort_flag, p.tc.fault);
+            float s[NVAL];
+#pragma unroll
+            for (int i = 0; i < NVAL; ++i) {
+                s[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) s[i] += slot[sp][c][i];
+            }
+            cst[k % 3][0] = LN ? s[NVAL - 1] / n : 0.f;
+            cst[k % 3][1] = s[0] / n;
+        }
+    };
+    auto rstd_of = [&](int64_t k) { return __ldg(p.rstd + row_of(k)); };
+    auto mean_of = [&](int64_t k) { return LN ? __ldg(p.mean + row_of(k)) : 0.f; };
+    auto dx_of = [&](int64_t k) { return static_cast<uint4 *>(p.dx) + row_of(k) * nv + v0; };
+
+    if (PF == 2) prefetch(0);
+    if constexpr (FUSE) {
+        for (int64_t j = 0; j < nrows + 2; ++j) {
+            const bool has1 = j < nrows, has2 = j >= 2;
+            if (PF == 1) prefetch(j);
+            if (PF == 2) prefetch(j + 1);
+            float v[NVAL];
+            const int64_t k1 = has1 ? j : 0, k2 = has2 ? j - 2 : 0;
+            const float rstd1 = has1 ? rstd_of(k1) : 0.f, mean1 = has1 ? mean_of(k1) : 0.f;
+            const float rstd2 = has2 ? rstd_of(k2) : 0.f, mean2 = has2 ? mean_of(k2) : 0.f;
+            const float c1 = cst[k2 % 3][0], c2 = cst[k2 % 3][1];
+            if (has1 && has2)
+                wide_bwd_sweep<T, LN, NT, U, true, true>(t, cnt, slice, gr, accs, row_x(k1), row_dy(k1),
+                                                         mean1, rstd1, v, row_x(k2), row_dy(k2), dx_of(k2),
+                                                         mean2, rstd2, c1, c2, keep, drop);
+            else if (has1)
+                wide_bwd_sweep<T, LN, NT, U, true, false>(t, cnt, slice, gr, accs, row_x(k1), row_dy(k1),
+                                                          mean1, rstd1, v, nullptr, nullptr, nullptr, 0.f,
+                                                          0.f, 0.f, 0.f, keep, drop);
+            else if (has2)
+                wide_bwd_sweep<T, LN, NT, U, false, true>(t, cnt, slice, gr, accs, nullptr, nullptr, 0.f,
+                                                          0.f, v, row_x(k2), row_dy(k2), dx_of(k2), mean2,
+                                                          rstd2, c1, c2, keep, drop);
+            if (has1) finish_pass1(j, v);
+            if (j >= 1 && j - 1 < nrows) recv(j - 1);
+        }
+    } else {
+        float v[NVAL];
+        if (nrows > 0) {
+            if (PF == 1) prefetch(0);
+            wide_bwd_sweep<T, LN, NT, U, true, false>(t, cnt, slice, gr, accs, row_x(0), row_dy(0),
+                                                      mean_of(0), rstd_of(0), v, nullptr, nullptr, nullptr,
+                                                      0.f, 0.f, 0.f, 0.f, keep, drop);
+            finish_pass1(0, v);
+        }
+        for (int64_t k = 0; k < nrows; ++k) {
+            if (k + 1 < nrows) {
+                if (PF == 1) prefetch(k + 1);
+                if (PF == 2) prefetch(k + 2);
+                wide_bwd_sweep<T, LN, NT, U, true, false>(t, cnt, slice, gr, accs, row_x(k + 1),
+                                                          row_dy(k + 1), mean_of(k + 1), rstd_of(k + 1), v,
+                                                          nullptr, nullptr, nullptr, 0.f, 0.f, 0.f, 0.f,
+                                                          keep, drop);
+                finish_pass1(k + 1, v);
+            }
+            recv(k);
+            wide_bwd_sweep<T, LN, NT, U, false, true>(t, cnt, slice, gr, accs, nullptr, nullptr, 0.f, 0.f,
+                                                      v, row_x(k), row_dy(k), dx_of(k), mean_of(k),
+                                                      rstd_of(k), cst[k % 3][0], cst[k % 3][1], keep, drop);
+        }
+    }
+    // No CTA leaves while a peer could still write into its shared memory
+    // (this matters only after an aborted wait).
+    if constexpr (CL > 1) cluster_sync_all();
+
+    // This CTA's slice of the cluster's partial row (P = clusters).
+    float4 *wsg = reinterpret_cast<float4 *>(p.ws + cid * p.N + v0 * E);
+    float4 *wsb = reinterpret_cast<float4 *>(p.ws + (ncl + cid) * p.N + v0 * E);
+    for (int vv = t; vv < cnt; vv += NT) {
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            wsg[vv * H + h] = accs[h * slice + vv];
+            if constexpr (LN) wsb[vv * H + h] = accs[(H + h) * slice + vv];
+        }
+    }
+}
+
+}  // namespace gbn

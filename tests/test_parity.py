@@ -47,7 +47,11 @@ def _geom(name):
     m = re.fullmatch(r"wide(\d+)u(\d+)b(\d+)p(\d+)", name)
     if m:
         nt, u, _, _ = (int(v) for v in m.groups())
-        return ("wide", nt, u)
+        return ("wide", nt, u, 1)
+    m = re.fullmatch(r"bwide(\d+)u(\d+)c(\d+)p(\d+)f(\d+)", name)
+    if m:
+        nt, u, cl, _, _ = (int(v) for v in m.groups())
+        return ("wide", nt, u, cl)
     return None
 
 
@@ -94,11 +98,14 @@ def test_forced_variant(op, direction, dtype, variant):
     if geo is None:  # the element-wise variant: odd N
         shapes = [(67, 1), (67, 77), (5, 3001)]
     elif geo[0] == "wide":
-        # any row length: two full load batches per thread, one vector short
-        # of that, a row where only part of the CTA holds a last vector, and a
-        # row shorter than the CTA (threads without elements)
-        nt, u = geo[1], geo[2]
-        shapes = [(9, 2 * nt * u * E), (9, 2 * nt * u * E - E), (7, nt * E + 5 * E), (5, 3 * E)]
+        # any row length (per CTA of the cluster): two full load batches per
+        # thread, one vector short of that, a slice where only part of the CTA
+        # holds a last vector, and a slice shorter than the CTA (threads
+        # without elements).  The backward keeps each slice's dgamma/dbeta
+        # sums in shared memory: the widest rows that fit are taken.
+        nt, u, cl = geo[1], geo[2], geo[3]
+        full = cl * 2 * nt * u * E
+        shapes = [(9, full), (9, full - E), (7, cl * (nt * E + 5 * E)), (5, cl * 3 * E)]
     else:
         tpr, vpt, r, cl, cta, tma = geo
         cap = tpr * vpt * cl * E
@@ -113,6 +120,12 @@ def test_forced_variant(op, direction, dtype, variant):
         shapes = [(M, cap), (M, cap - E)]
     try:
         g.force_variant(op == "ln", direction, dtype, variant)
+        if geo is not None and geo[0] == "wide" and direction == 1:
+            # the widest of the rows above whose slice sums fit
+            full = shapes[0][1]
+            while full > geo[3] * E and g.variant_name(op == "ln", 1, 9, full, dtype) != variant:
+                full //= 2
+            shapes = [(9, full), (9, full - E)] + shapes[2:]
         if geo is not None and geo[0] != "wide" and geo[5]:
             # A staged variant may hold fewer elements than its register
             # capacity when gamma/beta and two stages must fit in shared
@@ -253,6 +266,41 @@ def test_tma_ring_wraps(op, direction, N, limit):
     try:
         g.force_variant(op == "ln", direction, "bf16", variant)
         g.set_grid_limit(limit)
+        assert g.variant_name(op == "ln", direction, M, N, "bf16") == variant
+        rep, _, _ = run_case(op, "bf16", M, N)
+        rep.assert_ok()
+    finally:
+        g.set_grid_limit(0)
+        g.force_variant(op == "ln", direction, "bf16", None)
+
+
+# Wide-row variants (one CTA per row, or a cluster with an exchange ring of
+# four slots) that the pipeline test forces, per (direction, N).
+WIDE_PIPE = {(0, 16384): "wide512u8b2p1", (0, 65536): "wide1024u4b1p1",
+             (1, 8192): "bwide512u4c1p1f0", (1, 16384): "bwide512u2c1p2f1",
+             (1, 32768): "bwide512u2c2p2f1", (1, 32760): "bwide512u4c2p1f0",
+             (1, 65536): "bwide512u2c4p2f1", (1, 65528): "bwide512u4c4p2f0",
+             (1, 131072): "bwide512u2c8p2f1"}
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("key", sorted(WIDE_PIPE), ids=lambda k: f"{'fwd' if k[0] == 0 else 'bwd'}-{k[1]}")
+@pytest.mark.parametrize("limit", [1, 3])
+def test_wide_rows_pipeline(op, key, limit):
+    """A capped grid gives each CTA (or cluster) many rows in turn: the
+    forward's prefetch chain and the backward's pipeline (pass 2 two rows
+    behind pass 1, exchange barriers and slots reused every fourth row) run
+    through every phase, including rows counts that are not multiples of 4."""
+    import rmsnorm_norm_fwd_gb300 as g
+    direction, N = key
+    variant = WIDE_PIPE[key]
+    cl = int(re.search(r"c(\d+)p", variant).group(1)) if variant.startswith("bwide") else 1
+    M = 23
+    try:
+        g.force_variant(op == "ln", direction, "bf16", variant)
+        if g.variant_name(op == "ln", direction, M, N, "bf16") != variant:
+            pytest.skip(f"{variant} cannot hold {op} rows of {N}")
+        g.set_grid_limit(limit * cl)
         assert g.variant_name(op == "ln", direction, M, N, "bf16") == variant
         rep, _, _ = run_case(op, "bf16", M, N)
         rep.assert_ok()
