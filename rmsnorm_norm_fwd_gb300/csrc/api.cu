@@ -114,7 +114,8 @@ bool tma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, si
     const int ntens = c.dir == 0 ? 1 : 2;
     auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
     // Header, then gamma (and beta for the LayerNorm forward), then the ring.
-    const size_t params = al(row_bytes) * ((c.dir == 0 && c.is_ln) ? 2 : 1);
+    // (the backward keeps gamma widened to fp32)
+    const size_t params = c.dir == 0 ? al(row_bytes) * (c.is_ln ? 2 : 1) : al((size_t)c.N * 4);
     const size_t budget_all = (size_t)g_dev[dev].smem_optin / (size_t)v.ctas_per_sm;
     if (budget_all <= (size_t)kTmaHeaderBytes + params + 1024) return false;
     const size_t budget = budget_all - kTmaHeaderBytes - params;
@@ -125,18 +126,23 @@ bool tma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, si
         if (c.dir == 1) s += al((size_t)((rt + 7) & ~(int64_t)3) * 4 * (c.is_ln ? 2 : 1));
         return s;
     };
+    // Row groups of the CTA; without a producer warp each keeps its own part
+    // of the ring (at least two stages each, the same number for all).
+    const int rpp = v.consumers() / v.tpr;
+    const int min_stages = v.kind == kTmaP ? 2 * rpp : 2;
+    if (min_stages > kTmaMaxStages) return false;
     int64_t rt = (int64_t)(v.stage_target / (ntens * row_bytes));
     if (rt < 1) rt = 1;
     if (rt > c.M) rt = c.M > 0 ? c.M : 1;  // never more rows per tile than the problem has
-    while (rt > 1 && 2 * stride_of(rt) > budget) rt /= 2;
+    while (rt > 1 && (size_t)min_stages * stride_of(rt) > budget) rt /= 2;
     const size_t stride = stride_of(rt);
-    if (2 * stride > budget) return false;
+    if ((size_t)min_stages * stride > budget) return false;
     int stages = (int)(budget / stride);
     if (stages > kTmaMaxStages) stages = kTmaMaxStages;
+    if (v.kind == kTmaP) stages -= stages % rpp;
     size_t ring = (size_t)stages * stride;
     // The backward combines its row groups' partials in the idle ring: every
     // group's row of partials side by side ([NS][groups][TPR * VPT * E]).
-    const int rpp = v.consumers() / v.tpr;
     if (c.dir == 1 && rpp > 1) {
         const size_t comb = (size_t)v.consumers() * v.vpt * v.elems_per_vec * 4 * (c.is_ln ? 2 : 1);
         if (comb > ring) ring = comb;
@@ -192,6 +198,15 @@ bool wide_geometry(const Variant &v, const CallShape &c, int dev, size_t *dyn_sm
     return true;
 }
 
+// Shared memory of a row-resident variant with gamma (and beta) staged as
+// fp32: [N] floats each; false if it does not fit.
+bool rows_s_geometry(const Variant &v, const CallShape &c, int dev, size_t *dyn_smem) {
+    const size_t bytes = (size_t)c.N * 4u * (c.is_ln ? 2u : 1u);
+    if (bytes + 4096 > (size_t)g_dev[dev].smem_optin) return false;
+    *dyn_smem = bytes;
+    return true;
+}
+
 bool can_serve(const Variant &v, const CallShape &c, int dev) {
     if (v.kind == kElem) return true;
     if (!c.vec || c.N > v.max_n()) return false;
@@ -199,11 +214,15 @@ bool can_serve(const Variant &v, const CallShape &c, int dev) {
         size_t dyn;
         return wide_geometry(v, c, dev, &dyn);
     }
-    if (v.kind == kTma || v.kind == kTmaCl) {
+    if (v.kind == kRowsS) {
+        size_t dyn;
+        return rows_s_geometry(v, c, dev, &dyn);
+    }
+    if (v.staged_rows() || v.kind == kTmaCl) {
         if (c.dir == 1 && !c.stats) return false;
         TileCfg tc;
         size_t dyn;
-        return v.kind == kTma ? tma_geometry(v, c, dev, &tc, &dyn) : tmac_geometry(v, c, dev, &tc, &dyn);
+        return v.staged_rows() ? tma_geometry(v, c, dev, &tc, &dyn) : tmac_geometry(v, c, dev, &tc, &dyn);
     }
     return true;
 }
@@ -280,12 +299,12 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
     int o = slot.load(std::memory_order_relaxed);
     const Variant &v = kTables[c.is_ln][c.dir][c.dtype]->v[idx];
     // Kinds whose shared memory (and so occupancy) depends on the shape.
-    const bool per_shape = v.kind == kTma || (v.kind == kWide && dyn_smem > 0);
+    const bool per_shape = v.staged_rows() || v.kind == kRowsS || (v.kind == kWide && dyn_smem > 0);
     if (o > 0 && !per_shape) {
         *out = o;
         return GBNORM_OK;
     }
-    if (v.kind == kTma || v.kind == kTmaCl || (v.kind == kWide && dyn_smem > 0)) {
+    if (v.staged_rows() || v.kind == kTmaCl || v.kind == kRowsS || (v.kind == kWide && dyn_smem > 0)) {
         std::atomic<uint64_t> &cache = g_occ_tma[dev][c.is_ln][c.dir][c.dtype][idx];
         const uint64_t hit = cache.load(std::memory_order_relaxed);
         if (hit != 0 && (hit >> 16) == (uint64_t)dyn_smem) {
@@ -297,7 +316,10 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
             // Dynamic limit: the per-SM share, less the kernel's static shared memory.
             cudaFuncAttributes fa;
             if (cudaFuncGetAttributes(&fa, v.kernel) != cudaSuccess) return GBNORM_ERR_CUDA;
-            const int lim = g_dev[dev].smem_optin / v.ctas_per_sm - (int)fa.sharedSizeBytes;
+            // (kTma splits the SM between ctas_per_sm CTAs; for the other kinds it
+            // is only a launch bound and occupancy follows from the footprint.)
+            const int share = v.kind == kTma ? v.ctas_per_sm : 1;
+            const int lim = g_dev[dev].smem_optin / share - (int)fa.sharedSizeBytes;
             if (cudaFuncSetAttribute(v.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim) !=
                 cudaSuccess)
                 return GBNORM_ERR_CUDA;
@@ -358,9 +380,10 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
     pl->dyn_smem = 0;
     pl->tc = TileCfg{0, 0, 0, g_dev[dev].fault};
     if (c.M <= 0) return GBNORM_OK;
-    if (v.kind == kTma && !tma_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
+    if (v.staged_rows() && !tma_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kTmaCl && !tmac_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kWide && !wide_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
+    if (v.kind == kRowsS && !rows_s_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     int occ = 0;
     int st = occupancy(c, idx, dev, pl->dyn_smem, &occ);
     if (st != GBNORM_OK) return st;
@@ -386,7 +409,7 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
         pl->P = ncl;
         return GBNORM_OK;
     }
-    if (v.kind == kTma) {
+    if (v.staged_rows()) {
         const int64_t ntiles = (c.M + pl->tc.rows - 1) / pl->tc.rows;
         int64_t cap = (int64_t)occ * sms;
         if (limit > 0 && limit < cap) cap = limit;

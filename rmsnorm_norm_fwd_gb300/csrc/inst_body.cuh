@@ -33,16 +33,23 @@ namespace gbn {
             kWide, NT, U, 1, 1, NT, VecTraits<GBN_T>::E, MINB, 0},
 #define GBN_W_RMS(NT, U, MINB, PF) GBN_WIDE(false, NT, U, MINB, PF)
 #define GBN_W_LN(NT, U, MINB, PF) GBN_WIDE(true, NT, U, MINB, PF)
+#define GBN_ROWS_S(LN, TPR, VPT, CTA, MINB)                                                    \
+    Variant{GBN_FWD_S_VNAME(TPR, VPT, CTA, MINB), (const void *)&fwd_rows_s<GBN_T, LN, TPR, VPT, CTA, MINB>, \
+            kRowsS, TPR, VPT, 1, 1, CTA, VecTraits<GBN_T>::E, MINB, 0},
+#define GBN_S_RMS(TPR, VPT, CTA, MINB) GBN_ROWS_S(false, TPR, VPT, CTA, MINB)
+#define GBN_S_LN(TPR, VPT, CTA, MINB) GBN_ROWS_S(true, TPR, VPT, CTA, MINB)
 static const Variant rms_variants[] = {
     GBN_TMA_FWD_GEOMS(GBN_T_RMS)
     GBN_TMAC_FWD_GEOMS(GBN_C_RMS)
     GBN_WIDE_FWD_GEOMS(GBN_W_RMS)
+    GBN_FWD_S_GEOMS(GBN_S_RMS)
     GBN_FWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
     GBN_TMA_FWD_GEOMS(GBN_T_LN)
     GBN_TMAC_FWD_GEOMS(GBN_C_LN)
     GBN_WIDE_FWD_GEOMS(GBN_W_LN)
+    GBN_FWD_S_GEOMS(GBN_S_LN)
     GBN_FWD_GEOMS(GBN_X_LN)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, true>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 const VariantTable GBN_CAT(kFwdRms_, GBN_SFX) = {rms_variants, (int)(sizeof(rms_variants) / sizeof(Variant))};
@@ -59,6 +66,9 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_WIDE
 #undef GBN_W_RMS
 #undef GBN_W_LN
+#undef GBN_ROWS_S
+#undef GBN_S_RMS
+#undef GBN_S_LN
 #endif
 
 #ifdef GBN_BWD
@@ -82,14 +92,21 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
             kWide, NT, U, 1, CL, NT, VecTraits<GBN_T>::E, 1, 0},
 #define GBN_W_RMS(NT, U, CL, PF, F) GBN_BWIDE(false, NT, U, CL, PF, F)
 #define GBN_W_LN(NT, U, CL, PF, F) GBN_BWIDE(true, NT, U, CL, PF, F)
+#define GBN_TMP(LN, TPR, VPT, NT)                                                              \
+    Variant{GBN_TMP_VNAME(TPR, VPT, NT), (const void *)&bwd_tmp<GBN_T, LN, TPR, VPT, NT>, kTmaP, TPR, \
+            VPT, 0, 1, NT, VecTraits<GBN_T>::E, 1, 32768},
+#define GBN_P_RMS(TPR, VPT, NT) GBN_TMP(false, TPR, VPT, NT)
+#define GBN_P_LN(TPR, VPT, NT) GBN_TMP(true, TPR, VPT, NT)
 static const Variant rms_variants[] = {
     GBN_TMA_BWD_GEOMS(GBN_T_RMS)
+    GBN_TMP_BWD_GEOMS(GBN_P_RMS)
     GBN_TMAC_BWD_GEOMS(GBN_C_RMS)
     GBN_WIDE_BWD_GEOMS(GBN_W_RMS)
     GBN_BWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&bwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
     GBN_TMA_BWD_GEOMS(GBN_T_LN)
+    GBN_TMP_BWD_GEOMS(GBN_P_LN)
     GBN_TMAC_BWD_GEOMS(GBN_C_LN)
     GBN_WIDE_BWD_GEOMS(GBN_W_LN)
     GBN_BWD_GEOMS(GBN_X_LN)
@@ -99,6 +116,9 @@ const VariantTable GBN_CAT(kBwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_BWIDE
 #undef GBN_W_RMS
 #undef GBN_W_LN
+#undef GBN_TMP
+#undef GBN_P_RMS
+#undef GBN_P_LN
 #endif
 
 }  // namespace gbn

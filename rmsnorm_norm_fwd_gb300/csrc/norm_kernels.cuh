@@ -173,6 +173,135 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
     if constexpr (CL > 1) cluster_sync_all();
 }
 
+// ============================================================================ forward, parameters in shared memory
+// As fwd_rows (no cluster, one row per row group per iteration), with gamma
+// (and beta) converted once per CTA to fp32 in shared memory (dynamic,
+// [nv * E] floats each) instead of held packed in registers, and the row
+// converted once to fp32 registers.  Fewer registers per thread (more warps
+// per SM) and about half the instructions per element of fwd_rows for
+// LayerNorm: x is converted once, gamma and beta not at all per row.
+template <typename T, bool LN, int TPR, int VPT, int CTA, int MINB>
+__global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
+    static_assert(CTA % TPR == 0 && TPR % 32 == 0, "bad row-group shape");
+    constexpr int E = VecTraits<T>::E;
+    constexpr int H = E / 4;  // float4 per 16-byte vector
+    constexpr int RPC = CTA / TPR;
+    extern __shared__ __align__(16) float4 pars[];  // gamma [nv * H], then beta [nv * H]
+    __shared__ RowReduceSmem<TPR, RPC, 1, 2> red2;
+    __shared__ RowReduceSmem<TPR, RPC, 1, 1> red1;
+
+    const int t = threadIdx.x % TPR;
+    const int grp = threadIdx.x / TPR;
+    const int64_t nv = p.N / E;
+    const float n = (float)p.N;
+    const bool full = nv == (int64_t)TPR * VPT;  // uniform over the grid
+
+    for (int64_t v = threadIdx.x; v < nv; v += CTA) {
+        const uint4 g = ld_vec(p.gamma, v);
+        uint4 b = make_uint4(0, 0, 0, 0);
+        if constexpr (LN) b = ld_vec(p.beta, v);
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            pars[v * H + h] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
+                                          vget<T>(g, 4 * h + 3));
+            if constexpr (LN)
+                pars[(nv + v) * H + h] = make_float4(vget<T>(b, 4 * h), vget<T>(b, 4 * h + 1),
+                                                     vget<T>(b, 4 * h + 2), vget<T>(b, 4 * h + 3));
+        }
+    }
+    __syncthreads();
+
+    int64_t vid[VPT];
+    bool vok[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        vid[k] = (int64_t)k * TPR + t;
+        vok[k] = vid[k] < nv;
+    }
+    int parity = 0;
+    for (int64_t base = (int64_t)blockIdx.x * RPC; base < p.M; base += (int64_t)gridDim.x * RPC) {
+        const int64_t row = base + grp;
+        const bool rok = row < p.M;
+        float xf[VPT][E];
+        {
+            uint4 q[VPT];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+                q[k] = (rok && vok[k]) ? ld_vec(p.x, row * nv + vid[k]) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < E; ++e) xf[k][e] = vget<T>(q[k], e);
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < E; ++e) s += LN ? xf[k][e] : xf[k][e] * xf[k][e];
+        float mean = 0.f, rstd;
+        if (LN && full) {
+            // equal per-thread counts: local mean and M2, one merge (fwd_rows)
+            constexpr float kC = (float)(VPT * E);
+            float mm[1] = {s * (1.f / kC)}, m2[1] = {0.f};
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float d = xf[k][e] - mm[0];
+                    m2[0] += d * d;
+                }
+            row_merge_equal<TPR, RPC, 1>(mm, m2, kC, red2, parity);
+            mean = mm[0];
+            rstd = rsqrtf(m2[0] / n + p.eps);
+        } else {
+            float a[1] = {s};
+            row_allreduce<TPR, RPC, 1, 1>(a, red1, parity);
+            if constexpr (LN) {
+                mean = a[0] / n;
+                a[0] = 0.f;
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    if (!vok[k]) continue;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float d = xf[k][e] - mean;
+                        a[0] += d * d;
+                    }
+                }
+                row_allreduce<TPR, RPC, 1, 1>(a, red1, parity);
+            }
+            rstd = rsqrtf(a[0] / n + p.eps);
+        }
+        if (t == 0 && rok) {
+            if (p.rstd) p.rstd[row] = rstd;
+            if (LN && p.mean) p.mean[row] = mean;
+        }
+        // y = ((x - mean) * rstd) * gamma (+ beta)
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            if (!(rok && vok[k])) continue;
+            float o[E];
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const float4 g = pars[vid[k] * H + h];
+                float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (LN) b = pars[(nv + vid[k]) * H + h];
+                o[4 * h] = ((xf[k][4 * h] - mean) * rstd) * g.x;
+                o[4 * h + 1] = ((xf[k][4 * h + 1] - mean) * rstd) * g.y;
+                o[4 * h + 2] = ((xf[k][4 * h + 2] - mean) * rstd) * g.z;
+                o[4 * h + 3] = ((xf[k][4 * h + 3] - mean) * rstd) * g.w;
+                if constexpr (LN) {
+                    o[4 * h] += b.x;
+                    o[4 * h + 1] += b.y;
+                    o[4 * h + 2] += b.z;
+                    o[4 * h + 3] += b.w;
+                }
+            }
+            st_vec(p.y, row * nv + vid[k], vpack<T>(o));
+        }
+    }
+}
+
 // ============================================================================ backward, row-resident
 // Per row: xhat = (x - mean) * rstd, g = dy * gamma, c2 = mean(g * xhat),
 // c1 = mean(g) (LayerNorm), dx = rstd * (g - c1 - xhat * c2).  Each thread

@@ -50,6 +50,8 @@ enum VariantKind : int {
     kTma = 2,   // rows staged through a shared-memory ring by bulk async copies
     kTmaCl = 3, // as kTma, each row split across a thread-block cluster (column slices)
     kWide = 4,  // one CTA per row, the row streamed twice (DRAM, then L2); any row length
+    kRowsS = 5, // as kRows (no cluster), gamma/beta in shared memory as fp32
+    kTmaP = 6,  // as kTma without a producer warp (one thread of the CTA refills the ring)
 };
 
 // One compiled kernel and the geometry the host needs to launch it.
@@ -72,7 +74,8 @@ struct Variant {
     }
     // Threads of a CTA that work on rows (TMA kinds add one producer warp).
     int consumers() const { return (kind == kTma || kind == kTmaCl) ? cta - 32 : cta; }
-    int rows_per_cta_iter() const { return kind == kRows ? (cta / tpr) * rows : 1; }
+    bool staged_rows() const { return kind == kTma || kind == kTmaP; }
+    int rows_per_cta_iter() const { return (kind == kRows || kind == kRowsS) ? (cta / tpr) * rows : 1; }
 };
 
 struct VariantTable {

@@ -282,8 +282,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
     TmaHeader &h = *reinterpret_cast<TmaHeader *>(smem);
     const int64_t M = p.M, nv = p.N / E;
     const size_t row_bytes = (size_t)p.N * sizeof(T);
-    uint4 *par = reinterpret_cast<uint4 *>(smem + kTmaHeaderBytes);  // gamma [nv]
-    unsigned char *stages = smem + kTmaHeaderBytes + tma_param_bytes((int64_t)row_bytes, false);
+    constexpr int H = E / 4;  // float4 per 16-byte vector
+    float4 *gpar = reinterpret_cast<float4 *>(smem + kTmaHeaderBytes);  // gamma as fp32 [nv * H]
+    unsigned char *stages = smem + kTmaHeaderBytes + tma_param_bytes(p.N * 4, false);
     const int S = p.tc.stages, RT = p.tc.rows;
     const uint32_t tile_bytes = (uint32_t)((RT * row_bytes + 127) & ~(size_t)127);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -300,26 +301,45 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
     __syncthreads();
 
     if (warp == CW) {
-        if (lane == 0) {
-            load_params(&h.pbar, par, nullptr, p.gamma, nullptr, (uint32_t)row_bytes);
+        if (lane == 0)
             tma_produce<true, LN>(h, stages, p.tc, M, row_bytes, p.x, p.dy, p.rstd, p.mean, tile_bytes);
-        }
         return;
     }
 
-    mbar_wait_bounded(&h.pbar, 0, &h.abort, p.tc.fault);
-    const uint4 *gs = par;
+    // gamma, widened to fp32 once per CTA by the consumers.
+    for (int64_t v = threadIdx.x; v < nv; v += NT) {
+        const uint4 g = ld_vec(p.gamma, v);
+#pragma unroll
+        for (int hh = 0; hh < H; ++hh)
+            gpar[v * H + hh] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
+                                           vget<T>(g, 4 * hh + 3));
+    }
+    named_sync(kTmaBarAll, NT);
     const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
     float *scratch = h.red + grp * (2 * NS * WPR);
-    // HOLD: this thread's gamma, widened once (its columns never change).
+    // gamma of vector v of this thread's columns, as E floats.
+    auto gamma_of = [&](int v, float (&g)[E]) {
+#pragma unroll
+        for (int hh = 0; hh < H; ++hh) {
+            const float4 q = gpar[v * H + hh];
+            g[4 * hh] = q.x;
+            g[4 * hh + 1] = q.y;
+            g[4 * hh + 2] = q.z;
+            g[4 * hh + 3] = q.w;
+        }
+    };
+    // HOLD: this thread's gamma, kept in registers (its columns never change).
     float gf[HOLD ? VPT : 1][E];
     if constexpr (HOLD) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * TPR + t;
-            const uint4 g = v < nv ? lds128(gs + v) : make_uint4(0, 0, 0, 0);
+            if (v < nv) {
+                gamma_of(v, gf[k]);
+            } else {
 #pragma unroll
-            for (int e = 0; e < E; ++e) gf[k][e] = vget<T>(g, e);
+                for (int e = 0; e < E; ++e) gf[k][e] = 0.f;
+            }
         }
     }
     const float n = (float)p.N;
@@ -356,10 +376,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
                 rstd = in_win ? st[row] : __ldg(p.rstd + row);
                 if constexpr (LN) mean = in_win ? st[stat_stride(RT) + row] : __ldg(p.mean + row);
             }
-            // Pass 1: x-hat and g = dy * gamma, their products summed over the
-            // row.  With at most 24 elements per thread (HOLD) x-hat, g and the
-            // raw dy stay in registers for pass 2; otherwise pass 2 re-reads the
-            // staged row.
+            // Pass 1: g = dy * gamma and the row sums of g (x - mean) and g;
+            // sum g xhat = rstd * sum g (x - mean).  With at most 24 elements
+            // per thread (HOLD) x - mean, g and the raw dy stay in registers for
+            // pass 2; otherwise pass 2 re-reads the staged row.
             float sum[NS];
 #pragma unroll
             for (int i = 0; i < NS; ++i) sum[i] = 0.f;
@@ -371,28 +391,36 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
                 const bool ok = rok && v < nv;
                 const uint4 q = ok ? lds128(xs + v) : make_uint4(0, 0, 0, 0);
                 const uint4 d = ok ? lds128(ds + v) : make_uint4(0, 0, 0, 0);
-                uint4 g = make_uint4(0, 0, 0, 0);
+                float gk[E];
                 if constexpr (HOLD) {
                     hd[k] = d;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) gk[e] = gf[HOLD ? k : 0][e];
+                } else if (ok) {
+                    gamma_of(v, gk);
                 } else {
-                    g = ok ? lds128(gs + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) gk[e] = 0.f;
                 }
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    const float xh = (vget<T>(q, e) - mean) * rstd;
-                    const float gg = vget<T>(d, e) * (HOLD ? gf[HOLD ? k : 0][e] : vget<T>(g, e));
+                    const float xc = vget<T>(q, e) - mean;
+                    const float gg = vget<T>(d, e) * gk[e];
                     if constexpr (HOLD) {
-                        hx[k][e] = xh;
+                        hx[k][e] = xc;
                         hg[k][e] = gg;
                     }
-                    sum[0] += gg * xh;
+                    sum[0] += gg * xc;
                     if constexpr (LN) sum[NS - 1] += gg;
                 }
             }
             group_allreduce<TPR, NS>(sum, scratch, parity, 1 + grp);
             if (!rok) continue;  // uniform per row group: no collective below
-            const float c2 = sum[0] / n;
-            const float c1 = LN ? sum[NS - 1] / n : 0.f;
+            // dx = rstd (g - c1 - xhat c2) = rstd g - rstd c1 - (rstd c2) xhat,
+            // c2 = rstd sum g (x - mean) / n, c1 = sum g / n.
+            const float c2 = rstd * sum[0] / n;
+            const float rc1 = LN ? rstd * (sum[NS - 1] / n) : 0.f;
+            const float rc2 = rstd * c2;
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * TPR + t;
@@ -402,18 +430,21 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
                         const float dyv = vget<T>(hd[k], e);
-                        o[e] = rstd * (hg[k][e] - c1 - hx[k][e] * c2);
-                        accg[k][e] += dyv * hx[k][e];
+                        const float xh = hx[k][e] * rstd;
+                        o[e] = fmaf(-rc2, xh, fmaf(rstd, hg[k][e], -rc1));
+                        accg[k][e] += dyv * xh;
                         if constexpr (LN) accb[k][e] += dyv;
                     }
                 } else {
-                    const uint4 q = lds128(xs + v), d = lds128(ds + v), g = lds128(gs + v);
+                    const uint4 q = lds128(xs + v), d = lds128(ds + v);
+                    float gk[E];
+                    gamma_of(v, gk);
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
                         const float xh = (vget<T>(q, e) - mean) * rstd;
                         const float dyv = vget<T>(d, e);
-                        const float gg = dyv * vget<T>(g, e);
-                        o[e] = rstd * (gg - c1 - xh * c2);
+                        const float gg = dyv * gk[e];
+                        o[e] = fmaf(-rc2, xh, fmaf(rstd, gg, -rc1));
                         accg[k][e] += dyv * xh;
                         if constexpr (LN) accb[k][e] += dyv;
                     }
@@ -464,6 +495,272 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
             for (int e = 0; e < E; ++e) {
                 wsg[v * E + e] = accg[k][e];
                 if constexpr (LN) wsb[v * E + e] = accb[k][e];
+            }
+        }
+    }
+}
+
+// ============================================================================ backward, no producer warp
+// As bwd_tma without a producer warp: the CTA's NT threads form RPP = NT / TPR
+// row groups, and each group runs its own pipeline over its share of the
+// CTA's tiles (group g takes the CTA's tiles g, g + RPP, ...) through its own
+// S / RPP stages of the ring, refilled by the group's first thread.  The
+// group barrier inside the first row's reduction of the group's tile j
+// follows every group thread's last read of tile j - 1's stage, so right
+// after it that thread issues the copy of tile j - 1 + S / RPP into it.
+// Without a 17th warp the register budget is 65536 / NT per thread (128 for
+// 512 threads), which holds the dgamma and dbeta partials and, for up to 24
+// elements per thread, the pass-1 values (x - mean, g and dy) for pass 2.
+template <typename T, bool LN, int TPR, int VPT, int NT>
+__global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
+    pdl_launch_dependents();  // the column reduce waits for this grid's completion
+    constexpr int E = VecTraits<T>::E;
+    constexpr int H = E / 4;
+    constexpr int NS = LN ? 2 : 1;
+    constexpr int RPP = NT / TPR;
+    constexpr int WPR = TPR / 32;
+    constexpr bool HOLD = VPT * E <= 24;
+    // TPR > 32: the group reduction is a named barrier, which the refill relies on
+    static_assert(NT % TPR == 0 && TPR % 32 == 0 && TPR > 32 && RPP <= 14, "CTA shape");
+    static_assert(RPP * 2 * NS * WPR <= (int)(sizeof(TmaHeader::red) / 4), "scratch");
+    extern __shared__ __align__(128) unsigned char smem[];
+    TmaHeader &h = *reinterpret_cast<TmaHeader *>(smem);
+    const int64_t M = p.M, nv = p.N / E;
+    const size_t row_bytes = (size_t)p.N * sizeof(T);
+    float4 *gpar = reinterpret_cast<float4 *>(smem + kTmaHeaderBytes);  // gamma as fp32 [nv * H]
+    unsigned char *stages = smem + kTmaHeaderBytes + tma_param_bytes(p.N * 4, false);
+    const int SG = p.tc.stages / RPP, RT = p.tc.rows;  // stages per row group
+    const uint32_t tile_bytes = (uint32_t)((RT * row_bytes + 127) & ~(size_t)127);
+    const int64_t ntiles = (M + RT - 1) / RT;
+    const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
+    float *scratch = h.red + grp * (2 * NS * WPR);
+    volatile int *abort_flag = &h.abort;
+    int issued = 0;  // group leader: copies issued
+
+    // The CTA tile of the group's j-th tile, or -1.
+    auto tile_of = [&](int64_t j) {
+        const int64_t tile = blockIdx.x + (grp + j * RPP) * (int64_t)gridDim.x;
+        return tile < ntiles ? tile : (int64_t)-1;
+    };
+    // Copy the group's j-th tile into its stage j % SG (group leader).
+    auto issue = [&](int64_t j) {
+        const int64_t tile = tile_of(j);
+        if (tile < 0) return;
+        const int s = grp * SG + (int)(j % SG);
+        const int64_t r0 = tile * RT;
+        const int rows = (int)(M - r0 < RT ? M - r0 : RT);
+        const uint32_t bytes = (uint32_t)(rows * row_bytes);
+        unsigned char *dst = stages + (size_t)s * p.tc.stride;
+        int64_t wa, wb;
+        stat_window(r0, rows, M, &wa, &wb);
+        mbar_arrive_expect_tx(&h.full[s], 2 * bytes + (uint32_t)(wb - wa) * 4u * (LN ? 2u : 1u));
+        bulk_g2s(dst, static_cast<const unsigned char *>(p.x) + r0 * row_bytes, bytes, &h.full[s]);
+        bulk_g2s(dst + tile_bytes, static_cast<const unsigned char *>(p.dy) + r0 * row_bytes, bytes, &h.full[s]);
+        if (wb > wa) {
+            float *sd = reinterpret_cast<float *>(dst + 2 * (size_t)tile_bytes);
+            bulk_g2s(sd, p.rstd + wa, (uint32_t)(wb - wa) * 4u, &h.full[s]);
+            if constexpr (LN) bulk_g2s(sd + stat_stride(RT), p.mean + wa, (uint32_t)(wb - wa) * 4u, &h.full[s]);
+        }
+        ++issued;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RPP * SG; ++s) mbar_init(&h.full[s], 1);
+        h.abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (t == 0)
+        for (int j = 0; j < SG; ++j) issue(j);
+    for (int64_t v = threadIdx.x; v < nv; v += NT) {
+        const uint4 g = ld_vec(p.gamma, v);
+#pragma unroll
+        for (int hh = 0; hh < H; ++hh)
+            gpar[v * H + hh] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
+                                           vget<T>(g, 4 * hh + 3));
+    }
+    __syncthreads();
+    auto gamma_of = [&](int v, float (&g)[E]) {
+#pragma unroll
+        for (int hh = 0; hh < H; ++hh) {
+            const float4 q = gpar[v * H + hh];
+            g[4 * hh] = q.x;
+            g[4 * hh + 1] = q.y;
+            g[4 * hh + 2] = q.z;
+            g[4 * hh + 3] = q.w;
+        }
+    };
+    float gf[HOLD ? VPT : 1][E];
+    if constexpr (HOLD) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * TPR + t;
+            if (v < nv) {
+                gamma_of(v, gf[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) gf[k][e] = 0.f;
+            }
+        }
+    }
+    const float n = (float)p.N;
+    float accg[VPT][E], accb[LN ? VPT : 1][E];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            accg[k][e] = 0.f;
+            if constexpr (LN) accb[k][e] = 0.f;
+        }
+    int parity = 0;
+    // Trip count uniform over the CTA (the epilogue's barriers); groups past
+    // their last tile idle through the remaining iterations.
+    const int64_t my_tiles = blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    for (int64_t j = 0; j < (my_tiles + RPP - 1) / RPP; ++j) {
+        const int64_t tile = tile_of(j);
+        if (tile < 0) break;  // uniform per group (named barriers only below)
+        const int s = grp * SG + (int)(j % SG);
+        mbar_wait_bounded(&h.full[s], (uint32_t)((j / SG) & 1), abort_flag, p.tc.fault);
+        const int64_t r0 = tile * RT;
+        const int rows = (int)(M - r0 < RT ? M - r0 : RT);
+        int64_t wa, wb;
+        stat_window(r0, rows, M, &wa, &wb);
+        const unsigned char *tb = stages + (size_t)s * p.tc.stride;
+        const float *st = reinterpret_cast<const float *>(tb + 2 * (size_t)tile_bytes) - wa;
+        for (int r = 0; r < rows; ++r) {  // every thread of the group works on the same row
+            const uint4 *xs = reinterpret_cast<const uint4 *>(tb + (size_t)r * row_bytes);
+            const uint4 *ds = reinterpret_cast<const uint4 *>(tb + tile_bytes + (size_t)r * row_bytes);
+            const int64_t row = r0 + r;
+            const bool in_win = row < wb;
+            const float rstd = in_win ? st[row] : __ldg(p.rstd + row);
+            const float mean = LN ? (in_win ? st[stat_stride(RT) + row] : __ldg(p.mean + row)) : 0.f;
+            float sum[NS];
+#pragma unroll
+            for (int q = 0; q < NS; ++q) sum[q] = 0.f;
+            float hx[HOLD ? VPT : 1][E], hg[HOLD ? VPT : 1][E];
+            uint4 hd[HOLD ? VPT : 1];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = k * TPR + t;
+                const bool ok = v < nv;
+                const uint4 q = ok ? lds128(xs + v) : make_uint4(0, 0, 0, 0);
+                const uint4 d = ok ? lds128(ds + v) : make_uint4(0, 0, 0, 0);
+                float gk[E];
+                if constexpr (HOLD) {
+                    hd[k] = d;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) gk[e] = gf[HOLD ? k : 0][e];
+                } else if (ok) {
+                    gamma_of(v, gk);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) gk[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float xc = vget<T>(q, e) - mean;
+                    const float gg = vget<T>(d, e) * gk[e];
+                    if constexpr (HOLD) {
+                        hx[k][e] = xc;
+                        hg[k][e] = gg;
+                    }
+                    sum[0] += gg * xc;
+                    if constexpr (LN) sum[NS - 1] += gg;
+                }
+            }
+            group_allreduce<TPR, NS>(sum, scratch, parity, 1 + grp);
+            if (r == 0 && j >= 1 && t == 0) {
+                // Every thread of the group is past its last read of the
+                // stage of its tile j - 1: order those reads before the bulk
+                // copy's writes, then refill.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(j - 1 + SG);
+            }
+            const float c2 = rstd * sum[0] / n;
+            const float rc1 = LN ? rstd * (sum[NS - 1] / n) : 0.f;
+            const float rc2 = rstd * c2;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = k * TPR + t;
+                if (v >= nv) continue;
+                float o[E];
+                if constexpr (HOLD) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float dyv = vget<T>(hd[k], e);
+                        const float xh = hx[k][e] * rstd;
+                        o[e] = fmaf(-rc2, xh, fmaf(rstd, hg[k][e], -rc1));
+                        accg[k][e] += dyv * xh;
+                        if constexpr (LN) accb[k][e] += dyv;
+                    }
+                } else {
+                    const uint4 q = lds128(xs + v), d = lds128(ds + v);
+                    float gk[E];
+                    gamma_of(v, gk);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float xh = (vget<T>(q, e) - mean) * rstd;
+                        const float dyv = vget<T>(d, e);
+                        o[e] = fmaf(-rc2, xh, fmaf(rstd, dyv * gk[e], -rc1));
+                        accg[k][e] += dyv * xh;
+                        if constexpr (LN) accb[k][e] += dyv;
+                    }
+                }
+                st_vec(p.dx, row * nv + v, vpack<T>(o));
+            }
+        }
+    }
+    if (t == 0 && *abort_flag) {
+        // Copies still landing after an aborted wait: wait for each (bounded)
+        // before the CTA may exit.
+        int zero = 0;
+        for (int j = issued > SG ? issued - SG : 0; j < issued; ++j)
+            mbar_wait_bounded(&h.full[grp * SG + j % SG], (uint32_t)((j / SG) & 1),
+                              reinterpret_cast<volatile int *>(&zero), nullptr);
+    }
+
+    // Epilogue: this CTA's partial row.  With several row groups (same
+    // columns), every group writes its partials to the idle ring, then each
+    // thread adds, for its columns, the groups' values in group order.
+    float *wsg = p.ws + (int64_t)blockIdx.x * p.N;
+    float *wsb = p.ws + ((int64_t)gridDim.x + blockIdx.x) * p.N;
+    if constexpr (RPP > 1) {
+        constexpr int CAP = TPR * VPT * E;
+        float *comb = reinterpret_cast<float *>(stages);  // [NS][RPP][CAP]
+        __syncthreads();  // every group is done with the ring
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int c = (k * TPR + t) * E + e;
+                comb[grp * CAP + c] = accg[k][e];
+                if constexpr (LN) comb[(RPP + grp) * CAP + c] = accb[k][e];
+            }
+        __syncthreads();
+        const int64_t ncol = nv * E < CAP ? nv * E : CAP;
+        for (int c = threadIdx.x; c < ncol; c += NT) {
+            float sg = 0.f, sb = 0.f;
+#pragma unroll
+            for (int gi = 0; gi < RPP; ++gi) {
+                sg += comb[gi * CAP + c];
+                if constexpr (LN) sb += comb[(RPP + gi) * CAP + c];
+            }
+            wsg[c] = sg;
+            if constexpr (LN) wsb[c] = sb;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t v = (int64_t)k * TPR + t;
+            if (v >= nv) continue;
+            float4 *g4 = reinterpret_cast<float4 *>(wsg + v * E);
+            float4 *b4 = reinterpret_cast<float4 *>(wsb + v * E);
+#pragma unroll
+            for (int hh = 0; hh < H; ++hh) {
+                g4[hh] = make_float4(accg[k][4 * hh], accg[k][4 * hh + 1], accg[k][4 * hh + 2], accg[k][4 * hh + 3]);
+                if constexpr (LN)
+                    b4[hh] = make_float4(accb[k][4 * hh], accb[k][4 * hh + 1], accb[k][4 * hh + 2],
+                                         accb[k][4 * hh + 3]);
             }
         }
     }

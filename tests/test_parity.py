@@ -36,6 +36,14 @@ def _geom(name):
     m = re.fullmatch(r"(\d+)x(\d+)r(\d+)c(\d+)b(\d+)", name)
     if m:
         return tuple(int(v) for v in m.groups()) + (False,)
+    m = re.fullmatch(r"s(\d+)x(\d+)b(\d+)m(\d+)", name)
+    if m:
+        tpr, vpt, cta, _ = (int(v) for v in m.groups())
+        return (tpr, vpt, 1, 1, cta, False)
+    m = re.fullmatch(r"tmp(\d+)x(\d+)b(\d+)", name)
+    if m:
+        tpr, vpt, nt = (int(v) for v in m.groups())
+        return (tpr, vpt, 1, 1, nt, True)
     m = re.fullmatch(r"tma(\d+)x(\d+)w(\d+)", name)
     if m:
         tpr, vpt, cw = (int(v) for v in m.groups())
