@@ -114,8 +114,10 @@ bool tma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, si
     const int ntens = c.dir == 0 ? 1 : 2;
     auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
     // Header, then gamma (and beta for the LayerNorm forward), then the ring.
-    // (the backward keeps gamma widened to fp32)
-    const size_t params = c.dir == 0 ? al(row_bytes) * (c.is_ln ? 2 : 1) : al((size_t)c.N * 4);
+    // The backward kernels and the kernels without a producer warp keep them
+    // widened to fp32.
+    const size_t pbytes = (c.dir == 1 || v.kind == kTmaP) ? (size_t)c.N * 4 : row_bytes;
+    const size_t params = al(pbytes) * ((c.dir == 0 && c.is_ln) ? 2 : 1);
     const size_t budget_all = (size_t)g_dev[dev].smem_optin / (size_t)v.ctas_per_sm;
     if (budget_all <= (size_t)kTmaHeaderBytes + params + 1024) return false;
     const size_t budget = budget_all - kTmaHeaderBytes - params;

@@ -371,113 +371,107 @@ __device__ __forceinline__ void group_allreduce(float (&v)[R], float *scratch, i
     parity ^= 1;
 }
 
-// ---------------------------------------------------------------- equal-count mean / M2 merge
-// For LayerNorm rows that fill a row group exactly, every thread holds the
-// same number c of elements, so two partners of a butterfly level always
-// merge equal counts: by the pairwise update of Chan, Golub and LeVeque
-// (1979) the merged mean is (ma + mb) / 2 (exact halving) and
-// M2 = M2a + M2b + (ma - mb)^2 * c / 2 -- no division.  Both partners compute
-// identical bits (commutative sums, the difference only squared, and the
-// round-to-nearest intrinsics prevent a contracted multiply-add from rounding
-// differently on each side).
-__device__ __forceinline__ void merge_equal(float &mean, float &m2, float om, float om2, float half_c) {
-    const float d = __fsub_rn(om, mean);
-    m2 = __fadd_rn(__fadd_rn(m2, om2), __fmul_rn(__fmul_rn(d, d), half_c));
-    mean = __fmul_rn(0.5f, __fadd_rn(mean, om));
-}
-
-// Row-group merge of R rows' (mean, M2) for a CTA without a cluster: lane
-// butterfly, then the WPR warps of the group through shared memory as a
-// pairwise tree (equal counts at every level; WPR is a power of two).
-// `c` is the per-thread element count.  All threads of the CTA call it.
+// ---------------------------------------------------------------- equal-count group combine
+// (mean, M2) of a row from the threads' (mean_t, M2_t) when every thread holds
+// the same count c: the union of groups of equal size k has mean
+// M = (1/G) sum m_g and M2 = sum (M2_g + k (m_g - M)^2) (the group form of the
+// update of Chan, Golub and LeVeque; exact algebra, centred on the union's
+// mean).  Applied twice: over the lanes of a warp (butterfly sums, every lane
+// identical bits), then over the warps of the row group through shared
+// memory (every thread adds the warps in index order).  About half the
+// instructions of merging pairs level by level.
 template <int TPR, int RPC, int R>
-__device__ __forceinline__ void row_merge_equal(float (&mean)[R], float (&m2)[R], float c,
-                                                RowReduceSmem<TPR, RPC, 1, 2 * R> &sm, int &parity) {
+__device__ __forceinline__ void row_meanvar_equal(float (&mean)[R], float (&m2)[R], float c,
+                                                  RowReduceSmem<TPR, RPC, 1, 2 * R> &sm, int &parity) {
+    constexpr int L = TPR < 32 ? TPR : 32;  // lanes per warp in the group
+    float s[R], q[R];
 #pragma unroll
-    for (int o = 1; o < (TPR < 32 ? TPR : 32); o <<= 1) {
+    for (int r = 0; r < R; ++r) s[r] = mean[r];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float om = __shfl_xor_sync(0xffffffffu, mean[r], o);
-            const float om2 = __shfl_xor_sync(0xffffffffu, m2[r], o);
-            merge_equal(mean[r], m2[r], om, om2, 0.5f * c);
-        }
-        c *= 2.f;
+    for (int o = 1; o < L; o <<= 1)
+#pragma unroll
+        for (int r = 0; r < R; ++r) s[r] += __shfl_xor_sync(0xffffffffu, s[r], o);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const float mw = s[r] * (1.f / L);
+        const float d = mean[r] - mw;
+        q[r] = m2[r] + c * (d * d);
+        mean[r] = mw;
     }
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1)
+#pragma unroll
+        for (int r = 0; r < R; ++r) q[r] += __shfl_xor_sync(0xffffffffu, q[r], o);
+#pragma unroll
+    for (int r = 0; r < R; ++r) m2[r] = q[r];
     if constexpr (TPR > 32) {
         constexpr int WPR = TPR / 32;
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const int grp = threadIdx.x / TPR, wig = warp % WPR;
-        float *buf = sm.warp_part + parity * (RPC * 2 * R * WPR);
+        float2 *buf = reinterpret_cast<float2 *>(sm.warp_part + parity * (RPC * 2 * R * WPR)) + grp * R * WPR;
         if (lane == 0) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                buf[((grp * R + r) * 2) * WPR + wig] = mean[r];
-                buf[((grp * R + r) * 2 + 1) * WPR + wig] = m2[r];
-            }
+            for (int r = 0; r < R; ++r) buf[r * WPR + wig] = make_float2(mean[r], m2[r]);
         }
         __syncthreads();
+        const float cw = c * 32.f;  // count per warp
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const float *bm = buf + ((grp * R + r) * 2) * WPR;
-            const float *b2 = bm + WPR;
-            float tm[WPR], t2[WPR];
+            float ms = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPR; ++w) ms += buf[r * WPR + w].x;
+            const float M = ms * (1.f / WPR);
+            float t2 = 0.f;
 #pragma unroll
             for (int w = 0; w < WPR; ++w) {
-                tm[w] = bm[w];
-                t2[w] = b2[w];
+                const float2 b = buf[r * WPR + w];
+                const float dd = b.x - M;
+                t2 += b.y + cw * (dd * dd);
             }
-            float cc = c;
-#pragma unroll
-            for (int step = 1; step < WPR; step <<= 1) {
-#pragma unroll
-                for (int w = 0; w + step < WPR; w += 2 * step)
-                    merge_equal(tm[w], t2[w], tm[w + step], t2[w + step], 0.5f * cc);
-                cc *= 2.f;
-            }
-            mean[r] = tm[0];
-            m2[r] = t2[0];
+            mean[r] = M;
+            m2[r] = t2;
         }
     }
     parity ^= 1;
 }
 
-// Equal-count (mean, M2) merge over a row group of TPR consecutive threads that
-// does not span the whole CTA (TPR > 32: warps through `scratch`, this group's
-// [2][2][TPR/32] floats, as a pairwise tree under named barrier bar_id).
+// The same combine over a row group of TPR consecutive threads that does not
+// span the whole CTA (TPR > 32: warps through `scratch`, this group's
+// [2][WPR] float2, under named barrier bar_id).
 template <int TPR>
-__device__ __forceinline__ void group_merge_equal(float &mean, float &m2, float c, float *scratch,
-                                                  int &parity, int bar_id) {
+__device__ __forceinline__ void group_meanvar_equal(float &mean, float &m2, float c, float *scratch,
+                                                    int &parity, int bar_id) {
+    constexpr int L = TPR < 32 ? TPR : 32;
+    float s = mean;
 #pragma unroll
-    for (int o = 1; o < (TPR < 32 ? TPR : 32); o <<= 1) {
-        const float om = __shfl_xor_sync(0xffffffffu, mean, o);
-        const float om2 = __shfl_xor_sync(0xffffffffu, m2, o);
-        merge_equal(mean, m2, om, om2, 0.5f * c);
-        c *= 2.f;
-    }
+    for (int o = 1; o < L; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float mw = s * (1.f / L);
+    const float d = mean - mw;
+    float q = m2 + c * (d * d);
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    mean = mw;
+    m2 = q;
     if constexpr (TPR > 32) {
         constexpr int WPR = TPR / 32;
         const int wig = (threadIdx.x % TPR) >> 5, lane = threadIdx.x & 31;
-        float *buf = scratch + parity * (2 * WPR);
-        if (lane == 0) {
-            buf[wig] = mean;
-            buf[WPR + wig] = m2;
-        }
+        float2 *buf = reinterpret_cast<float2 *>(scratch) + parity * WPR;
+        if (lane == 0) buf[wig] = make_float2(mw, q);
         named_sync(bar_id, TPR);
-        float tm[WPR], t2[WPR];
+        const float cw = c * 32.f;
+        float ms = 0.f;
+#pragma unroll
+        for (int w = 0; w < WPR; ++w) ms += buf[w].x;
+        const float M = ms * (1.f / WPR);
+        float t2 = 0.f;
 #pragma unroll
         for (int w = 0; w < WPR; ++w) {
-            tm[w] = buf[w];
-            t2[w] = buf[WPR + w];
+            const float2 b = buf[w];
+            const float dd = b.x - M;
+            t2 += b.y + cw * (dd * dd);
         }
-#pragma unroll
-        for (int step = 1; step < WPR; step <<= 1) {
-#pragma unroll
-            for (int w = 0; w + step < WPR; w += 2 * step)
-                merge_equal(tm[w], t2[w], tm[w + step], t2[w + step], 0.5f * c);
-            c *= 2.f;
-        }
-        mean = tm[0];
-        m2 = t2[0];
+        mean = M;
+        m2 = t2;
     }
     parity ^= 1;
 }

@@ -38,7 +38,13 @@ namespace gbn {
             kRowsS, TPR, VPT, 1, 1, CTA, VecTraits<GBN_T>::E, MINB, 0},
 #define GBN_S_RMS(TPR, VPT, CTA, MINB) GBN_ROWS_S(false, TPR, VPT, CTA, MINB)
 #define GBN_S_LN(TPR, VPT, CTA, MINB) GBN_ROWS_S(true, TPR, VPT, CTA, MINB)
+#define GBN_FTMP(LN, TPR, VPT, NT)                                                             \
+    Variant{GBN_TMP_VNAME(TPR, VPT, NT), (const void *)&fwd_tmp<GBN_T, LN, TPR, VPT, NT>, kTmaP, TPR, \
+            VPT, 0, 1, NT, VecTraits<GBN_T>::E, 1, 32768},
+#define GBN_FP_RMS(TPR, VPT, NT) GBN_FTMP(false, TPR, VPT, NT)
+#define GBN_FP_LN(TPR, VPT, NT) GBN_FTMP(true, TPR, VPT, NT)
 static const Variant rms_variants[] = {
+    GBN_TMP_FWD_GEOMS(GBN_FP_RMS)
     GBN_TMA_FWD_GEOMS(GBN_T_RMS)
     GBN_TMAC_FWD_GEOMS(GBN_C_RMS)
     GBN_WIDE_FWD_GEOMS(GBN_W_RMS)
@@ -46,6 +52,7 @@ static const Variant rms_variants[] = {
     GBN_FWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
+    GBN_TMP_FWD_GEOMS(GBN_FP_LN)
     GBN_TMA_FWD_GEOMS(GBN_T_LN)
     GBN_TMAC_FWD_GEOMS(GBN_C_LN)
     GBN_WIDE_FWD_GEOMS(GBN_W_LN)
@@ -69,6 +76,9 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_ROWS_S
 #undef GBN_S_RMS
 #undef GBN_S_LN
+#undef GBN_FTMP
+#undef GBN_FP_RMS
+#undef GBN_FP_LN
 #endif
 
 #ifdef GBN_BWD

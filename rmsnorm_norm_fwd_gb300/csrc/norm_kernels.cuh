@@ -39,8 +39,8 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
     constexpr int E = VecTraits<T>::E;
     constexpr int RPC = CTA / TPR;
     // LayerNorm rows that fill the row group exactly (no cluster) take one
-    // equal-count (mean, M2) merge; otherwise the mean first, then the centred
-    // sum of squares.
+    // equal-count (mean, M2) combine; otherwise the mean first, then the
+    // centred sum of squares.
     constexpr bool MERGE = LN && CL == 1;
     __shared__ RowReduceSmem<TPR, RPC, CL, MERGE ? 2 * R : 1> red2;
     __shared__ RowReduceSmem<TPR, RPC, CL, R> red;
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
         float mean[R], rstd[R];
         if (MERGE && full) {
             // Every thread holds VPT * E elements of each row: local mean and
-            // M2 from the registers, then one equal-count merge over the row.
+            // M2 from the registers, then one equal-count combine over the row.
             constexpr float kC = (float)(VPT * E);
             float m2[R];
 #pragma unroll
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
                         m2[r] += d * d;
                     }
             }
-            if constexpr (MERGE) row_merge_equal<TPR, RPC, R>(mean, m2, kC, red2, parity);
+            if constexpr (MERGE) row_meanvar_equal<TPR, RPC, R>(mean, m2, kC, red2, parity);
 #pragma unroll
             for (int r = 0; r < R; ++r) rstd[r] = rsqrtf(m2[r] / n + p.eps);
         } else {
@@ -186,7 +186,9 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
     constexpr int E = VecTraits<T>::E;
     constexpr int H = E / 4;  // float4 per 16-byte vector
     constexpr int RPC = CTA / TPR;
-    extern __shared__ __align__(16) float4 pars[];  // gamma [nv * H], then beta [nv * H]
+    // gamma as [H][nv] float4 (plane-major: a warp's 16-byte reads are
+    // consecutive, no bank conflicts), then beta likewise
+    extern __shared__ __align__(16) float4 pars[];
     __shared__ RowReduceSmem<TPR, RPC, 1, 2> red2;
     __shared__ RowReduceSmem<TPR, RPC, 1, 1> red1;
 
@@ -202,10 +204,10 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
         if constexpr (LN) b = ld_vec(p.beta, v);
 #pragma unroll
         for (int h = 0; h < H; ++h) {
-            pars[v * H + h] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
-                                          vget<T>(g, 4 * h + 3));
+            pars[h * nv + v] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
+                                           vget<T>(g, 4 * h + 3));
             if constexpr (LN)
-                pars[(nv + v) * H + h] = make_float4(vget<T>(b, 4 * h), vget<T>(b, 4 * h + 1),
+                pars[(H + h) * nv + v] = make_float4(vget<T>(b, 4 * h), vget<T>(b, 4 * h + 1),
                                                      vget<T>(b, 4 * h + 2), vget<T>(b, 4 * h + 3));
         }
     }
@@ -233,24 +235,28 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
 #pragma unroll
                 for (int e = 0; e < E; ++e) xf[k][e] = vget<T>(q[k], e);
         }
-        float s = 0.f;
+        // four independent accumulation chains per thread (latency)
+        float sa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < E; ++e) s += LN ? xf[k][e] : xf[k][e] * xf[k][e];
+            for (int e = 0; e < E; ++e) sa[e & 3] += LN ? xf[k][e] : xf[k][e] * xf[k][e];
+        const float s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
         float mean = 0.f, rstd;
         if (LN && full) {
-            // equal per-thread counts: local mean and M2, one merge (fwd_rows)
+            // equal per-thread counts: local mean and M2, one combine (fwd_rows)
             constexpr float kC = (float)(VPT * E);
-            float mm[1] = {s * (1.f / kC)}, m2[1] = {0.f};
+            float mm[1] = {s * (1.f / kC)}, m2[1];
+            float qa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const float d = xf[k][e] - mm[0];
-                    m2[0] += d * d;
+                    qa[e & 3] += d * d;
                 }
-            row_merge_equal<TPR, RPC, 1>(mm, m2, kC, red2, parity);
+            m2[0] = (qa[0] + qa[1]) + (qa[2] + qa[3]);
+            row_meanvar_equal<TPR, RPC, 1>(mm, m2, kC, red2, parity);
             mean = mm[0];
             rstd = rsqrtf(m2[0] / n + p.eps);
         } else {
@@ -283,9 +289,9 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
             float o[E];
 #pragma unroll
             for (int h = 0; h < H; ++h) {
-                const float4 g = pars[vid[k] * H + h];
+                const float4 g = pars[h * nv + vid[k]];
                 float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-                if constexpr (LN) b = pars[(nv + vid[k]) * H + h];
+                if constexpr (LN) b = pars[(H + h) * nv + vid[k]];
                 o[4 * h] = ((xf[k][4 * h] - mean) * rstd) * g.x;
                 o[4 * h + 1] = ((xf[k][4 * h + 1] - mean) * rstd) * g.y;
                 o[4 * h + 2] = ((xf[k][4 * h + 2] - mean) * rstd) * g.z;

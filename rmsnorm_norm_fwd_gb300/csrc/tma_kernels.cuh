@@ -200,7 +200,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
             float mean = 0.f;
             if (LN && full) {
                 // Every thread holds VPT * E elements of the row: local mean and
-                // M2 from the staged row, then one equal-count merge.
+                // M2 from the staged row, then one equal-count combine.
                 constexpr float kC = (float)(VPT * E);
                 mean = acc[0] * (1.f / kC);
                 float m2 = 0.f;
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
                         m2 += d * d;
                     }
                 }
-                group_merge_equal<TPR>(mean, m2, kC, scratch, parity, 1 + grp);
+                group_meanvar_equal<TPR>(mean, m2, kC, scratch, parity, 1 + grp);
                 acc[0] = m2;
             } else {
             group_allreduce<TPR, 1>(acc, scratch, parity, 1 + grp);
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
     const int64_t M = p.M, nv = p.N / E;
     const size_t row_bytes = (size_t)p.N * sizeof(T);
     constexpr int H = E / 4;  // float4 per 16-byte vector
-    float4 *gpar = reinterpret_cast<float4 *>(smem + kTmaHeaderBytes);  // gamma as fp32 [nv * H]
+    float4 *gpar = reinterpret_cast<float4 *>(smem + kTmaHeaderBytes);  // gamma as fp32 [H][nv]
     unsigned char *stages = smem + kTmaHeaderBytes + tma_param_bytes(p.N * 4, false);
     const int S = p.tc.stages, RT = p.tc.rows;
     const uint32_t tile_bytes = (uint32_t)((RT * row_bytes + 127) & ~(size_t)127);
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
         const uint4 g = ld_vec(p.gamma, v);
 #pragma unroll
         for (int hh = 0; hh < H; ++hh)
-            gpar[v * H + hh] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
+            gpar[hh * nv + v] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
                                            vget<T>(g, 4 * hh + 3));
     }
     named_sync(kTmaBarAll, NT);
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
     auto gamma_of = [&](int v, float (&g)[E]) {
 #pragma unroll
         for (int hh = 0; hh < H; ++hh) {
-            const float4 q = gpar[v * H + hh];
+            const float4 q = gpar[hh * nv + v];
             g[4 * hh] = q.x;
             g[4 * hh + 1] = q.y;
             g[4 * hh + 2] = q.z;
@@ -500,6 +500,180 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
     }
 }
 
+// ============================================================================ forward, no producer warp
+// Forward counterpart of bwd_tmp: RPP = NT / TPR row groups, each streaming
+// its share of the CTA's tiles of x through its own part of the ring (S /
+// RPP stages), refilled by the group's first thread after the group barrier
+// that follows the last read of the previous tile.  gamma (and beta) sit in
+// shared memory as fp32, converted once per CTA; each row is converted once
+// into fp32 registers.
+template <typename T, bool LN, int TPR, int VPT, int NT>
+__global__ void __launch_bounds__(NT, 1) fwd_tmp(const FwdParams p) {
+    constexpr int E = VecTraits<T>::E;
+    constexpr int H = E / 4;
+    constexpr int RPP = NT / TPR;
+    constexpr int WPR = TPR / 32;
+    static_assert(NT % TPR == 0 && TPR % 32 == 0 && TPR > 32 && RPP <= 14, "CTA shape");
+    static_assert(RPP * 2 * 2 * WPR <= (int)(sizeof(TmaHeader::red) / 4), "scratch");
+    extern __shared__ __align__(128) unsigned char smem[];
+    TmaHeader &h = *reinterpret_cast<TmaHeader *>(smem);
+    const int64_t M = p.M, nv = p.N / E;
+    const size_t row_bytes = (size_t)p.N * sizeof(T);
+    float4 *gpar = reinterpret_cast<float4 *>(smem + kTmaHeaderBytes);  // gamma [H][nv], then beta
+    float4 *bpar = gpar + tma_param_bytes(p.N * 4, false) / 16;
+    unsigned char *stages = smem + kTmaHeaderBytes + tma_param_bytes(p.N * 4, LN);
+    const int SG = p.tc.stages / RPP, RT = p.tc.rows;
+    const int64_t ntiles = (M + RT - 1) / RT;
+    const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
+    float *scratch = h.red + grp * (2 * 2 * WPR);
+    volatile int *abort_flag = &h.abort;
+    int issued = 0;
+
+    auto tile_of = [&](int64_t j) {
+        const int64_t tile = blockIdx.x + (grp + j * RPP) * (int64_t)gridDim.x;
+        return tile < ntiles ? tile : (int64_t)-1;
+    };
+    auto issue = [&](int64_t j) {
+        const int64_t tile = tile_of(j);
+        if (tile < 0) return;
+        const int s = grp * SG + (int)(j % SG);
+        const int64_t r0 = tile * RT;
+        const int rows = (int)(M - r0 < RT ? M - r0 : RT);
+        const uint32_t bytes = (uint32_t)(rows * row_bytes);
+        mbar_arrive_expect_tx(&h.full[s], bytes);
+        bulk_g2s(stages + (size_t)s * p.tc.stride, static_cast<const unsigned char *>(p.x) + r0 * row_bytes,
+                 bytes, &h.full[s]);
+        ++issued;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RPP * SG; ++s) mbar_init(&h.full[s], 1);
+        h.abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (t == 0)
+        for (int j = 0; j < SG; ++j) issue(j);
+    for (int64_t v = threadIdx.x; v < nv; v += NT) {
+        const uint4 g = ld_vec(p.gamma, v);
+        uint4 b = make_uint4(0, 0, 0, 0);
+        if constexpr (LN) b = ld_vec(p.beta, v);
+#pragma unroll
+        for (int hh = 0; hh < H; ++hh) {
+            gpar[hh * nv + v] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
+                                           vget<T>(g, 4 * hh + 3));
+            if constexpr (LN)
+                bpar[hh * nv + v] = make_float4(vget<T>(b, 4 * hh), vget<T>(b, 4 * hh + 1),
+                                               vget<T>(b, 4 * hh + 2), vget<T>(b, 4 * hh + 3));
+        }
+    }
+    __syncthreads();
+
+    const float n = (float)p.N;
+    const bool full = nv == (int64_t)TPR * VPT;  // every thread holds VPT vectors of each row
+    int parity = 0;
+    for (int64_t j = 0;; ++j) {
+        const int64_t tile = tile_of(j);
+        if (tile < 0) break;  // uniform per group (named barriers only)
+        const int s = grp * SG + (int)(j % SG);
+        mbar_wait_bounded(&h.full[s], (uint32_t)((j / SG) & 1), abort_flag, p.tc.fault);
+        const int64_t r0 = tile * RT;
+        const int rows = (int)(M - r0 < RT ? M - r0 : RT);
+        const unsigned char *tb = stages + (size_t)s * p.tc.stride;
+        for (int r = 0; r < rows; ++r) {  // every thread of the group works on the same row
+            const uint4 *xs = reinterpret_cast<const uint4 *>(tb + (size_t)r * row_bytes);
+            const int64_t row = r0 + r;
+            float xf[VPT][E];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = k * TPR + t;
+                const uint4 q = v < nv ? lds128(xs + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int e = 0; e < E; ++e) xf[k][e] = vget<T>(q, e);
+            }
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc += LN ? xf[k][e] : xf[k][e] * xf[k][e];
+            float mean = 0.f;
+            if (LN && full) {
+                constexpr float kC = (float)(VPT * E);
+                mean = acc * (1.f / kC);
+                float m2 = 0.f;
+#pragma unroll
+                for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float d = xf[k][e] - mean;
+                        m2 += d * d;
+                    }
+                group_meanvar_equal<TPR>(mean, m2, kC, scratch, parity, 1 + grp);
+                acc = m2;
+            } else {
+                float a[1] = {acc};
+                group_allreduce<TPR, 1>(a, scratch, parity, 1 + grp);
+                acc = a[0];
+                if constexpr (LN) {
+                    mean = acc / n;
+                    a[0] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k) {
+                        if (k * TPR + t >= nv) continue;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            const float d = xf[k][e] - mean;
+                            a[0] += d * d;
+                        }
+                    }
+                    group_allreduce<TPR, 1>(a, scratch, parity, 1 + grp);
+                    acc = a[0];
+                }
+            }
+            if (r == 0 && j >= 1 && t == 0) {
+                // Every thread of the group is past its last read of the stage
+                // of its tile j - 1: order those reads before the bulk copy's
+                // writes, then refill.
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(j - 1 + SG);
+            }
+            const float rstd = rsqrtf(acc / n + p.eps);
+            if (t == 0) {
+                if (p.rstd) p.rstd[row] = rstd;
+                if (LN && p.mean) p.mean[row] = mean;
+            }
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = k * TPR + t;
+                if (v >= nv) continue;
+                float o[E];
+#pragma unroll
+                for (int hh = 0; hh < H; ++hh) {
+                    const float4 g = gpar[hh * nv + v];
+                    o[4 * hh] = ((xf[k][4 * hh] - mean) * rstd) * g.x;
+                    o[4 * hh + 1] = ((xf[k][4 * hh + 1] - mean) * rstd) * g.y;
+                    o[4 * hh + 2] = ((xf[k][4 * hh + 2] - mean) * rstd) * g.z;
+                    o[4 * hh + 3] = ((xf[k][4 * hh + 3] - mean) * rstd) * g.w;
+                    if constexpr (LN) {
+                        const float4 b = bpar[hh * nv + v];
+                        o[4 * hh] += b.x;
+                        o[4 * hh + 1] += b.y;
+                        o[4 * hh + 2] += b.z;
+                        o[4 * hh + 3] += b.w;
+                    }
+                }
+                st_vec(p.y, row * nv + v, vpack<T>(o));
+            }
+        }
+    }
+    if (t == 0 && *abort_flag) {
+        int zero = 0;
+        for (int j = issued > SG ? issued - SG : 0; j < issued; ++j)
+            mbar_wait_bounded(&h.full[grp * SG + j % SG], (uint32_t)((j / SG) & 1),
+                              reinterpret_cast<volatile int *>(&zero), nullptr);
+    }
+}
+
 // ============================================================================ backward, no producer warp
 // As bwd_tma without a producer warp: the CTA's NT threads form RPP = NT / TPR
 // row groups, and each group runs its own pipeline over its share of the
@@ -527,7 +701,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
     TmaHeader &h = *reinterpret_cast<TmaHeader *>(smem);
     const int64_t M = p.M, nv = p.N / E;
     const size_t row_bytes = (size_t)p.N * sizeof(T);
-    float4 *gpar = reinterpret_cast<float4 *>(smem + kTmaHeaderBytes);  // gamma as fp32 [nv * H]
+    float4 *gpar = reinterpret_cast<float4 *>(smem + kTmaHeaderBytes);  // gamma as fp32 [H][nv]
     unsigned char *stages = smem + kTmaHeaderBytes + tma_param_bytes(p.N * 4, false);
     const int SG = p.tc.stages / RPP, RT = p.tc.rows;  // stages per row group
     const uint32_t tile_bytes = (uint32_t)((RT * row_bytes + 127) & ~(size_t)127);
@@ -576,14 +750,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
         const uint4 g = ld_vec(p.gamma, v);
 #pragma unroll
         for (int hh = 0; hh < H; ++hh)
-            gpar[v * H + hh] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
+            gpar[hh * nv + v] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
                                            vget<T>(g, 4 * hh + 3));
     }
     __syncthreads();
     auto gamma_of = [&](int v, float (&g)[E]) {
 #pragma unroll
         for (int hh = 0; hh < H; ++hh) {
-            const float4 q = gpar[v * H + hh];
+            const float4 q = gpar[hh * nv + v];
             g[4 * hh] = q.x;
             g[4 * hh + 1] = q.y;
             g[4 * hh + 2] = q.z;
