@@ -28,11 +28,11 @@ namespace gbn {
             kTmacNT, VPT, RS, CL, (kTmacCW + 1) * 32, VecTraits<GBN_T>::E, 1, 0},
 #define GBN_C_RMS(CL, VPT, RS) GBN_TMAC(false, CL, VPT, RS)
 #define GBN_C_LN(CL, VPT, RS) GBN_TMAC(true, CL, VPT, RS)
-#define GBN_WIDE(LN, NT, U, MINB, PF)                                                          \
-    Variant{GBN_WIDE_VNAME(NT, U, MINB, PF), (const void *)&fwd_wide<GBN_T, LN, NT, U, MINB, PF>,   \
-            kWide, NT, U, 1, 1, NT, VecTraits<GBN_T>::E, MINB, 0},
-#define GBN_W_RMS(NT, U, MINB, PF) GBN_WIDE(false, NT, U, MINB, PF)
-#define GBN_W_LN(NT, U, MINB, PF) GBN_WIDE(true, NT, U, MINB, PF)
+#define GBN_WIDE(LN, NT, U, MINB, PF, R)                                                       \
+    Variant{GBN_WIDE_VNAME(NT, U, MINB, PF, R), (const void *)&fwd_wide<GBN_T, LN, NT, U, MINB, PF, R>, \
+            kWide, NT, U, R, 1, NT, VecTraits<GBN_T>::E, MINB, 0},
+#define GBN_W_RMS(NT, U, MINB, PF, R) GBN_WIDE(false, NT, U, MINB, PF, R)
+#define GBN_W_LN(NT, U, MINB, PF, R) GBN_WIDE(true, NT, U, MINB, PF, R)
 #define GBN_ROWS_S(LN, TPR, VPT, CTA, MINB)                                                    \
     Variant{GBN_FWD_S_VNAME(TPR, VPT, CTA, MINB), (const void *)&fwd_rows_s<GBN_T, LN, TPR, VPT, CTA, MINB>, \
             kRowsS, TPR, VPT, 1, 1, CTA, VecTraits<GBN_T>::E, MINB, 0},

@@ -61,7 +61,7 @@ struct Variant {
     int kind;            // VariantKind
     int tpr;             // threads per row group (within one CTA)
     int vpt;             // 16-byte vectors per thread per row (max); kWide: vectors per batch
-    int rows;            // rows per row group per iteration (kRows); rows per exchange step (kTmaCl)
+    int rows;            // rows per row group per iteration (kRows, kWide); rows per exchange step (kTmaCl)
     int cl;              // CTAs per row (thread-block cluster size)
     int cta;             // threads per CTA
     int elems_per_vec;   // E (16 bytes / sizeof(T)); 1 for element-wise kernels
@@ -75,7 +75,9 @@ struct Variant {
     // Threads of a CTA that work on rows (TMA kinds add one producer warp).
     int consumers() const { return (kind == kTma || kind == kTmaCl) ? cta - 32 : cta; }
     bool staged_rows() const { return kind == kTma || kind == kTmaP; }
-    int rows_per_cta_iter() const { return (kind == kRows || kind == kRowsS) ? (cta / tpr) * rows : 1; }
+    int rows_per_cta_iter() const {
+        return (kind == kRows || kind == kRowsS) ? (cta / tpr) * rows : (kind == kWide && cl == 1) ? rows : 1;
+    }
 };
 
 struct VariantTable {

@@ -98,26 +98,30 @@ __device__ __forceinline__ void warp_combine(float &n, float &mean, float &m2) {
 }
 
 // PF (prefetch): 0 none; 1 each row is bulk-prefetched into L2 as its pass 1
-// starts; 2 as 1 for the first row, then the CTA's next row is prefetched as
-// the current row's pass 2 starts (two rows per CTA resident in L2).
-template <typename T, bool LN, int NT, int UV, int MINB, int PF>
+// starts; 2 as 1 for the first rows, then the CTA's next rows are prefetched
+// as the current rows' pass 2 starts (twice the rows per CTA resident in L2).
+// R rows per CTA at a time: their pass-1 loads share the batches, their
+// statistics one CTA barrier, and their pass 2 one load of gamma (and beta)
+// per vector, which halves (R = 2) the L2 reads of the parameters.
+template <typename T, bool LN, int NT, int UV, int MINB, int PF, int R>
 __global__ void __launch_bounds__(NT, MINB) fwd_wide(const FwdParams p) {
     constexpr int E = VecTraits<T>::E;
     constexpr int W = NT / 32;
     constexpr bool kRoomy = 65536 / (NT * MINB) >= 128;  // registers per thread >= 128
-    // The LayerNorm batch is read twice from registers (sum, then M2): with
-    // fewer than 128 registers per thread it holds at most 4 vectors.
-    constexpr int U = (LN && !kRoomy && UV > 4) ? 4 : UV;
-    // Pass 2 loads x, gamma (and beta) per vector: fewer vectors per batch
-    // unless the register budget is roomy.
+    // Vectors per thread per load batch (all R rows together at most 8, and
+    // at most 4 for the LayerNorm batch, read twice from registers, when
+    // registers are short).
+    constexpr int UR = UV * R > 8 ? (8 / R > 0 ? 8 / R : 1) : UV;
+    constexpr int U = (LN && !kRoomy && UR * R > 4) ? (4 / R > 0 ? 4 / R : 1) : UR;
+    // Pass 2 loads x of R rows and gamma (and beta) per vector: fewer vectors
+    // per batch unless the register budget is roomy.
     constexpr int U2r = LN ? U / 2 : (kRoomy ? U : U / 2);
     constexpr int U2 = U2r > 0 ? U2r : 1;
-    // Independent partial sums per thread in pass 1 (two for the LayerNorm
-    // batch sum and M2 when registers are short).
-    constexpr int A0 = (LN && !kRoomy) ? 2 : 4;
+    // Independent partial sums per thread and row in pass 1.
+    constexpr int A0 = (LN && !kRoomy) ? 2 : (R > 1 ? 2 : 4);
     constexpr int A = U < A0 ? U : A0;
-    static_assert(NT % 32 == 0 && NT <= 1024, "CTA shape");
-    __shared__ float red[2][3][W];
+    static_assert(NT % 32 == 0 && NT <= 1024 && R >= 1 && R <= 2, "CTA shape");
+    __shared__ float red[2][3][R][W];
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t nv = p.N / E;
@@ -126,155 +130,204 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wide(const FwdParams p) {
     const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
     const uint4 *gam = static_cast<const uint4 *>(p.gamma);
     const uint4 *bet = static_cast<const uint4 *>(p.beta);
+    const uint4 *xg = static_cast<const uint4 *>(p.x);
     int parity = 0;
+    const int64_t step = (int64_t)gridDim.x * R;
 
-    if (PF == 2 && warp == 0 && blockIdx.x < p.M)
-        prefetch_row(static_cast<const uint4 *>(p.x) + (int64_t)blockIdx.x * nv, row_bytes, lane, keep);
-
-    for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
-        const uint4 *xr = static_cast<const uint4 *>(p.x) + row * nv;
-        uint4 *yr = static_cast<uint4 *>(p.y) + row * nv;
-        if (PF == 1 && warp == 0) prefetch_row(xr, row_bytes, lane, keep);
-
-        // ---- pass 1: statistics (row from DRAM, kept in L2)
-        float cnt = 0.f, mean = 0.f, acc = 0.f;  // acc: sum x^2 (RMS) or M2 (LN)
-        float pa[A];
+    auto prefetch_rows = [&](int64_t base) {
+        if (warp == 0) {
 #pragma unroll
-        for (int a = 0; a < A; ++a) pa[a] = 0.f;
+            for (int r = 0; r < R; ++r)
+                if (base + r < p.M) prefetch_row(xg + (base + r) * nv, row_bytes, lane, keep);
+        }
+    };
+    if (PF == 2) prefetch_rows((int64_t)blockIdx.x * R);
+
+    for (int64_t base = (int64_t)blockIdx.x * R; base < p.M; base += step) {
+        bool ok[R];
+        const uint4 *xr[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            ok[r] = base + r < p.M;
+            xr[r] = xg + (ok[r] ? base + r : base) * nv;
+        }
+        if (PF == 1) prefetch_rows(base);
+
+        // ---- pass 1: statistics (rows from DRAM, kept in L2)
+        float cnt[R], mean[R], acc[R];  // acc: sum x^2 (RMS) or M2 (LN)
+        float pa[R][A];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            cnt[r] = mean[r] = acc[r] = 0.f;
+#pragma unroll
+            for (int a = 0; a < A; ++a) pa[r][a] = 0.f;
+        }
         for (int64_t b = t; b < nv; b += (int64_t)NT * U) {
-            uint4 q[U];
+            uint4 q[R][U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = b + (int64_t)u * NT;
-                q[u] = v < nv ? ld_l2hint(xr + v, keep) : make_uint4(0, 0, 0, 0);
-            }
-            if constexpr (!LN) {
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float f = vget<T>(q[u], e);
-                        pa[u % A] += f * f;
-                    }
-            } else {
-                float ps[A], pm[A];
-                int nb = 0;
-#pragma unroll
-                for (int a = 0; a < A; ++a) ps[a] = pm[a] = 0.f;
+            for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    if (b + (int64_t)u * NT < nv) {
-                        nb += E;
-#pragma unroll
-                        for (int e = 0; e < E; ++e) ps[u % A] += vget<T>(q[u], e);
-                    }
+                    const int64_t v = b + (int64_t)u * NT;
+                    q[r][u] = (ok[r] && v < nv) ? ld_l2hint(xr[r] + v, keep) : make_uint4(0, 0, 0, 0);
                 }
-                float s = ps[0];
 #pragma unroll
-                for (int a = 1; a < A; ++a) s += ps[a];
-                const float fb = (float)nb;
-                const float mb = __fdiv_rn(s, fb);
+            for (int r = 0; r < R; ++r) {
+                if constexpr (!LN) {
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (b + (int64_t)u * NT < nv) {
+                    for (int u = 0; u < U; ++u)
 #pragma unroll
                         for (int e = 0; e < E; ++e) {
-                            const float d = vget<T>(q[u], e) - mb;
-                            pm[u % A] += d * d;
+                            const float f = vget<T>(q[r][u], e);
+                            pa[r][u % A] += f * f;
+                        }
+                } else {
+                    float ps[A], pm[A];
+                    int nb = 0;
+#pragma unroll
+                    for (int a = 0; a < A; ++a) ps[a] = pm[a] = 0.f;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        if (b + (int64_t)u * NT < nv) {
+                            nb += E;
+#pragma unroll
+                            for (int e = 0; e < E; ++e) ps[u % A] += vget<T>(q[r][u], e);
                         }
                     }
-                }
-                float m2b = pm[0];
+                    float s = ps[0];
 #pragma unroll
-                for (int a = 1; a < A; ++a) m2b += pm[a];
-                if (cnt == 0.f) {
-                    cnt = fb;
-                    mean = mb;
-                    acc = m2b;
-                } else {
-                    // running += batch (one division per batch of U vectors)
-                    const float tot = cnt + fb;
-                    const float d = mb - mean;
-                    const float r = __fdiv_rn(fb, tot);
-                    mean += d * r;
-                    acc += m2b + d * d * cnt * r;
-                    cnt = tot;
+                    for (int a = 1; a < A; ++a) s += ps[a];
+                    const float fb = (float)nb;
+                    const float mb = __fdiv_rn(s, fb);
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        if (b + (int64_t)u * NT < nv) {
+#pragma unroll
+                            for (int e = 0; e < E; ++e) {
+                                const float d = vget<T>(q[r][u], e) - mb;
+                                pm[u % A] += d * d;
+                            }
+                        }
+                    }
+                    float m2b = pm[0];
+#pragma unroll
+                    for (int a = 1; a < A; ++a) m2b += pm[a];
+                    if (cnt[r] == 0.f) {
+                        cnt[r] = fb;
+                        mean[r] = mb;
+                        acc[r] = m2b;
+                    } else {
+                        // running += batch (one division per batch of U vectors)
+                        const float tot = cnt[r] + fb;
+                        const float d = mb - mean[r];
+                        const float rr = __fdiv_rn(fb, tot);
+                        mean[r] += d * rr;
+                        acc[r] += m2b + d * d * cnt[r] * rr;
+                        cnt[r] = tot;
+                    }
                 }
             }
         }
         if constexpr (!LN) {
-            acc = pa[0];
 #pragma unroll
-            for (int a = 1; a < A; ++a) acc += pa[a];
+            for (int r = 0; r < R; ++r) {
+                acc[r] = pa[r][0];
+#pragma unroll
+                for (int a = 1; a < A; ++a) acc[r] += pa[r][a];
+            }
         }
 
         // ---- CTA reduction (identical bits in every thread)
-        float *buf = &red[parity][0][0];
+        float (*buf)[R][W] = red[parity];
         parity ^= 1;
         if constexpr (!LN) {
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0) buf[warp] = acc;
-            __syncthreads();
-            acc = 0.f;
-#pragma unroll 4
-            for (int w = 0; w < W; ++w) acc += buf[w];
-        } else {
-            warp_combine(cnt, mean, acc);
+            for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+                for (int r = 0; r < R; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
             if (lane == 0) {
-                buf[warp] = cnt;
-                buf[W + warp] = mean;
-                buf[2 * W + warp] = acc;
+#pragma unroll
+                for (int r = 0; r < R; ++r) buf[0][r][warp] = acc[r];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                acc[r] = 0.f;
+#pragma unroll 4
+                for (int w = 0; w < W; ++w) acc[r] += buf[0][r][w];
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r) warp_combine(cnt[r], mean[r], acc[r]);
+            if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    buf[0][r][warp] = cnt[r];
+                    buf[1][r][warp] = mean[r];
+                    buf[2][r][warp] = acc[r];
+                }
             }
             __syncthreads();
             // the same group combine over the W warps, in warp order
-            float tn = 0.f, ts = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float tn = 0.f, ts = 0.f;
 #pragma unroll 4
-            for (int w = 0; w < W; ++w) {
-                tn += buf[w];
-                ts += buf[w] * buf[W + w];
-            }
-            mean = ts / tn;  // tn = N > 0
-            acc = 0.f;
+                for (int w = 0; w < W; ++w) {
+                    tn += buf[0][r][w];
+                    ts += buf[0][r][w] * buf[1][r][w];
+                }
+                mean[r] = ts / tn;  // tn = N > 0
+                float a2 = 0.f;
 #pragma unroll 4
-            for (int w = 0; w < W; ++w) {
-                const float d = buf[W + w] - mean;
-                acc += buf[2 * W + w] + buf[w] * (d * d);
+                for (int w = 0; w < W; ++w) {
+                    const float d = buf[1][r][w] - mean[r];
+                    a2 += buf[2][r][w] + buf[0][r][w] * (d * d);
+                }
+                acc[r] = a2;
             }
         }
-        const float rstd = rsqrtf(acc / n + p.eps);
-        if (!LN) mean = 0.f;
-        if (t == 0) {
-            if (p.rstd) p.rstd[row] = rstd;
-            if (LN && p.mean) p.mean[row] = mean;
+        float rstd[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            rstd[r] = rsqrtf(acc[r] / n + p.eps);
+            if (!LN) mean[r] = 0.f;
+            if (t == 0 && ok[r]) {
+                if (p.rstd) p.rstd[base + r] = rstd[r];
+                if (LN && p.mean) p.mean[base + r] = mean[r];
+            }
         }
 
-        if (PF == 2 && warp == 0 && row + gridDim.x < p.M)
-            prefetch_row(xr + (int64_t)gridDim.x * nv, row_bytes, lane, keep);
+        if (PF == 2) prefetch_rows(base + step);
 
         // ---- pass 2: y = (x - mean) * rstd * gamma (+ beta), x from L2
         for (int64_t b = t; b < nv; b += (int64_t)NT * U2) {
-            uint4 q[U2], g[U2], bb[LN ? U2 : 1];
+            uint4 q[R][U2], g[U2], bb[LN ? U2 : 1];
 #pragma unroll
             for (int u = 0; u < U2; ++u) {
                 const int64_t v = b + (int64_t)u * NT;
                 if (v < nv) {
-                    q[u] = ld_l2hint(xr + v, drop);
                     g[u] = ld_l2hint(gam + v, keep);
                     if constexpr (LN) bb[u] = ld_l2hint(bet + v, keep);
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        if (ok[r]) q[r][u] = ld_l2hint(xr[r] + v, drop);
                 }
             }
 #pragma unroll
             for (int u = 0; u < U2; ++u) {
                 const int64_t v = b + (int64_t)u * NT;
-                if (v < nv) {
+                if (v >= nv) continue;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (!ok[r]) continue;
                     float o[E];
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
-                        o[e] = ((vget<T>(q[u], e) - mean) * rstd) * vget<T>(g[u], e);
+                        o[e] = ((vget<T>(q[r][u], e) - mean[r]) * rstd[r]) * vget<T>(g[u], e);
                         if constexpr (LN) o[e] += vget<T>(bb[u], e);
                     }
-                    st_l2hint(yr + v, vpack<T>(o), drop);
+                    st_l2hint(static_cast<uint4 *>(p.y) + (base + r) * nv + v, vpack<T>(o), drop);
                 }
             }
         }

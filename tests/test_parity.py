@@ -52,9 +52,9 @@ def _geom(name):
     if m:
         cl, vpt, rs = (int(v) for v in m.groups())
         return (256, vpt, rs, cl, 288, True)
-    m = re.fullmatch(r"wide(\d+)u(\d+)b(\d+)p(\d+)", name)
+    m = re.fullmatch(r"wide(\d+)u(\d+)b(\d+)p(\d+)r(\d+)", name)
     if m:
-        nt, u, _, _ = (int(v) for v in m.groups())
+        nt, u, _, _, _ = (int(v) for v in m.groups())
         return ("wide", nt, u, 1)
     m = re.fullmatch(r"bwide(\d+)u(\d+)c(\d+)p(\d+)f(\d+)", name)
     if m:
@@ -284,7 +284,7 @@ def test_tma_ring_wraps(op, direction, N, limit):
 
 # Wide-row variants (one CTA per row, or a cluster with an exchange ring of
 # four slots) that the pipeline test forces, per (direction, N).
-WIDE_PIPE = {(0, 16384): "wide512u8b2p1", (0, 65536): "wide1024u4b1p1",
+WIDE_PIPE = {(0, 16384): "wide512u8b2p1r1", (0, 65536): "wide1024u4b1p1r1", (0, 32768): "wide512u4b2p1r2",
              (1, 8192): "bwide512u4c1p1f0", (1, 16384): "bwide512u2c1p2f1",
              (1, 32768): "bwide512u2c2p2f1", (1, 32760): "bwide512u4c2p1f0",
              (1, 65536): "bwide512u2c4p2f1", (1, 65528): "bwide512u4c4p2f0",
