@@ -97,11 +97,12 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
             kTmacNT, VPT, RS, CL, (kTmacCW + 1) * 32, VecTraits<GBN_T>::E, 1, 0},
 #define GBN_C_RMS(CL, VPT, RS) GBN_TMAC(false, CL, VPT, RS)
 #define GBN_C_LN(CL, VPT, RS) GBN_TMAC(true, CL, VPT, RS)
-#define GBN_BWIDE(LN, NT, U, CL, PF, F)                                                        \
-    Variant{GBN_BWIDE_VNAME(NT, U, CL, PF, F), (const void *)&bwd_wide<GBN_T, LN, NT, U, CL, PF, F>, \
-            kWide, NT, U, 1, CL, NT, VecTraits<GBN_T>::E, 1, 0},
-#define GBN_W_RMS(NT, U, CL, PF, F) GBN_BWIDE(false, NT, U, CL, PF, F)
-#define GBN_W_LN(NT, U, CL, PF, F) GBN_BWIDE(true, NT, U, CL, PF, F)
+#define GBN_BWIDE(LN, NT, U, CL, PF, F, MINB)                                                  \
+    Variant{GBN_BWIDE_VNAME(NT, U, CL, PF, F, MINB),                                           \
+            (const void *)&bwd_wide<GBN_T, LN, NT, U, CL, PF, F, MINB>, kWide, NT, U, 1, CL, NT,   \
+            VecTraits<GBN_T>::E, MINB, 0},
+#define GBN_W_RMS(NT, U, CL, PF, F, MINB) GBN_BWIDE(false, NT, U, CL, PF, F, MINB)
+#define GBN_W_LN(NT, U, CL, PF, F, MINB) GBN_BWIDE(true, NT, U, CL, PF, F, MINB)
 #define GBN_TMP(LN, TPR, VPT, NT)                                                              \
     Variant{GBN_TMP_VNAME(TPR, VPT, NT), (const void *)&bwd_tmp<GBN_T, LN, TPR, VPT, NT>, kTmaP, TPR, \
             VPT, 0, 1, NT, VecTraits<GBN_T>::E, 1, 32768},

@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wide(const FwdParams p) {
 namespace gbn {
 
 // ============================================================================ backward
-// Backward for wide rows: a cluster of CL CTAs (CL = 1, 2, 4 or 8) shares each
+// Backward for wide rows: a cluster of CL CTAs (CL = 1, 2, 4, 8 or 16) shares each
 // row; CTA `rank` owns a contiguous column slice and keeps its dgamma (and
 // dbeta) partial sums for that slice in shared memory across all the rows it
 // visits.  Per row: pass 1 streams the slice of x and dy from DRAM (L2
@@ -463,15 +463,16 @@ __device__ __forceinline__ void wide_bwd_sweep(int t, int cnt, int64_t slice, co
 // FUSE: 1 the schedule above; 0 pass 1 of row k + 1 (and its send), then the
 // wait for row k's exchange, then pass 2 of row k (one row's loads per batch,
 // larger batches).
-template <typename T, bool LN, int NT, int U, int CL, int PF, int FUSE>
-__global__ void __launch_bounds__(NT, 1) bwd_wide(const BwdParams p) {
+// MINB: CTAs per SM the launch bound asks for (registers 65536 / (NT * MINB)).
+template <typename T, bool LN, int NT, int U, int CL, int PF, int FUSE, int MINB>
+__global__ void __launch_bounds__(NT, MINB) bwd_wide(const BwdParams p) {
     pdl_launch_dependents();  // the column reduce waits for this grid's completion
     constexpr int E = VecTraits<T>::E;
     constexpr int W = NT / 32;
     constexpr int H = E / 4;          // float4 accumulators per 16-byte vector
     constexpr int NVAL = LN ? 2 : 1;  // partial sums per row; accumulator planes
     constexpr int NS = 4;             // exchange slots
-    static_assert(NT % 32 == 0 && NT <= 1024 && CL >= 1 && CL <= 8, "shape");
+    static_assert(NT % 32 == 0 && NT <= 1024 && CL >= 1 && CL <= 16, "shape");
     extern __shared__ __align__(16) float4 accs[];  // [NVAL][H][slice]
     __shared__ float red[2][NVAL][W];
     __shared__ float slot[NS][CL][NVAL];

@@ -56,9 +56,9 @@ def _geom(name):
     if m:
         nt, u, _, _, _ = (int(v) for v in m.groups())
         return ("wide", nt, u, 1)
-    m = re.fullmatch(r"bwide(\d+)u(\d+)c(\d+)p(\d+)f(\d+)", name)
+    m = re.fullmatch(r"bwide(\d+)u(\d+)c(\d+)p(\d+)f(\d+)m(\d+)", name)
     if m:
-        nt, u, cl, _, _ = (int(v) for v in m.groups())
+        nt, u, cl, _, _, _ = (int(v) for v in m.groups())
         return ("wide", nt, u, cl)
     return None
 
@@ -285,10 +285,10 @@ def test_tma_ring_wraps(op, direction, N, limit):
 # Wide-row variants (one CTA per row, or a cluster with an exchange ring of
 # four slots) that the pipeline test forces, per (direction, N).
 WIDE_PIPE = {(0, 16384): "wide512u8b2p1r1", (0, 65536): "wide1024u4b1p1r1", (0, 32768): "wide512u4b2p1r2",
-             (1, 8192): "bwide512u4c1p1f0", (1, 16384): "bwide512u2c1p2f1",
-             (1, 32768): "bwide512u2c2p2f1", (1, 32760): "bwide512u4c2p1f0",
-             (1, 65536): "bwide512u2c4p2f1", (1, 65528): "bwide512u4c4p2f0",
-             (1, 131072): "bwide512u2c8p2f1"}
+             (1, 8192): "bwide512u4c1p1f0m1", (1, 16384): "bwide512u2c1p2f1m1",
+             (1, 32768): "bwide512u2c2p2f1m1", (1, 32760): "bwide512u4c2p1f0m1",
+             (1, 65536): "bwide512u2c4p2f1m1", (1, 65528): "bwide512u4c4p2f0m1",
+             (1, 131072): "bwide512u2c8p2f1m1"}
 
 
 @pytest.mark.parametrize("op", ["rms", "ln"])
