@@ -134,3 +134,21 @@ def test_product_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "from oracle" not in text, fn
                 assert "norm_oracle" not in text, fn
+
+
+def test_dispatch_table_names_compiled_variants(lib):
+    """Every variant the dispatch table names exists in the compiled tables of
+    every (op, direction, dtype) its row applies to: a misspelt or removed name
+    would otherwise be skipped silently and the row's shapes served by the
+    next row."""
+    from rmsnorm_norm_fwd_gb300 import binding as b
+    table = os.path.join(ROOT, "rmsnorm_norm_fwd_gb300", "csrc", "dispatch_table.inc")
+    rows = re.findall(r'^\{(-?\d+), (\d+), (-?\d+), (\d+), "([^"]+)"\}', open(table).read(), re.M)
+    assert len(rows) > 50
+    names = {0: "fp32", 1: "fp16", 2: "bf16"}
+    for ln, d, dt, nv, variant in rows:
+        for is_ln in ((0, 1) if ln == "-1" else (int(ln),)):
+            for code in ((0, 1, 2) if dt == "-1" else (int(dt),)):
+                assert variant in b.variants(bool(is_ln), int(d), names[code]), \
+                    (variant, is_ln, d, names[code])
+        assert int(nv) > 0
