@@ -324,6 +324,11 @@ def run_ours(args, ws, rank, local):
 
     # End to end through the public API from pinned host memory, per step:
     # H2D of x, dy, gamma; forward; backward; D2H of y, rstd, dx, dgamma.
+    # The host link is full duplex: shape i is computed on the launching
+    # stream while shape i + 1 comes in on one copy stream and shape i - 1
+    # goes out on another; events order every reuse of a buffer (a copy-in
+    # waits for the previous step's computation on that shape, the
+    # computation for the previous step's copy-out of its outputs).
     e2e = None
     if not args.no_e2e:
         hb = []
@@ -336,17 +341,39 @@ def run_ours(args, ws, rank, local):
         h2d = sum(h["x"].nbytes + h["dy"].nbytes + h["gamma"].nbytes for h in hb)
         d2h = sum(h["y"].nbytes + h["dx"].nbytes + h["rstd"].nbytes + h["dgamma"].nbytes for h in hb)
 
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in data]
+        ev_comp = [torch.cuda.Event() for _ in data]
+        ev_out = [torch.cuda.Event() for _ in data]
+        for i in range(len(data)):  # "previous step" events start completed
+            ev_comp[i].record(stream)
+            ev_out[i].record(stream)
+
         def e2e_step():
-            for d, h in zip(data, hb):
-                d["x"].copy_(h["x"], non_blocking=True)
-                d["dy"].copy_(h["dy"], non_blocking=True)
-                d["gamma"].copy_(h["gamma"], non_blocking=True)
+            start = torch.cuda.Event()
+            start.record(stream)
+            for i, (d, h) in enumerate(zip(data, hb)):
+                s_in.wait_event(start)
+                s_in.wait_event(ev_comp[i])  # the last step's kernels are done with x, dy, gamma
+                with torch.cuda.stream(s_in):
+                    d["x"].copy_(h["x"], non_blocking=True)
+                    d["dy"].copy_(h["dy"], non_blocking=True)
+                    d["gamma"].copy_(h["gamma"], non_blocking=True)
+                ev_in[i].record(s_in)
+                stream.wait_event(ev_in[i])
+                stream.wait_event(ev_out[i])  # the last step's outputs have left
                 call_fwd(d)
                 call_bwd(d)
-                h["y"].copy_(d["y"], non_blocking=True)
-                h["dx"].copy_(d["dx"], non_blocking=True)
-                h["rstd"].copy_(d["rstd"], non_blocking=True)
-                h["dgamma"].copy_(d["dgamma"], non_blocking=True)
+                ev_comp[i].record(stream)
+                s_out.wait_event(ev_comp[i])
+                with torch.cuda.stream(s_out):
+                    h["y"].copy_(d["y"], non_blocking=True)
+                    h["dx"].copy_(d["dx"], non_blocking=True)
+                    h["rstd"].copy_(d["rstd"], non_blocking=True)
+                    h["dgamma"].copy_(d["dgamma"], non_blocking=True)
+                ev_out[i].record(s_out)
+            for e in ev_out:  # the step ends when its last output has arrived
+                stream.wait_event(e)
 
         e2e_step()
         torch.cuda.synchronize()
