@@ -1,0 +1,50 @@
+"""tune.py's table writer (CPU only): a partial sweep replaces exactly the
+rows it measured, keeps the fastest variant per (op, direction, dtype, N),
+leaves every other row and the default rows as they were, and is stable."""
+import os
+import re
+import shutil
+
+from rmsnorm_norm_fwd_gb300 import tune
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TABLE = os.path.join(ROOT, "rmsnorm_norm_fwd_gb300", "csrc", "dispatch_table.inc")
+
+
+def _rows(text):
+    start = text.index("// ---- measured rows (tune.py) ----")
+    end = text.index("// ---- forward defaults")
+    return [l for l in text[start:end].splitlines() if l.startswith("{")]
+
+
+def test_emit_merges_partial_sweep(tmp_path):
+    path = tmp_path / "dispatch_table.inc"
+    shutil.copy(TABLE, path)
+    before = path.read_text()
+    old_rows = _rows(before)
+    results = [  # two variants for one measured shape, one for a new N
+        {"op": "ln", "dir": 1, "dtype": "bf16", "M": 16384, "N": 8192, "variant": "slow", "gbs": 100.0},
+        {"op": "ln", "dir": 1, "dtype": "bf16", "M": 16384, "N": 8192, "variant": "fast", "gbs": 200.0},
+        {"op": "rms", "dir": 0, "dtype": "fp16", "M": 8, "N": 24, "variant": "tiny", "gbs": 1.0},
+    ]
+    tune.emit(results, str(path))
+    after = path.read_text()
+    new_rows = _rows(after)
+    # the measured LN row now names the faster variant; N = 8192 bf16 is 1024 vectors
+    assert any(r.startswith('{1, 1, 2, 1024, "fast"}') for r in new_rows)
+    assert not any('"slow"' in r for r in new_rows)
+    # a new (op, dir, dtype, N) is added (24 fp16 elements = 3 vectors)
+    assert any(r.startswith('{0, 0, 1, 3, "tiny"}') for r in new_rows)
+    # every other measured row is unchanged
+    key = lambda r: tuple(re.match(r"\{(\d+), (\d+), (\d+), (\d+),", r).groups())
+    untouched = {key(r): r for r in old_rows if key(r) not in {("1", "1", "2", "1024"), ("0", "0", "1", "3")}}
+    new_by_key = {key(r): r for r in new_rows}
+    for k, r in untouched.items():
+        assert new_by_key[k] == r
+    assert len(new_rows) == len(old_rows) + 1
+    # the defaults after the measured block are untouched
+    tail = lambda t: t[t.index("// ---- forward defaults"):]
+    assert tail(after) == tail(before)
+    # emitting nothing changes nothing
+    tune.emit([], str(path))
+    assert path.read_text() == after
