@@ -53,11 +53,15 @@ L2_CLEAN_BYTES = 512 << 20
 
 # Measured DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # roofline kernel, from the ncu capture summarised under profiles/, valid only
-# while the files that kernel is compiled and launched from (ROOFLINE_SOURCES:
+# while the code that kernel is compiled and launched from (ROOFLINE_SOURCES:
 # its kernel file, the shared device helpers and argument blocks, and the host
-# code that sizes its grid and ring) hash to the digest recorded with it.
-ROOFLINE_SOURCES = ("tma_kernels.cuh", "device_common.cuh", "params.h", "api.cu")
-NCU_TRAFFIC = {"sources_digest": "dd9a2ec88be4d727", "variant": "tma128x2w8", "N": 2048,
+# code that dispatches it and sizes its grid and ring) hashes to the digest
+# recorded with it.
+# api.cu counts up to its argument-check section: the dispatch, geometry,
+# occupancy and launch code that decides how the kernel runs.
+ROOFLINE_SOURCES = ("tma_kernels.cuh", "device_common.cuh", "params.h",
+                    ("api.cu", "// ------------------------------------------------------------------ argument checks"))
+NCU_TRAFFIC = {"sources_digest": "03dc30e100b6e437", "variant": "tma128x2w8", "N": 2048,
                "bytes_per_launch": 537184512 + 232258048}
 
 
@@ -69,14 +73,22 @@ def bwd_bytes(m, n):
     return 3 * m * n * B + n * B + 4 * m + 4 * n
 
 
-def kernel_digest(names=None) -> str:
-    """Digest of the CUDA sources (all of them, or the listed file names)."""
+def kernel_digest(names=None, read=None) -> str:
+    """Digest of the CUDA sources: all of them, or the listed entries (a file
+    name, or (file name, marker) for the file's text before the marker)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rmsnorm_norm_fwd_gb300", "csrc")
+    read = read or (lambda fn: open(os.path.join(csrc, fn), "rb").read())
+    cut = {}
+    for e in names or ():
+        fn, mark = (e, None) if isinstance(e, str) else e
+        cut[fn] = mark
     for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h", ".inc")) and (names is None or fn in names):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+        if fn.endswith((".cu", ".cuh", ".h", ".inc")) and (names is None or fn in cut):
+            data = read(fn)
+            if names is not None and cut[fn] is not None:
+                data = data[:data.index(cut[fn].encode())]
+            h.update(fn.encode() + data)
     return h.hexdigest()[:16]
 
 

@@ -39,9 +39,18 @@
  *     them share it.  Arithmetic is float32 throughout; each output element
  *     is rounded once to dtype, round-to-nearest-even.
  *   - Ownership: the caller allocates and owns every buffer.  The library
- *     never allocates device memory, never frees, and never synchronises.
- *     All work is enqueued on `stream` (NULL = the legacy default stream) and
+ *     never allocates device memory, never frees, and never synchronises
+ *     (except the one-time copy of the default parameters below).  All work
+ *     is enqueued on `stream` (NULL = the legacy default stream) and
  *     completes asynchronously.
+ *   - Optional parameters: gamma may be NULL in every entry point (gamma_j =
+ *     1: RMSNorm or LayerNorm without a scale), beta may be NULL in
+ *     layernorm_fwd (beta_j = 0: no bias), and dgamma / dbeta may be NULL in
+ *     the backward (that column sum is not produced).  A NULL gamma or beta
+ *     needs N <= GBNORM_DEFAULT_PARAM_MAX_N (else GBNORM_ERR_UNSUPPORTED): the
+ *     library reads constant rows of ones / zeros that it keeps on each
+ *     device, copied there (synchronously, once per device) by the first call
+ *     that needs them.
  *   - Alignment: with 16-byte-aligned pointers and N * sizeof(dtype) a
  *     multiple of 16, rows move as 128-bit vectors; anything else takes a
  *     correct element-wise path.
@@ -78,7 +87,7 @@ typedef enum {
 
 typedef enum {
     GBNORM_OK = 0,
-    GBNORM_ERR_INVALID_ARG = 1, /* null pointer, bad shape or dtype, overlapping buffers, bad eps */
+    GBNORM_ERR_INVALID_ARG = 1, /* required pointer null, bad shape or dtype, overlapping buffers, bad eps */
     GBNORM_ERR_UNSUPPORTED = 2, /* a valid request this build cannot serve (e.g. no sm_103a device) */
     GBNORM_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than norm_bwd_workspace_size */
     GBNORM_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
@@ -87,10 +96,13 @@ typedef enum {
 /* Largest row length N accepted by every entry point. */
 #define GBNORM_MAX_N ((int64_t)1 << 24)
 
+/* Largest row length N for which gamma or beta may be NULL (see above). */
+#define GBNORM_DEFAULT_PARAM_MAX_N ((int64_t)1 << 18)
+
 /*
  * RMSNorm forward.
  *   x      [M, N] dtype, read only.
- *   gamma  [N] dtype, read only.
+ *   gamma  [N] dtype, read only; may be NULL (gamma = 1).
  *   y      [M, N] dtype, written (may equal x).
  *   rstd   [M] float32, written; may be NULL (nothing stored, e.g. inference).
  *   eps    added to the mean square under the root; finite and >= 0.
@@ -100,7 +112,8 @@ int rmsnorm_fwd(const void *x, const void *gamma, void *y, float *rstd, int64_t 
 
 /*
  * LayerNorm forward.
- *   x, gamma, y, rstd as for rmsnorm_fwd; beta [N] dtype, read only.
+ *   x, gamma, y, rstd as for rmsnorm_fwd; beta [N] dtype, read only, may be
+ *   NULL (beta = 0).
  *   mean   [M] float32, written; may be NULL.  rstd may be NULL.
  *   eps    added to the biased variance under the root; finite and >= 0.
  */
@@ -117,10 +130,12 @@ size_t norm_bwd_workspace_size(int is_layernorm, int64_t M, int64_t N, int dtype
 
 /*
  * RMSNorm backward.
- *   dy, x  [M, N] dtype, read only.   gamma [N] dtype, read only.
+ *   dy, x  [M, N] dtype, read only.   gamma [N] dtype, read only, may be
+ *          NULL (gamma = 1).
  *   rstd   [M] float32 as saved by rmsnorm_fwd, read only.
  *   dx     [M, N] dtype, written (may equal dy).
- *   dgamma [N] float32, written (overwritten, not accumulated).
+ *   dgamma [N] float32, written (overwritten, not accumulated); may be NULL
+ *          (not produced).
  *   workspace / workspace_bytes: device scratch of at least
  *          norm_bwd_workspace_size(0, M, N, dtype) bytes, 16-byte aligned;
  *          its contents on entry are ignored and on exit are unspecified.
@@ -133,7 +148,7 @@ int rmsnorm_bwd(const void *dy, const void *x, const void *gamma, const float *r
 /*
  * LayerNorm backward.
  *   as rmsnorm_bwd, plus mean [M] float32 as saved by layernorm_fwd (read
- *   only) and dbeta [N] float32 (written).  Workspace of at least
+ *   only) and dbeta [N] float32 (written; may be NULL).  Workspace of at least
  *   norm_bwd_workspace_size(1, M, N, dtype) bytes.
  */
 int layernorm_bwd(const void *dy, const void *x, const void *gamma, const float *mean,

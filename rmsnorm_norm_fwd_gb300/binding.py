@@ -84,11 +84,15 @@ def _vec(name, t, n, dtype):
     return t
 
 
+def _opt_vec(name, t, n, dtype):
+    return None if t is None else _vec(name, t, n, dtype)
+
+
 def rmsnorm_fwd(x, gamma, eps: float, y=None, rstd=None, save_stats: bool = True, stream=None):
-    """y = x * rstd * gamma per row; returns (y, rstd) (rstd None if not saved)."""
+    """y = x * rstd * gamma per row (gamma None: 1); returns (y, rstd) (rstd None if not saved)."""
     _mat("x", x)
     M, N = x.shape
-    _vec("gamma", gamma, N, x.dtype)
+    _opt_vec("gamma", gamma, N, x.dtype)
     y = torch.empty_like(x) if y is None else _mat("y", y, x.dtype)
     if rstd is None and save_stats:
         rstd = torch.empty(M, device=x.device, dtype=torch.float32)
@@ -99,11 +103,12 @@ def rmsnorm_fwd(x, gamma, eps: float, y=None, rstd=None, save_stats: bool = True
 
 def layernorm_fwd(x, gamma, beta, eps: float, y=None, mean=None, rstd=None, save_stats: bool = True,
                   stream=None):
-    """y = (x - mean) * rstd * gamma + beta per row; returns (y, mean, rstd)."""
+    """y = (x - mean) * rstd * gamma + beta per row (gamma None: 1, beta None: 0);
+    returns (y, mean, rstd)."""
     _mat("x", x)
     M, N = x.shape
-    _vec("gamma", gamma, N, x.dtype)
-    _vec("beta", beta, N, x.dtype)
+    _opt_vec("gamma", gamma, N, x.dtype)
+    _opt_vec("beta", beta, N, x.dtype)
     y = torch.empty_like(x) if y is None else _mat("y", y, x.dtype)
     if save_stats:
         mean = torch.empty(M, device=x.device, dtype=torch.float32) if mean is None else mean
@@ -129,15 +134,18 @@ def _workspace(is_ln, x, workspace):
     return workspace, workspace.numel() * workspace.element_size()
 
 
-def rmsnorm_bwd(dy, x, gamma, rstd, dx=None, dgamma=None, workspace=None, stream=None):
-    """Returns (dx, dgamma) with dgamma in float32."""
+def rmsnorm_bwd(dy, x, gamma, rstd, dx=None, dgamma=None, workspace=None, stream=None,
+                need_dgamma: bool = True):
+    """Returns (dx, dgamma) with dgamma in float32 (gamma None: 1; need_dgamma
+    False with no dgamma given: not produced, None)."""
     _mat("x", x)
     M, N = x.shape
     _mat("dy", dy, x.dtype)
-    _vec("gamma", gamma, N, x.dtype)
+    _opt_vec("gamma", gamma, N, x.dtype)
     _vec("rstd", rstd, M, torch.float32)
     dx = torch.empty_like(x) if dx is None else _mat("dx", dx, x.dtype)
-    dgamma = torch.empty(N, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
+    if dgamma is None and need_dgamma:
+        dgamma = torch.empty(N, device=x.device, dtype=torch.float32)
     ws, wsb = _workspace(False, x, workspace)
     _check("rmsnorm_bwd", lib.rmsnorm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx),
                                           _ptr(dgamma), _ptr(ws), wsb, M, N, DTYPE_CODE[x.dtype],
@@ -146,17 +154,20 @@ def rmsnorm_bwd(dy, x, gamma, rstd, dx=None, dgamma=None, workspace=None, stream
 
 
 def layernorm_bwd(dy, x, gamma, mean, rstd, dx=None, dgamma=None, dbeta=None, workspace=None,
-                  stream=None):
-    """Returns (dx, dgamma, dbeta) with dgamma and dbeta in float32."""
+                  stream=None, need_dgamma: bool = True, need_dbeta: bool = True):
+    """Returns (dx, dgamma, dbeta) with dgamma and dbeta in float32 (gamma None:
+    1; a sum not needed and not given is not produced, None)."""
     _mat("x", x)
     M, N = x.shape
     _mat("dy", dy, x.dtype)
-    _vec("gamma", gamma, N, x.dtype)
+    _opt_vec("gamma", gamma, N, x.dtype)
     _vec("mean", mean, M, torch.float32)
     _vec("rstd", rstd, M, torch.float32)
     dx = torch.empty_like(x) if dx is None else _mat("dx", dx, x.dtype)
-    dgamma = torch.empty(N, device=x.device, dtype=torch.float32) if dgamma is None else dgamma
-    dbeta = torch.empty(N, device=x.device, dtype=torch.float32) if dbeta is None else dbeta
+    if dgamma is None and need_dgamma:
+        dgamma = torch.empty(N, device=x.device, dtype=torch.float32)
+    if dbeta is None and need_dbeta:
+        dbeta = torch.empty(N, device=x.device, dtype=torch.float32)
     ws, wsb = _workspace(True, x, workspace)
     _check("layernorm_bwd", lib.layernorm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd),
                                               _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(ws), wsb, M, N,

@@ -468,6 +468,11 @@ int launch_kernel(const Variant &v, const Plan &pl, void *params, cudaStream_t s
 }
 
 // ------------------------------------------------------------------ argument checks
+}  // namespace
+// Constant rows read in place of a NULL gamma (ones) or beta (zeros); defaults.cu.
+int default_params(int dtype, const void **ones, const void **zeros);
+namespace {
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlap(const void *a, size_t na, const void *b, size_t nb) {
@@ -509,9 +514,11 @@ bool bad_aliasing(const Buf *outs, int no, const Buf *ins, int ni, const void *i
 int do_fwd(int is_ln, const void *x, const void *gamma, const void *beta, void *y, float *mean,
            float *rstd, int64_t M, int64_t N, int dtype, float eps, cudaStream_t stream) {
     if (!valid_shape(M, N, dtype)) return GBNORM_ERR_INVALID_ARG;
-    if (!gamma || (is_ln && !beta)) return GBNORM_ERR_INVALID_ARG;
     if (M > 0 && (!x || !y)) return GBNORM_ERR_INVALID_ARG;
     if (!std::isfinite(eps) || eps < 0.f) return GBNORM_ERR_INVALID_ARG;
+    // A NULL gamma / beta reads the device's constant rows (gamma = 1, beta = 0).
+    const bool no_g = gamma == nullptr, no_b = is_ln && beta == nullptr;
+    if ((no_g || no_b) && N > GBNORM_DEFAULT_PARAM_MAX_N) return GBNORM_ERR_UNSUPPORTED;
     const size_t b = (size_t)elem_size(dtype);
     const size_t mat = (size_t)M * (size_t)N * b, vec = (size_t)N * b, st = (size_t)M * 4;
     const Buf outs[3] = {{y, mat}, {rstd, st}, {is_ln ? mean : nullptr, st}};
@@ -521,6 +528,13 @@ int do_fwd(int is_ln, const void *x, const void *gamma, const void *beta, void *
     int s = current_device(&dev);
     if (s != GBNORM_OK) return s;
     if (M == 0) return GBNORM_OK;
+    if (no_g || no_b) {
+        const void *ones, *zeros;
+        s = default_params(dtype, &ones, &zeros);
+        if (s != GBNORM_OK) return s;
+        if (no_g) gamma = ones;
+        if (no_b) beta = zeros;
+    }
     CallShape c{is_ln, 0, dtype, M, N, false, true};
     c.vec = (vec % 16) == 0 && aligned16(x) && aligned16(y) && aligned16(gamma) &&
             (!is_ln || aligned16(beta));
@@ -554,8 +568,12 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
            const float *rstd, void *dx, float *dgamma, float *dbeta, void *ws, size_t ws_bytes,
            int64_t M, int64_t N, int dtype, cudaStream_t stream) {
     if (!valid_shape(M, N, dtype)) return GBNORM_ERR_INVALID_ARG;
-    if (!gamma || !dgamma || (is_ln && !dbeta)) return GBNORM_ERR_INVALID_ARG;
     if (M > 0 && (!dy || !x || !rstd || !dx || (is_ln && !mean))) return GBNORM_ERR_INVALID_ARG;
+    // A NULL gamma reads the device's row of ones; a NULL dgamma / dbeta is
+    // not produced.
+    const bool no_g = gamma == nullptr;
+    if (no_g && N > GBNORM_DEFAULT_PARAM_MAX_N) return GBNORM_ERR_UNSUPPORTED;
+    if (!is_ln) dbeta = nullptr;
     const size_t b = (size_t)elem_size(dtype);
     const size_t mat = (size_t)M * (size_t)N * b, vec = (size_t)N * b, st = (size_t)M * 4,
                  pv = (size_t)N * 4;
@@ -572,6 +590,12 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
         const Buf all_out[4] = {outs[0], outs[1], outs[2], {ws, need}};
         if (bad_aliasing(all_out, 4, ins, 5, dx, dy)) return GBNORM_ERR_INVALID_ARG;
     }
+    if (no_g && M > 0) {
+        const void *ones, *zeros;
+        s = default_params(dtype, &ones, &zeros);
+        if (s != GBNORM_OK) return s;
+        gamma = ones;
+    }
     int64_t P = 0;
     if (M > 0) {
         CallShape c{is_ln, 1, dtype, M, N, false, false};
@@ -585,7 +609,9 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
         if (s != GBNORM_OK) return s;
         P = pl.P;
     }
-    // Stage two: column sums of the P partial rows (P = 0 writes zeros).
+    // Stage two: column sums of the P partial rows (P = 0 writes zeros); a
+    // NULL output's blocks return at once.
+    if (!dgamma && !dbeta) return GBNORM_OK;
     const bool v4 = (N % 4) == 0;
     const int64_t cols_per_cta = 32 * (v4 ? 4 : 1);
     const dim3 grid2((unsigned)((N + cols_per_cta - 1) / cols_per_cta), is_ln ? 2u : 1u);

@@ -557,6 +557,7 @@ __global__ void __launch_bounds__(kColCTA) colreduce(const float *ws, int64_t P,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float *src = ws + (int64_t)blockIdx.y * P * N;
     float *out = blockIdx.y ? out1 : out0;
+    if (out == nullptr) return;  // that sum is not wanted
     const int64_t col = ((int64_t)blockIdx.x * 32 + lane) * VW;
     const bool ok = col < N;
     const int64_t p0 = P * warp / W, p1 = P * (warp + 1) / W;

@@ -82,7 +82,7 @@ def test_forward_rejects_bad_arguments(lib):
     assert f(V(A), V(B), V(C), V(D), 4, 0, bf16, 1e-6, None) == 1            # N = 0
     assert f(V(A), V(B), V(C), V(D), -1, 8, bf16, 1e-6, None) == 1           # M < 0
     assert f(V(A), V(B), V(C), V(D), 4, 8, 7, 1e-6, None) == 1               # dtype
-    assert f(V(A), None, V(C), V(D), 4, 8, bf16, 1e-6, None) == 1            # gamma null
+    assert f(V(A), None, V(C), V(D), 4, (1 << 18) + 8, bf16, 1e-6, None) == 2  # NULL gamma, N too large
     assert f(None, V(B), V(C), V(D), 4, 8, bf16, 1e-6, None) == 1            # x null
     assert f(V(A), V(B), V(C), V(D), 4, 8, bf16, float("nan"), None) == 1    # eps
     assert f(V(A), V(B), V(C), V(D), 4, 8, bf16, -1.0, None) == 1            # eps < 0
@@ -90,7 +90,7 @@ def test_forward_rejects_bad_arguments(lib):
     assert f(V(A), V(B), V(C), V(C + 4), 4, 8, bf16, 1e-6, None) == 1        # rstd overlaps y
     assert f(V(A), V(B), V(C), V(D), 4, (1 << 24) + 1, bf16, 1e-6, None) == 1  # N too large
     g = lib.layernorm_fwd
-    assert g(V(A), V(B), None, V(C), V(D), V(E_), 4, 8, bf16, 1e-5, None) == 1  # beta null
+    assert g(V(A), V(B), None, V(C), V(D), V(E_), 4, (1 << 18) + 8, bf16, 1e-5, None) == 2  # NULL beta, N too large
     assert g(V(A), V(B), V(F), V(C), V(D), V(D), 4, 8, bf16, 1e-5, None) == 1   # mean == rstd
 
 
@@ -99,13 +99,30 @@ def test_backward_rejects_bad_arguments(lib):
     f = lib.rmsnorm_bwd
     # dx overlapping x (not the permitted in-place pair dx == dy)
     assert f(V(A), V(B), V(C), V(D), V(B), V(E_), V(F), 1 << 20, 4, 8, bf16, None) == 1
-    assert f(V(A), V(B), V(C), V(D), V(E_), None, V(F), 1 << 20, 4, 8, bf16, None) == 1  # dgamma
+    assert f(V(A), V(B), None, V(D), V(E_), V(G), V(F), 1 << 20, 4, (1 << 18) + 8, bf16,
+             None) == 2  # NULL gamma, N too large
     assert f(V(A), V(B), V(C), None, V(E_), V(G), V(F), 1 << 20, 4, 8, bf16, None) == 1  # rstd
     assert f(V(A), V(B), V(C), V(D), V(E_), V(G), V(F), 1 << 20, 4, 0, bf16, None) == 1  # N
     g = lib.layernorm_bwd
     assert g(V(A), V(B), V(C), None, V(D), V(E_), V(F), V(G), V(H), 1 << 20, 4, 8, bf16, None) == 1
     assert g(V(A), V(B), V(C), V(D), V(D + 8), V(E_), V(F), V(F), V(H), 1 << 20, 4, 8, bf16,
              None) == 1  # dgamma == dbeta
+
+
+def test_null_parameters_are_accepted(lib):
+    """gamma / beta / dgamma / dbeta may be NULL (defaults, or sums not
+    produced): such calls pass the argument checks; without a usable device
+    they report CUDA or unsupported, never invalid arguments."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    bf16 = 2
+    assert lib.rmsnorm_fwd(V(A), None, V(C), V(D), 4, 8, bf16, 1e-6, None) in (2, 4)
+    assert lib.layernorm_fwd(V(A), None, None, V(C), V(D), V(E_), 4, 8, bf16, 1e-5, None) in (2, 4)
+    assert lib.rmsnorm_bwd(V(A), V(B), None, V(D), V(E_), None, V(F), 1 << 20, 4, 8, bf16,
+                           None) in (2, 4)
+    assert lib.layernorm_bwd(V(A), V(B), None, V(C), V(D), V(E_), None, None, V(H), 1 << 20, 4, 8,
+                             bf16, None) in (2, 4)
 
 
 def test_valid_call_without_device_reports_cuda_or_unsupported(lib):
