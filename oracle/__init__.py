@@ -105,19 +105,24 @@ def layernorm_fwd(x, gamma, beta, eps: float):
     return y, mean, rstd
 
 
-def rmsnorm_bwd(dy, x, gamma, eps: float, want_dx: bool = True, want_dgamma: bool = True):
-    """Returns (dx [M,N] f64 or None, dgamma [N] f64 or None)."""
+def rmsnorm_bwd(dy, x, gamma, eps: float, want_dx: bool = True, want_dgamma: bool = True, dres=None):
+    """Returns (dx [M,N] f64 or None, dgamma [N] f64 or None).  dres: the
+    gradient reaching the normalised rows from a residual stream (see
+    residual_add), added to dx."""
     dy, x, gamma = _f64(dy), _f64(x), _f64(gamma)
     M, N = x.shape
     dx = np.empty((M, N), np.float64) if want_dx else None
     dg = np.empty(N, np.float64) if want_dgamma else None
     if _load().oracle_rmsnorm_bwd(dy, x, gamma, M, N, eps, _ptr(dx), _ptr(dg)) != 0:
         raise MemoryError("oracle: out of host memory")
+    if dx is not None and dres is not None:
+        dx += _f64(dres)
     return dx, dg
 
 
-def layernorm_bwd(dy, x, gamma, eps: float, want_dx: bool = True, want_dparams: bool = True):
-    """Returns (dx [M,N] f64 or None, dgamma [N] f64 or None, dbeta [N] f64 or None)."""
+def layernorm_bwd(dy, x, gamma, eps: float, want_dx: bool = True, want_dparams: bool = True, dres=None):
+    """Returns (dx [M,N] f64 or None, dgamma [N] f64 or None, dbeta [N] f64 or
+    None).  dres as for rmsnorm_bwd."""
     dy, x, gamma = _f64(dy), _f64(x), _f64(gamma)
     M, N = x.shape
     dx = np.empty((M, N), np.float64) if want_dx else None
@@ -125,4 +130,26 @@ def layernorm_bwd(dy, x, gamma, eps: float, want_dx: bool = True, want_dparams: 
     db = np.empty(N, np.float64) if want_dparams else None
     if _load().oracle_layernorm_bwd(dy, x, gamma, M, N, eps, _ptr(dx), _ptr(dg), _ptr(db)) != 0:
         raise MemoryError("oracle: out of host memory")
+    if dx is not None and dres is not None:
+        dx += _f64(dres)
     return dx, dg, db
+
+
+def residual_add(x, r, dtype=None):
+    """The residual sum a fused "add + norm" normalises and stores: h = x + r,
+    rounded once (round to nearest even) to `dtype`, the storage type of x and
+    r ("bf16", "fp16", "fp32"; None keeps the exact fp64 sum, for
+    finite-difference checks).  The norm is then taken of the stored h -- the
+    result an unfused h = x + r followed by the norm gives.
+
+    x + r is formed in fp64; for two values of one of these types the fp64 sum
+    is either exact, or (exponents more than 29 apart for fp32, 45 for bf16)
+    so far from a rounding midpoint of the type that rounding it once more
+    gives the same value as rounding the exact sum.  Returns a CPU torch tensor
+    of `dtype` (or an fp64 numpy array)."""
+    s = _f64(x) + _f64(r)
+    if dtype is None:
+        return s
+    import torch
+    t = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[dtype]
+    return torch.from_numpy(s).to(t)

@@ -279,5 +279,122 @@ def pin_torch_fp64():
             _close(dg, gt.grad.numpy(), 1e-11, 1e-12, f"torch {op} dgamma {M}x{N}")
 
 
+# --------------------------------------------------------------------------- residual add + norm
+_DT = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+_PREC = {"bf16": (8, -126), "fp16": (11, -14), "fp32": (24, -126)}  # significand bits, min exponent
+
+
+def round_exact(q: Fraction, dtype: str) -> Fraction:
+    """q rounded to the nearest value of dtype, ties to even, in exact
+    rational arithmetic (normal and subnormal range; no overflow)."""
+    if q == 0:
+        return Fraction(0)
+    p, emin = _PREC[dtype]
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    quantum = Fraction(2) ** (max(e, emin) - (p - 1))
+    n = a / quantum
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return (fl * quantum) * (1 if q > 0 else -1)
+
+
+def pin_residual_rounding():
+    """h = x + r rounded once to the storage type, against exact rational
+    sums rounded by hand: random pairs with exponents up to 40 apart, and sums
+    that fall exactly on a rounding midpoint (ties go to the even value)."""
+    rng = np.random.default_rng(17)
+    for dtype, t in _DT.items():
+        p, _ = _PREC[dtype]
+        xs = rng.normal(size=300) * np.exp2(rng.integers(-10, 10, 300))
+        rs = rng.normal(size=300) * np.exp2(rng.integers(-40, 10, 300))
+        x = torch.tensor(xs).to(t)
+        r = torch.tensor(rs).to(t)
+        one, half = 1.0, 2.0 ** -p  # half an ulp of 1
+        x = torch.cat([x, torch.tensor([one, one + 2 * half, -one, 3.0]).to(t)])
+        r = torch.cat([r, torch.tensor([half, half, -half, 6 * half]).to(t)])
+        h = oracle.residual_add(x, r, dtype)
+        assert h.dtype == t
+        for xi, ri, hi in zip(x.double().tolist(), r.double().tolist(), h.double().tolist()):
+            want = round_exact(Fraction(xi) + Fraction(ri), dtype)
+            assert Fraction(hi) == want, f"{dtype}: {xi!r} + {ri!r} -> {hi!r}, want {float(want)!r}"
+        # the midpoints: 1 + half -> 1 (even); (1 + 2 half) + half -> 1 + 4 half
+        assert h[-4].item() == 1.0 and h[-3].item() == 1.0 + 4 * half and h[-2].item() == -1.0
+
+
+def pin_residual_worked():
+    w = load_worked("residual_worked.txt")
+    eps = float(w["eps"][0][0])
+    x, r, gamma = _arr(w["x"]), _arr(w["r"]), _arr(w["gamma"])[0]
+    dy, dres = _arr(w["dy"]), _arr(w["dres"])
+    for dtype in ("bf16", "fp16", "fp32"):
+        h = oracle.residual_add(x, r, dtype)
+        _close(h.double().numpy(), _arr(w["h"]), 0, 0, f"residual worked h {dtype}")
+        y, rstd = oracle.rmsnorm_fwd(h, gamma, eps)
+        _close(y, _arr(w["y"]), 1e-14, 1e-15, "residual worked y")
+        _close(rstd, _arr(w["rstd"]).ravel(), 1e-14, 0, "residual worked rstd")
+        dx, dg = oracle.rmsnorm_bwd(dy, h, gamma, eps, dres=dres)
+        _close(dx, _arr(w["dx"]), 1e-13, 1e-15, "residual worked dx")
+        _close(dg, _arr(w["dgamma"])[0], 1e-13, 1e-15, "residual worked dgamma")
+
+
+def pin_residual_finite_differences():
+    """With the exact sum (no rounding), the gradient of
+    L = sum dy * norm(x + r) + sum dres * (x + r) with respect to x and to r
+    both equal the oracle's dx with dres added."""
+    for op in ("rms", "ln"):
+        for (M, N) in ((1, 3), (2, 5), (2, 16)):
+            rng = np.random.default_rng(M * 31 + N)
+            x = rng.normal(0.2, 1.3, (M, N))
+            r = rng.normal(-0.1, 0.7, (M, N))
+            gamma = 1.0 + 0.3 * rng.normal(size=N)
+            beta = 0.2 * rng.normal(size=N)
+            dy = rng.normal(size=(M, N))
+            dres = rng.normal(size=(M, N))
+            eps = 1e-2
+
+            def loss(xv, rv):
+                h = oracle.residual_add(xv, rv, None)
+                return _loss(op, h, gamma, beta, dy, eps) + float(np.sum(dres * h))
+
+            h = oracle.residual_add(x, r, None)
+            if op == "rms":
+                dx, _ = oracle.rmsnorm_bwd(dy, h, gamma, eps, dres=dres)
+            else:
+                dx, _, _ = oracle.layernorm_bwd(dy, h, gamma, eps, dres=dres)
+            for which in ("x", "r"):
+                fd = np.zeros_like(x)
+                for i in range(M):
+                    for j in range(N):
+                        if which == "x":
+                            fd[i, j] = _fd(lambda v: loss(v, r), x, (i, j), 1e-4)
+                        else:
+                            fd[i, j] = _fd(lambda v: loss(x, v), r, (i, j), 1e-4)
+                _close(dx, fd, 0, 1e-8 * max(1.0, np.abs(fd).max()), f"{op} residual FD d{which} {M}x{N}")
+
+
+def pin_residual_special_cases():
+    """r = 0 stores h = x and normalises x; dres = 0 leaves dx as the plain
+    backward; for LayerNorm, dx - dres sums to zero along each row."""
+    rng = np.random.default_rng(23)
+    M, N = 4, 24
+    x = torch.tensor(rng.normal(size=(M, N))).to(torch.bfloat16)
+    gamma = 1.0 + 0.1 * rng.normal(size=N)
+    dy = rng.normal(size=(M, N))
+    h = oracle.residual_add(x, torch.zeros(M, N, dtype=torch.bfloat16), "bf16")
+    assert torch.equal(h, x)
+    dx0, _ = oracle.rmsnorm_bwd(dy, h, gamma, 1e-6)
+    dxz, _ = oracle.rmsnorm_bwd(dy, h, gamma, 1e-6, dres=np.zeros((M, N)))
+    assert np.array_equal(dx0, dxz)
+    dres = rng.normal(size=(M, N))
+    dxl, _, _ = oracle.layernorm_bwd(dy, h, gamma, 1e-5, dres=dres)
+    _close((dxl - dres).sum(axis=1), np.zeros(M), 0, 1e-12, "ln residual: sum (dx - dres) = 0")
+
+
 ALL_PINS = [pin_worked_rms, pin_worked_ln, pin_finite_differences, pin_forward_invariants,
-            pin_backward_invariants, pin_special_cases, pin_torch_fp64]
+            pin_backward_invariants, pin_special_cases, pin_torch_fp64, pin_residual_rounding,
+            pin_residual_worked, pin_residual_finite_differences, pin_residual_special_cases]

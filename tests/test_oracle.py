@@ -32,3 +32,15 @@ def test_worked_fixtures_are_exact_by_construction():
         assert 1 / (r * r) == var + eps
         assert [(v - mu) * r * g + b for v, g, b in zip(xr, w["gamma"][0], w["beta"][0])] == yr
     assert F(0) == sum(w["dx"][0]) == sum(w["dx"][1])  # LayerNorm: each dx row sums to zero
+
+
+def test_residual_fixture_is_exact_by_construction():
+    """The residual fixture: h = x + r exactly; its rows are the worked RMSNorm
+    rows (same eps, gamma, dy, so the same y and dgamma); dx is that example's
+    dx plus dres."""
+    r = P.load_worked("residual_worked.txt")
+    w = P.load_worked("rmsnorm_worked.txt")
+    assert r["eps"] == w["eps"] and r["gamma"] == w["gamma"] and r["dy"] == w["dy"]
+    assert [[a + b for a, b in zip(xr, rr)] for xr, rr in zip(r["x"], r["r"])] == r["h"] == w["x"]
+    assert r["y"] == w["y"] and r["rstd"] == w["rstd"] and r["dgamma"] == w["dgamma"]
+    assert [[a + b for a, b in zip(dr, sr)] for dr, sr in zip(w["dx"], r["dres"])] == r["dx"]

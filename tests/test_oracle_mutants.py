@@ -66,3 +66,64 @@ def test_pins_catch_planted_mistake(tmp_path, monkeypatch, name, old, new):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake {name!r}"
+
+
+# Mistakes in the residual add + norm part of the oracle (its Python layer),
+# planted by wrapping the oracle's functions for the duration of one case.
+def _mut_dres_dropped(orig):
+    def f(*a, dres=None, **k):
+        return orig(*a, **k)
+    return f
+
+
+def _mut_dres_subtracted(orig):
+    def f(*a, dres=None, **k):
+        return orig(*a, dres=None if dres is None else -oracle._f64(dres), **k)
+    return f
+
+
+def _mut_sum_not_rounded(orig):
+    def f(x, r, dtype=None):
+        import torch
+        return orig(x, r, None) if dtype is None else torch.from_numpy(orig(x, r, None))
+    return f
+
+
+def _mut_residual_not_added(orig):
+    def f(x, r, dtype=None):
+        return orig(x, 0 * oracle._f64(r), dtype)
+    return f
+
+
+def _mut_round_toward_zero(orig):
+    def f(x, r, dtype=None):
+        import torch
+        h = orig(x, r, dtype)
+        if dtype is None:
+            return h
+        s = torch.from_numpy(oracle._f64(x) + oracle._f64(r))
+        # one step toward zero wherever rounding went away from zero
+        return torch.where(h.double().abs() > s.abs(), torch.nextafter(h, torch.zeros_like(h)), h)
+    return f
+
+
+RESIDUAL_MUTANTS = [
+    ("dres_dropped", ("rmsnorm_bwd", "layernorm_bwd"), _mut_dres_dropped),
+    ("dres_subtracted", ("rmsnorm_bwd", "layernorm_bwd"), _mut_dres_subtracted),
+    ("sum_not_rounded", ("residual_add",), _mut_sum_not_rounded),
+    ("residual_not_added", ("residual_add",), _mut_residual_not_added),
+    ("round_toward_zero", ("residual_add",), _mut_round_toward_zero),
+]
+
+
+@pytest.mark.parametrize("name,fns,make", RESIDUAL_MUTANTS, ids=[m[0] for m in RESIDUAL_MUTANTS])
+def test_pins_catch_planted_residual_mistake(monkeypatch, name, fns, make):
+    for fn in fns:
+        monkeypatch.setattr(oracle, fn, make(getattr(oracle, fn)))
+    caught = []
+    for pin in P.ALL_PINS:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name!r}"
