@@ -13,6 +13,16 @@ Workspace traffic counts as time, never as bytes.  L2 is flushed (a 1 GiB
 write, then a 512 MiB read so the lines left are clean; outside the events)
 before every timed call.
 
+The JSON line's "families" object adds every other workload of the path,
+timed per shape and direction in the same run (median of 5 calls, L2 flushed
+before each): RMSNorm 1024x1024; LayerNorm 16384 x {4096, 8192}; RMSNorm and
+LayerNorm 2048 x {16K, 32K, 64K, 128K}; RMSNorm and LayerNorm 16384 x {4096,
+5120, 8192} in bf16, fp16 and fp32 with the accumulation-stress inputs; the
+sweep above in the same form; and ("general_form") the strided, mixed-type
+and residual-add calls of norm_fwd_ex / norm_bwd_ex at 16384 x 8192.  For each family the largest row length is
+held to the targets: forward >= 0.85 and backward >= 0.75 of the measured
+copy peak.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs the same per-GPU workload (weak
 scaling); rank 0 prints one JSON line.
@@ -63,6 +73,42 @@ ROOFLINE_SOURCES = ("tma_kernels.cuh", "device_common.cuh", "params.h",
                     ("api.cu", "// ------------------------------------------------------------------ argument checks"))
 NCU_TRAFFIC = {"sources_digest": "03dc30e100b6e437", "variant": "tma128x2w8", "N": 2048,
                "bytes_per_launch": 537184512 + 232258048}
+
+
+# The other workloads of the path, each timed per shape and direction inside
+# the same run (reported under "families"; not part of `value`):
+# (name, op, dtype, M, row lengths, input distribution).
+FAMILIES = (
+    ("rms_1024x1024", "rms", "bf16", 1024, (1024,), "rms"),
+    ("ln_16384", "ln", "bf16", 16384, (4096, 8192), "ln"),
+    ("wide_rms_2048", "rms", "bf16", 2048, (16384, 32768, 65536, 131072), "rms"),
+    ("wide_ln_2048", "ln", "bf16", 2048, (16384, 32768, 65536, 131072), "rms"),
+) + tuple((f"llm_{op}_16384_{dt}", op, dt, 16384, (4096, 5120, 8192), "llm")
+          for op in ("rms", "ln") for dt in ("bf16", "fp16", "fp32"))
+# The general form (strided rows, a storage type per tensor, fused residual
+# add), timed the same way: (name, op, x dtype, parameter dtype, y dtype, M, N,
+# row stride, residual add).
+EX_FAMILIES = (
+    ("ex_rms_bf16_x_fp32_gamma", "rms", "bf16", "fp32", "bf16", 16384, 8192, 8192, False),
+    ("ex_ln_bf16_x_fp32_gamma", "ln", "bf16", "fp32", "bf16", 16384, 8192, 8192, False),
+    ("ex_rms_fp32_x_bf16_y", "rms", "fp32", "fp32", "bf16", 16384, 8192, 8192, False),
+    ("ex_rms_bf16_strided", "rms", "bf16", "bf16", "bf16", 16384, 8192, 8448, False),
+    ("ex_rms_bf16_residual", "rms", "bf16", "bf16", "bf16", 16384, 8192, 8192, True),
+    ("ex_ln_bf16_residual", "ln", "bf16", "bf16", "bf16", 16384, 8192, 8192, True),
+)
+# Targets on the largest row length of each family (fraction of the measured
+# copy peak): forward 0.85, backward 0.75.
+TARGET = {"fwd": 0.85, "bwd": 0.75}
+ESIZE = {"bf16": 2, "fp16": 2, "fp32": 4}
+DTYPES_T = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+
+
+def alg_bytes(op, direction, m, n, b):
+    """Algorithmic bytes of one call: x, gamma, y, rstd (+ beta, mean) forward;
+    dy, x, gamma, rstd, dx, dgamma (+ mean, dbeta) backward."""
+    if direction == "fwd":
+        return 2 * m * n * b + n * b + 4 * m if op == "rms" else 2 * m * n * b + 2 * n * b + 8 * m
+    return 3 * m * n * b + n * b + 4 * m + 4 * n if op == "rms" else 3 * m * n * b + n * b + 8 * m + 8 * n
 
 
 def fwd_bytes(m, n):
@@ -183,39 +229,56 @@ def reduce_max_sum(vals_max, vals_sum, ws):
 
 
 # ---------------------------------------------------------------------------- oracle on the host
-def oracle_sample(rows_per_n: int, seed: int = 20261202):
-    """Time the fp64 oracle (as it stands) on `rows_per_n` rows of every N of
-    the workload: forward plus backward (dx and dgamma).  Returns
-    (bytes, seconds, threads)."""
+def oracle_inputs(rows_per_n: int, seed: int = 20261202):
+    """float64 host copies of `rows_per_n` rows of every N of the workload
+    (drawn and promoted outside any timing)."""
     import numpy as np
-
-    import oracle
-    tot_b, tot_t = 0, 0.0
+    out = []
     for n in NS:
         inp = make_inputs(rows_per_n, n, dtype="bf16", dist="rms", op="rms", seed=seed)
-        x = np.ascontiguousarray(inp.x.double().numpy())
-        dy = np.ascontiguousarray(inp.dy.double().numpy())
-        g = np.ascontiguousarray(inp.gamma.double().numpy())
+        out.append((n, np.ascontiguousarray(inp.x.double().numpy()),
+                    np.ascontiguousarray(inp.dy.double().numpy()),
+                    np.ascontiguousarray(inp.gamma.double().numpy())))
+    return out
+
+
+def oracle_pass(data):
+    """One timed pass of the fp64 oracle (as it stands) over `data`: forward
+    plus backward (dx and dgamma) at every N.  Returns (bytes, seconds)."""
+    import oracle
+    tot_b, tot_t = 0, 0.0
+    for n, x, dy, g in data:
         t0 = time.perf_counter()
         oracle.rmsnorm_fwd(x, g, EPS)
         oracle.rmsnorm_bwd(dy, x, g, EPS)
         tot_t += time.perf_counter() - t0
-        tot_b += fwd_bytes(rows_per_n, n) + bwd_bytes(rows_per_n, n)
-    return tot_b, tot_t, oracle.threads()
+        tot_b += fwd_bytes(x.shape[0], n) + bwd_bytes(x.shape[0], n)
+    return tot_b, tot_t
 
 
 def cpu_baseline(target_s: float = 10.0):
     """The oracle on a bounded sample of the workload: `rows` rows at every N,
-    repeated until about target_s seconds of oracle time have been spent."""
-    rows = 8192
-    b, t, th = oracle_sample(rows)
-    reps = 1
-    while t < target_s and reps < 64:
-        b1, t1, th = oracle_sample(rows)
-        b, t, reps = b + b1, t + t1, reps + 1
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": th, "kind": "oracle",
-            "sample": f"{rows} of {M} rows at each N of the sweep, fwd+bwd, timed {reps} times "
-                      f"({t:.1f} s of oracle time; bf16 inputs promoted to fp64 outside the timing)"}
+    timed repeatedly on all host threads (median pass; about target_s seconds
+    of oracle time), and once on one thread for a per-core figure."""
+    import oracle
+    rows = 16384
+    data = oracle_inputs(rows)
+    th = oracle.threads()
+    b, t = oracle_pass(data)
+    reps = max(3, min(31, int(target_s / max(t, 1e-3))))
+    ts = [t] + [oracle_pass(data)[1] for _ in range(reps - 1)]
+    t_med = statistics.median(ts)
+    one = oracle_inputs(1024)
+    oracle.set_threads(1)
+    try:
+        b1, t1 = oracle_pass(one)
+    finally:
+        oracle.set_threads(th)
+    return {"value": b / t_med / 1e9, "unit": "GB/s", "cores": th, "kind": "oracle",
+            "sample": f"{rows} of {M} rows at each N of the sweep, fwd+bwd; median of {reps} passes "
+                      f"({sum(ts):.1f} s of oracle time; bf16 inputs promoted to fp64 outside the timing)",
+            "value_1_thread": b1 / t1 / 1e9,
+            "sample_1_thread": f"1024 rows at each N, one pass on one thread ({t1:.1f} s)"}
 
 
 def run_reference(args, ws, rank):
@@ -223,12 +286,14 @@ def run_reference(args, ws, rank):
     each step a bounded row sample of it."""
     if rank != 0:
         return
+    import oracle
     rows = 4096
+    data = oracle_inputs(rows)
     for _ in range(args.warmup):
-        oracle_sample(rows // 8)
-    tb, tt, th = 0, 0.0, 1
+        oracle_pass(data)
+    tb, tt, th = 0, 0.0, oracle.threads()
     for _ in range(args.steps):
-        b, t, th = oracle_sample(rows)
+        b, t = oracle_pass(data)
         tb += b
         tt += t
     v = tb / tt / 1e9
@@ -407,6 +472,35 @@ def run_ours(args, ws, rank, local):
         e2e = {"value": be / (te * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
+    families = None
+    if rank == 0 and not args.no_families:
+        fam_clock = ClockSampler(local)
+        fam_clock.start()
+        families = run_families(gb, dev, stream, flush_l2)
+        families["rms_1024x1024"]["graph_100_calls"] = graph_per_call(gb, dev, stream, flush_l2)
+        ex_fam = run_ex_families(gb, dev, stream, flush_l2)
+        fam_clk = fam_clock.stop()
+        # the sweep above, in the same form
+        peak_, _ = peak_hbm()
+        sweep = {}
+        for n, p in sorted(per.items()):
+            sweep[str(n)] = {d: {"gbs": round(nb / (statistics.median(p[k]) * 1e-3) / 1e9, 1),
+                                 "frac": round(nb / (statistics.median(p[k]) * 1e-3) / 1e9 / peak_, 4),
+                                 "ms": round(statistics.median(p[k]), 5),
+                                 "variant": gb.variant_name(False, di, M, n, torch.bfloat16)}
+                             for d, k, nb, di in (("fwd", "fwd_ms", fwd_bytes(M, n), 0),
+                                                  ("bwd", "bwd_ms", bwd_bytes(M, n), 1))}
+        big = sweep[str(NS[-1])]
+        families = {"rms_sweep_65536": {"op": "rms", "dtype": "bf16", "M": M, "dist": "rms", "shapes": sweep,
+                                        "largest": {"N": NS[-1], "fwd_frac": big["fwd"]["frac"],
+                                                    "bwd_frac": big["bwd"]["frac"],
+                                                    "meets_target": big["fwd"]["frac"] >= TARGET["fwd"]
+                                                    and big["bwd"]["frac"] >= TARGET["bwd"]}},
+                    **families, "general_form": ex_fam, "clocks": fam_clk,
+                    "timing": "per shape and direction: median of 5 CUDA-event-timed calls after 3 "
+                              "warm-up calls, L2 flushed before each; inputs drawn on the device; "
+                              "rms_1024x1024 also as a CUDA graph of 100 calls on rotating buffers"}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = cpu_baseline(args.cpu_seconds)
@@ -436,9 +530,186 @@ def run_ours(args, ws, rank, local):
             "gpu_launches": args.steps * len(NS) * 3,
             "clocks": clocks,
             "breakdown": breakdown,
+            "families": families,
             "kernel_digest": digest,
         }
         print(json.dumps(line), flush=True)
+
+
+def run_families(gb, dev, stream, flush_l2, steps=5, warmup=3):
+    """Every other workload of the path, per shape and direction: median
+    CUDA-event time of `steps` calls (L2 flushed before each, outside the
+    events), effective GB/s, fraction of the measured copy peak, and the
+    variant that ran.  Inputs are drawn on the device with the same recipe."""
+    peak, _ = peak_hbm()
+    out = {}
+    for name, op, dt, m, ns, dist in FAMILIES:
+        ln, b = op == "ln", ESIZE[dt]
+        shapes = {}
+        for n in ns:
+            inp = make_inputs(m, n, dtype=dt, dist=dist, op=op, device=str(dev))
+            x, dy, g, be = inp.x, inp.dy, inp.gamma, inp.beta
+            y, dx = torch.empty_like(x), torch.empty_like(x)
+            mean, rstd = torch.empty(m, device=dev), torch.empty(m, device=dev)
+            dg, db = torch.empty(n, device=dev), torch.empty(n, device=dev)
+            wsb = torch.empty(gb.norm_bwd_workspace_size(ln, m, n, x.dtype), device=dev, dtype=torch.uint8)
+
+            def fwd():
+                if ln:
+                    gb.layernorm_fwd(x, g, be, inp.eps, y=y, mean=mean, rstd=rstd)
+                else:
+                    gb.rmsnorm_fwd(x, g, inp.eps, y=y, rstd=rstd)
+
+            def bwd():
+                if ln:
+                    gb.layernorm_bwd(dy, x, g, mean, rstd, dx=dx, dgamma=dg, dbeta=db, workspace=wsb)
+                else:
+                    gb.rmsnorm_bwd(dy, x, g, rstd, dx=dx, dgamma=dg, workspace=wsb)
+
+            res = {}
+            for d, call in (("fwd", fwd), ("bwd", bwd)):
+                for _ in range(warmup):
+                    flush_l2()
+                    call()
+                evs = []
+                for _ in range(steps):
+                    flush_l2()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    call()
+                    e1.record(stream)
+                    evs.append((e0, e1))
+                torch.cuda.synchronize()
+                ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+                gbs = alg_bytes(op, d, m, n, b) / (ms * 1e-3) / 1e9
+                res[d] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "ms": round(ms, 5),
+                          "variant": gb.variant_name(ln, 0 if d == "fwd" else 1, m, n, x.dtype)}
+            shapes[str(n)] = res
+            del inp, x, dy, g, be, y, dx, mean, rstd, dg, db, wsb
+        big = shapes[str(ns[-1])]
+        out[name] = {"op": op, "dtype": dt, "M": m, "dist": dist, "shapes": shapes,
+                     "largest": {"N": ns[-1], "fwd_frac": big["fwd"]["frac"], "bwd_frac": big["bwd"]["frac"],
+                                 "meets_target": big["fwd"]["frac"] >= TARGET["fwd"]
+                                 and big["bwd"]["frac"] >= TARGET["bwd"]}}
+    torch.cuda.empty_cache()
+    return out
+
+
+def ex_bytes(op, direction, m, n, bx, bp, by, residual):
+    """Algorithmic bytes of one general-form call: forward x (+ residual in,
+    h out), y, gamma (+ beta), rstd (+ mean); backward dy, x (h), dx
+    (+ the residual gradient in), gamma, rstd (+ mean), dgamma (+ dbeta)."""
+    ln = op == "ln"
+    if direction == "fwd":
+        return m * n * (bx + (2 * bx if residual else 0) + by) + n * bp * (2 if ln else 1) + 4 * m * (2 if ln else 1)
+    return m * n * (by + bx + bx + (bx if residual else 0)) + n * bp + 4 * m * (2 if ln else 1) + \
+        4 * n * (2 if ln else 1)
+
+
+def run_ex_families(gb, dev, stream, flush_l2, steps=5, warmup=3):
+    """The general form's workloads (EX_FAMILIES), per direction: median
+    CUDA-event time, effective GB/s and fraction of the measured copy peak."""
+    peak, _ = peak_hbm()
+    out = {}
+    for name, op, xd, pd, yd, m, n, ld, residual in EX_FAMILIES:
+        ln = op == "ln"
+        inp = make_inputs(m, n, dtype=xd, dist="llm", op=op, device=str(dev), param_dtype=pd, dy_dtype=yd)
+
+        def rows(t):  # t inside a buffer of row stride ld
+            buf = torch.empty(m, ld, device=dev, dtype=t.dtype)
+            v = buf[:, :n]
+            v.copy_(t)
+            return v
+        x, dy = rows(inp.x), rows(inp.dy)
+        r = rows(make_inputs(m, n, dtype=xd, op=op, device=str(dev), seed=5).x) if residual else None
+        dres = rows(make_inputs(m, n, dtype=xd, op=op, device=str(dev), seed=6).dy) if residual else None
+        y, dx = rows(torch.empty(m, n, device=dev, dtype=DTYPES_T[yd])), rows(torch.empty_like(inp.x))
+        h = rows(torch.empty_like(inp.x)) if residual else None
+        g, be = inp.gamma, inp.beta if ln else None
+        mean = torch.empty(m, device=dev) if ln else None
+        rstd = torch.empty(m, device=dev)
+        dg, db = torch.empty(n, device=dev), torch.empty(n, device=dev) if ln else None
+        wsb = torch.empty(gb.norm_bwd_ex_workspace_size(ln, m, n), device=dev, dtype=torch.uint8)
+
+        def fwd():
+            gb.norm_fwd_ex(ln, x, g, be, inp.eps, residual=r, y=y, h=h, mean=mean, rstd=rstd)
+
+        def bwd():
+            gb.norm_bwd_ex(ln, dy, h if residual else x, g, mean, rstd, dres=dres, dx=dx, dgamma=dg, dbeta=db,
+                           workspace=wsb)
+
+        res = {"op": op, "x_dtype": xd, "param_dtype": pd, "y_dtype": yd, "M": m, "N": n, "row_stride": ld,
+               "residual": residual}
+        for d, call in (("fwd", fwd), ("bwd", bwd)):
+            for _ in range(warmup):
+                flush_l2()
+                call()
+            evs = []
+            for _ in range(steps):
+                flush_l2()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+            nb = ex_bytes(op, d, m, n, ESIZE[xd], ESIZE[pd], ESIZE[yd], residual)
+            gbs = nb / (ms * 1e-3) / 1e9
+            res[d] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "ms": round(ms, 5)}
+        out[name] = res
+        del inp, x, dy, r, dres, y, dx, h, wsb
+    torch.cuda.empty_cache()
+    return out
+
+
+def graph_per_call(gb, dev, stream, flush_l2, m=1024, n=1024, calls=100):
+    """RMSNorm bf16 [m, n], forward and backward, as the per-call time of a
+    CUDA graph of `calls` back-to-back calls on rotating buffers (calls x the
+    buffers of one call exceed L2, so every call reads its inputs from DRAM).
+    A launch-bound shape's throughput when the launches are not in the way."""
+    sets = []
+    for i in range(calls):
+        inp = make_inputs(m, n, dtype="bf16", op="rms", device=str(dev), seed=1000 + i)
+        sets.append({"x": inp.x, "dy": inp.dy, "g": inp.gamma, "y": torch.empty_like(inp.x),
+                     "dx": torch.empty_like(inp.x), "rstd": torch.empty(m, device=dev),
+                     "dg": torch.empty(n, device=dev),
+                     "ws": torch.empty(gb.norm_bwd_workspace_size(False, m, n, torch.bfloat16), device=dev,
+                                       dtype=torch.uint8)})
+    out = {}
+    peak, _ = peak_hbm()
+    for d in ("fwd", "bwd"):
+        def body():
+            for b in sets:
+                if d == "fwd":
+                    gb.rmsnorm_fwd(b["x"], b["g"], EPS, y=b["y"], rstd=b["rstd"])
+                else:
+                    gb.rmsnorm_bwd(b["dy"], b["x"], b["g"], b["rstd"], dx=b["dx"], dgamma=b["dg"],
+                                   workspace=b["ws"])
+        try:
+            body()  # warm-up outside the capture (first-call set-up)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                body()
+            ts = []
+            for _ in range(5):
+                flush_l2()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            us = statistics.median(ts) * 1e3 / calls
+            nb = (fwd_bytes if d == "fwd" else bwd_bytes)(m, n)
+            gbs = nb / (us * 1e-6) / 1e9
+            out[d] = {"us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        except Exception as e:  # a capture this torch build refuses: say so
+            out[d] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    del sets
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_case(args):
@@ -448,18 +719,20 @@ def run_case(args):
     op, d, n = args.case.split(":")
     n, ln, bwd = int(n), op == "ln", d == "bwd"
     m = args.rows or M
+    dt = args.dtype
+    b = ESIZE[dt]
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    inp = make_inputs(m, n, dtype="bf16", dist="ln" if ln else "rms", op=op)
-    x, dy, g, b = (t.to(dev) for t in (inp.x, inp.dy, inp.gamma, inp.beta))
+    inp = make_inputs(m, n, dtype=dt, dist=args.dist or ("ln" if ln else "rms"), op=op, device="cuda")
+    x, dy, g, be = inp.x, inp.dy, inp.gamma, inp.beta
     y, dx = torch.empty_like(x), torch.empty_like(x)
     mean, rstd = torch.empty(m, device=dev), torch.empty(m, device=dev)
     dg, db = torch.empty(n, device=dev), torch.empty(n, device=dev)
-    ws = torch.empty(gb.norm_bwd_workspace_size(ln, m, n, torch.bfloat16), device=dev, dtype=torch.uint8)
+    ws = torch.empty(gb.norm_bwd_workspace_size(ln, m, n, x.dtype), device=dev, dtype=torch.uint8)
 
     def fwd():
         if ln:
-            gb.layernorm_fwd(x, g, b, inp.eps, y=y, mean=mean, rstd=rstd)
+            gb.layernorm_fwd(x, g, be, inp.eps, y=y, mean=mean, rstd=rstd)
         else:
             gb.rmsnorm_fwd(x, g, inp.eps, y=y, rstd=rstd)
 
@@ -470,7 +743,7 @@ def run_case(args):
             gb.rmsnorm_bwd(dy, x, g, rstd, dx=dx, dgamma=dg, workspace=ws)
 
     if args.variant:
-        gb.force_variant(ln, int(bwd), torch.bfloat16, args.variant)
+        gb.force_variant(ln, int(bwd), x.dtype, args.variant)
     fwd()
     call = bwd_ if bwd else fwd
     for _ in range(args.warmup):
@@ -485,9 +758,9 @@ def run_case(args):
         e.synchronize()
         ts.append(a.elapsed_time(e))
     ms = statistics.median(ts)
-    nbytes = (bwd_bytes(m, n) if bwd else fwd_bytes(m, n)) if not ln else (
-        3 * m * n * B + n * B + 8 * m + 8 * n if bwd else 2 * m * n * B + 2 * n * B + 8 * m)
-    print(json.dumps({"case": args.case, "M": m, "N": n, "variant": gb.variant_name(ln, int(bwd), m, n, torch.bfloat16),
+    nbytes = alg_bytes(op, d, m, n, b)
+    print(json.dumps({"case": args.case, "dtype": dt, "M": m, "N": n,
+                      "variant": gb.variant_name(ln, int(bwd), m, n, x.dtype),
                       "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "l2": "not flushed"}), flush=True)
 
 
@@ -499,11 +772,15 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--no-families", action="store_true",
+                    help="skip the per-shape timing of the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--case", help="op:dir:N (e.g. rms:bwd:2048): time one call shape of bf16 rows "
                                    "only, for profiling one kernel")
     ap.add_argument("--rows", type=int, default=0, help="rows for --case (default 65536)")
     ap.add_argument("--variant", help="with --case: force this kernel variant (profiling)")
+    ap.add_argument("--dtype", default="bf16", choices=("bf16", "fp16", "fp32"), help="with --case")
+    ap.add_argument("--dist", default=None, choices=("rms", "ln", "llm"), help="with --case")
     args = ap.parse_args(argv)
     if args.case:
         run_case(args)

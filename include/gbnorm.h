@@ -39,18 +39,14 @@
  *     them share it.  Arithmetic is float32 throughout; each output element
  *     is rounded once to dtype, round-to-nearest-even.
  *   - Ownership: the caller allocates and owns every buffer.  The library
- *     never allocates device memory, never frees, and never synchronises
- *     (except the one-time copy of the default parameters below).  All work
- *     is enqueued on `stream` (NULL = the legacy default stream) and
- *     completes asynchronously.
+ *     never allocates device memory, never frees, and never synchronises.
+ *     All work is enqueued on `stream` (NULL = the legacy default stream)
+ *     and completes asynchronously.
  *   - Optional parameters: gamma may be NULL in every entry point (gamma_j =
  *     1: RMSNorm or LayerNorm without a scale), beta may be NULL in
  *     layernorm_fwd (beta_j = 0: no bias), and dgamma / dbeta may be NULL in
- *     the backward (that column sum is not produced).  A NULL gamma or beta
- *     needs N <= GBNORM_DEFAULT_PARAM_MAX_N (else GBNORM_ERR_UNSUPPORTED): the
- *     library reads constant rows of ones / zeros that it keeps on each
- *     device, copied there (synchronously, once per device) by the first call
- *     that needs them.
+ *     the backward (that column sum is not produced).  The kernels use the
+ *     constants in place of the missing row; nothing is read for it.
  *   - Alignment: with 16-byte-aligned pointers and N * sizeof(dtype) a
  *     multiple of 16, rows move as 128-bit vectors; anything else takes a
  *     correct element-wise path.
@@ -95,9 +91,6 @@ typedef enum {
 
 /* Largest row length N accepted by every entry point. */
 #define GBNORM_MAX_N ((int64_t)1 << 24)
-
-/* Largest row length N for which gamma or beta may be NULL (see above). */
-#define GBNORM_DEFAULT_PARAM_MAX_N ((int64_t)1 << 18)
 
 /*
  * RMSNorm forward.
@@ -155,6 +148,69 @@ int layernorm_bwd(const void *dy, const void *x, const void *gamma, const float 
                   const float *rstd, void *dx, float *dgamma, float *dbeta, void *workspace,
                   size_t workspace_bytes, int64_t M, int64_t N, int dtype,
                   gbnorm_stream_t stream);
+
+/*
+ * General form: strided rows, a storage type per tensor, and a residual add
+ * fused in front of the norm.
+ *
+ * Rows with a stride other than N and optional gamma / beta are the path's
+ * first ranked extension, parameters and outputs in their own types (for
+ * example bf16 rows with fp32 gamma, or fp32 rows with a bf16 y) the second,
+ * and the fused residual add the third; the "Fused RMSNorm" page's "How it
+ * works" section (16-bit storage, fp32 arithmetic) and the "SOTA
+ * normalization performance with torch.compile" page's paragraphs on fusing a
+ * norm with its neighbouring operations describe the motivation.  What is
+ * computed is the definition at the top of this file, with:
+ *
+ *   h_ij = rnd_x(x_ij + r_ij)  when a residual r is given (else h = x): the
+ *          sum in fp32, rounded once to x_dtype -- what an unfused h = x + r
+ *          followed by the norm computes; h is normalised and, if `h` is
+ *          given, stored.
+ *   y    = the forward of h, rounded once to y_dtype.
+ *   dx   = the input gradient of the norm at h, plus dres (the gradient that
+ *          reaches h from the residual stream), rounded once to x_dtype; it is
+ *          the gradient of both x and r.
+ *
+ * Arguments:
+ *   is_layernorm  0 RMSNorm, 1 LayerNorm.
+ *   M, N          rows and row length (M >= 0, 1 <= N <= GBNORM_MAX_N).
+ *   x, ldx, x_dtype           [M] rows of N elements, row i at x + i * ldx
+ *                             elements (ldx >= N); read only.
+ *   residual, ldr             rows of x_dtype, or NULL (no residual add).
+ *   h, ldh                    rows of x_dtype written with the residual sum,
+ *                             or NULL (not stored); must be NULL without a
+ *                             residual.
+ *   gamma, beta, param_dtype  [N] each, or NULL (1 / 0); beta LayerNorm only.
+ *   y, ldy, y_dtype           output rows.
+ *   mean, rstd                [M] float32, written; may be NULL (mean is
+ *                             LayerNorm only).
+ *   dy, lddy, y_dtype         [M] rows: gradient of y, read only.
+ *   x, ldx, x_dtype (bwd)     the rows that were normalised (h when the
+ *                             forward added a residual), read only.
+ *   dres, lddres              rows of x_dtype added into dx, or NULL.
+ *   dx, lddx                  rows of x_dtype, written.
+ *   dgamma, dbeta             [N] float32, written; may be NULL.
+ *   workspace                 at least norm_bwd_ex_workspace_size(is_layernorm,
+ *                             M, N) bytes, 16-byte aligned, not shared with a
+ *                             concurrent call.
+ *
+ * An output may be exactly one of the inputs (same address, row stride and
+ * element size: in place, e.g. h over r, or dx over dres or dy); any other
+ * overlap of the spans [p, p + ((M - 1) * ld + N) * size) is rejected, and dx
+ * may not be x.  With every row 16-byte aligned (base and stride), N a
+ * multiple of 8 and 16-byte-aligned gamma / beta, rows move as 16-byte
+ * vectors; anything else takes a correct element-wise path.  Status codes,
+ * ownership, streams and threading as above.
+ */
+int norm_fwd_ex(int is_layernorm, int64_t M, int64_t N, float eps, const void *x, int64_t ldx, int x_dtype,
+                const void *residual, int64_t ldr, void *h, int64_t ldh, const void *gamma, const void *beta,
+                int param_dtype, void *y, int64_t ldy, int y_dtype, float *mean, float *rstd,
+                gbnorm_stream_t stream);
+size_t norm_bwd_ex_workspace_size(int is_layernorm, int64_t M, int64_t N);
+int norm_bwd_ex(int is_layernorm, int64_t M, int64_t N, const void *dy, int64_t lddy, int y_dtype,
+                const void *x, int64_t ldx, int x_dtype, const void *dres, int64_t lddres, const void *gamma,
+                int param_dtype, const float *mean, const float *rstd, void *dx, int64_t lddx, float *dgamma,
+                float *dbeta, void *workspace, size_t workspace_bytes, gbnorm_stream_t stream);
 
 /*
  * RMSNorm backward without a caller-provided workspace.

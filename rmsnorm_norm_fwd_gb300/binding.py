@@ -31,6 +31,12 @@ lib.norm_bwd_workspace_size.argtypes = [_int, _i64, _i64, _int]
 lib.norm_bwd_workspace_size.restype = _sz
 lib.rmsnorm_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _int, _vp]
 lib.layernorm_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _int, _vp]
+lib.norm_fwd_ex.argtypes = [_int, _i64, _i64, _f, _vp, _i64, _int, _vp, _i64, _vp, _i64, _vp, _vp, _int,
+                            _vp, _i64, _int, _vp, _vp, _vp]
+lib.norm_bwd_ex_workspace_size.argtypes = [_int, _i64, _i64]
+lib.norm_bwd_ex_workspace_size.restype = _sz
+lib.norm_bwd_ex.argtypes = [_int, _i64, _i64, _vp, _i64, _int, _vp, _i64, _int, _vp, _i64, _vp, _int, _vp, _vp,
+                            _vp, _i64, _vp, _vp, _vp, _sz, _vp]
 lib.gbnorm_status_string.argtypes = [_int]
 lib.gbnorm_status_string.restype = ctypes.c_char_p
 lib.gbnorm_variant_name.argtypes = [_int, _int, _i64, _i64, _int, _int, ctypes.c_char_p, _sz]
@@ -40,7 +46,8 @@ lib.gbnorm_variant_at.argtypes = [_int, _int, _int, _int]
 lib.gbnorm_variant_at.restype = ctypes.c_char_p
 lib.gbnorm_read_fault.argtypes = [_int, ctypes.POINTER(ctypes.c_int)]
 lib.gbnorm_set_grid_limit.argtypes = [_int]
-for _fn in ("rmsnorm_fwd", "layernorm_fwd", "rmsnorm_bwd", "layernorm_bwd", "gbnorm_variant_name",
+for _fn in ("rmsnorm_fwd", "layernorm_fwd", "rmsnorm_bwd", "layernorm_bwd", "norm_fwd_ex", "norm_bwd_ex",
+            "gbnorm_variant_name",
             "gbnorm_force_variant", "gbnorm_variant_count", "gbnorm_read_fault",
             "gbnorm_set_grid_limit"):
     getattr(lib, _fn).restype = _int
@@ -173,6 +180,93 @@ def layernorm_bwd(dy, x, gamma, mean, rstd, dx=None, dgamma=None, dbeta=None, wo
                                               _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(ws), wsb, M, N,
                                               DTYPE_CODE[x.dtype], _stream(stream)))
     return dx, dgamma, dbeta
+
+
+# ---------------------------------------------------------------------------- general form
+def _rows(name, t):
+    """A 2-D CUDA tensor whose rows are contiguous (any row stride): (ptr, ld)."""
+    if not (t.is_cuda and t.dim() == 2 and (t.stride(1) == 1 or t.shape[1] <= 1)):
+        raise ValueError(f"{name} must be a 2-D CUDA tensor with unit column stride")
+    return t.data_ptr(), max(t.stride(0), t.shape[1])
+
+
+def _code(t, default):
+    return DTYPE_CODE[t.dtype] if t is not None else DTYPE_CODE[default]
+
+
+def norm_fwd_ex(is_layernorm: bool, x, gamma, beta, eps: float, residual=None, store_h: bool = True,
+                y_dtype=None, y=None, h=None, mean=None, rstd=None, save_stats: bool = True, stream=None):
+    """General forward: rows of x (any row stride), optional residual rows
+    (x's dtype) added first, gamma / beta of their own dtype, y of y_dtype
+    (default x's).  Returns (y, h, mean, rstd); h (the stored residual sum) is
+    None without a residual or with store_h False, mean None for RMSNorm."""
+    px, ldx = _rows("x", x)
+    M, N = x.shape
+    pr, ldr = _rows("residual", residual) if residual is not None else (None, N)
+    if residual is not None and (residual.dtype != x.dtype or residual.shape != x.shape):
+        raise ValueError("residual must match x in shape and dtype")
+    if gamma is not None and beta is not None and gamma.dtype != beta.dtype:
+        raise ValueError("gamma and beta must share a dtype")
+    pdt = gamma.dtype if gamma is not None else (beta.dtype if beta is not None else x.dtype)
+    for nm, v in (("gamma", gamma), ("beta", beta)):
+        if v is not None:
+            _vec(nm, v, N, pdt)
+    if y is None:
+        y = torch.empty(M, N, device=x.device, dtype=y_dtype or x.dtype)
+    py, ldy = _rows("y", y)
+    if residual is not None and store_h and h is None:
+        h = torch.empty_like(x, memory_format=torch.contiguous_format)
+    ph, ldh = _rows("h", h) if h is not None else (None, N)
+    if save_stats:
+        rstd = torch.empty(M, device=x.device, dtype=torch.float32) if rstd is None else rstd
+        if is_layernorm:
+            mean = torch.empty(M, device=x.device, dtype=torch.float32) if mean is None else mean
+    _check("norm_fwd_ex", lib.norm_fwd_ex(int(bool(is_layernorm)), M, N, float(eps), px, ldx, DTYPE_CODE[x.dtype],
+                                          pr, ldr, ph, ldh, _ptr(gamma), _ptr(beta), DTYPE_CODE[pdt], py, ldy,
+                                          DTYPE_CODE[y.dtype], _ptr(mean), _ptr(rstd), _stream(stream)))
+    return y, h, mean, rstd
+
+
+def norm_bwd_ex_workspace_size(is_layernorm: bool, M: int, N: int) -> int:
+    return int(lib.norm_bwd_ex_workspace_size(int(bool(is_layernorm)), M, N))
+
+
+def norm_bwd_ex(is_layernorm: bool, dy, x, gamma, mean, rstd, dres=None, dx=None, dgamma=None, dbeta=None,
+                workspace=None, need_dgamma: bool = True, need_dbeta: bool = True, stream=None):
+    """General backward: dy (y's dtype) and x (the normalised rows, h after a
+    residual add) with any row strides, gamma of its own dtype, dres (x's
+    dtype) added into dx.  Returns (dx, dgamma, dbeta) with dx of x's dtype."""
+    pdy, lddy = _rows("dy", dy)
+    px, ldx = _rows("x", x)
+    M, N = x.shape
+    if dy.shape != x.shape:
+        raise ValueError("dy must match x in shape")
+    pdr, lddr = _rows("dres", dres) if dres is not None else (None, N)
+    if dres is not None and (dres.dtype != x.dtype or dres.shape != x.shape):
+        raise ValueError("dres must match x in shape and dtype")
+    if gamma is not None:
+        _vec("gamma", gamma, N, gamma.dtype)
+    _vec("rstd", rstd, M, torch.float32)
+    if is_layernorm:
+        _vec("mean", mean, M, torch.float32)
+    if dx is None:
+        dx = torch.empty(M, N, device=x.device, dtype=x.dtype)
+    pdx, lddx = _rows("dx", dx)
+    if dgamma is None and need_dgamma:
+        dgamma = torch.empty(N, device=x.device, dtype=torch.float32)
+    if is_layernorm and dbeta is None and need_dbeta:
+        dbeta = torch.empty(N, device=x.device, dtype=torch.float32)
+    need = norm_bwd_ex_workspace_size(is_layernorm, M, N)
+    if need == 0:
+        raise GbnormError("norm_bwd_ex_workspace_size", 2)
+    if workspace is None:
+        workspace = torch.empty(need, device=x.device, dtype=torch.uint8)
+    _check("norm_bwd_ex", lib.norm_bwd_ex(int(bool(is_layernorm)), M, N, pdy, lddy, DTYPE_CODE[dy.dtype], px, ldx,
+                                          DTYPE_CODE[x.dtype], pdr, lddr, _ptr(gamma), _code(gamma, x.dtype),
+                                          _ptr(mean if is_layernorm else None), _ptr(rstd), pdx, lddx,
+                                          _ptr(dgamma), _ptr(dbeta if is_layernorm else None), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dx, dgamma, (dbeta if is_layernorm else None)
 
 
 def variant_name(is_layernorm: bool, direction: int, M: int, N: int, dtype, aligned: bool = True) -> str:

@@ -25,10 +25,13 @@ __device__ int g_fault_word;
 namespace {
 
 constexpr int kMaxDev = 64;
-constexpr int kMaxVariants = 64;
+// Bound on the variants of one (op, direction, dtype) table: the per-variant
+// caches below are indexed by variant.  tables_fit() checks it once.
+constexpr int kMaxVariants = 160;
 
 struct DispatchRow {
     int is_ln, dir, dtype;
+    int64_t m_max;  // rows: the row applies to calls with M <= m_max (-1: any M)
     int64_t nv_max;
     const char *variant;
 };
@@ -66,8 +69,30 @@ std::atomic<uint64_t> g_occ_tma[kMaxDev][2][2][3][kMaxVariants];
 std::atomic<int> g_force[2][2][3];
 // Cap on the persistent grid (CTAs), 0 = none (tests and tuning only).
 std::atomic<int> g_grid_limit{0};
+// Call counter of the single-kernel backward variants (their flag epochs).
+std::atomic<uint32_t> g_epoch{0};
+uint32_t next_epoch() {
+    uint32_t e;
+    do {
+        e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    } while (e == 0);
+    return e;
+}
+
+// Every compiled table within the caches' bound (else no call is served).
+bool tables_fit() {
+    static const bool ok = [] {
+        for (int ln = 0; ln < 2; ++ln)
+            for (int dir = 0; dir < 2; ++dir)
+                for (int dt = 0; dt < 3; ++dt)
+                    if (kTables[ln][dir][dt]->count > kMaxVariants) return false;
+        return true;
+    }();
+    return ok;
+}
 
 int current_device(int *dev) {
+    if (!tables_fit()) return GBNORM_ERR_UNSUPPORTED;
     if (cudaGetDevice(dev) != cudaSuccess) return GBNORM_ERR_CUDA;
     if (*dev < 0 || *dev >= kMaxDev) return GBNORM_ERR_UNSUPPORTED;
     DevInfo &d = g_dev[*dev];
@@ -149,6 +174,9 @@ bool tma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, si
         const size_t comb = (size_t)v.consumers() * v.vpt * v.elems_per_vec * 4 * (c.is_ln ? 2 : 1);
         if (comb > ring) ring = comb;
     }
+    // Single-kernel variants sum the partial rows through 16 x 128 floats of
+    // the idle ring.
+    if (v.fused && ring < kSkPartBytes) ring = kSkPartBytes;
     if (ring > budget) return false;
     tc->rows = (int)rt;
     tc->stages = stages;
@@ -184,6 +212,23 @@ bool tmac_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, s
     return true;
 }
 
+// Ring of a bulk-copy wide-row forward: stages of (params + 1) chunks of
+// tpr * vpt 16-byte vectors, as many as fit (at most kTmaMaxStages, at least 2).
+bool wtma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, size_t *dyn_smem) {
+    if (c.dir != 0) return false;
+    const size_t stage = (size_t)(c.is_ln ? 3 : 2) * (size_t)v.tpr * v.vpt * 16u;
+    const size_t budget = (size_t)g_dev[dev].smem_optin - kTmaHeaderBytes;
+    int stages = (int)(budget / stage);
+    if (stages > kTmaMaxStages) stages = kTmaMaxStages;
+    if (stages < 2) return false;
+    tc->rows = 1;
+    tc->stages = stages;
+    tc->stride = (uint32_t)stage;
+    tc->fault = g_dev[dev].fault;
+    *dyn_smem = kTmaHeaderBytes + (size_t)stages * stage;
+    return true;
+}
+
 // Shared memory of a wide-row variant: none for the forward; for the
 // backward each CTA's column slice of dgamma (and dbeta) sums in fp32.  False
 // if a CTA of the cluster would get no columns or the sums do not fit.
@@ -216,6 +261,11 @@ bool can_serve(const Variant &v, const CallShape &c, int dev) {
         size_t dyn;
         return wide_geometry(v, c, dev, &dyn);
     }
+    if (v.kind == kWtma) {
+        TileCfg tc;
+        size_t dyn;
+        return wtma_geometry(v, c, dev, &tc, &dyn);
+    }
     if (v.kind == kRowsS) {
         size_t dyn;
         return rows_s_geometry(v, c, dev, &dyn);
@@ -240,6 +290,7 @@ int find_variant(const VariantTable &t, const char *name) {
 constexpr int kMaxRows = sizeof(kDispatch) / sizeof(kDispatch[0]);
 struct Resolved {
     int n = 0;
+    int64_t m_max[kMaxRows];
     int64_t nv_max[kMaxRows];
     int idx[kMaxRows];
     int elem = -1;
@@ -259,6 +310,7 @@ struct ResolvedAll {
                             continue;
                         const int i = find_variant(t, row.variant);
                         if (i < 0) continue;
+                        o.m_max[o.n] = row.m_max;
                         o.nv_max[o.n] = row.nv_max;
                         o.idx[o.n] = i;
                         ++o.n;
@@ -280,7 +332,7 @@ int select_variant(const CallShape &c, int dev) {
     if (!c.vec) return r.elem;
     const int64_t nv = c.N / (16 / elem_size(c.dtype));
     for (int k = 0; k < r.n; ++k) {
-        if (nv > r.nv_max[k]) continue;
+        if (nv > r.nv_max[k] || (r.m_max[k] >= 0 && c.M > r.m_max[k])) continue;
         if (can_serve(t.v[r.idx[k]], c, dev)) return r.idx[k];
     }
     return r.elem;
@@ -301,12 +353,12 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
     int o = slot.load(std::memory_order_relaxed);
     const Variant &v = kTables[c.is_ln][c.dir][c.dtype]->v[idx];
     // Kinds whose shared memory (and so occupancy) depends on the shape.
-    const bool per_shape = v.staged_rows() || v.kind == kRowsS || (v.kind == kWide && dyn_smem > 0);
+    const bool per_shape = v.staged_rows() || v.kind == kRowsS || v.kind == kWtma || (v.kind == kWide && dyn_smem > 0);
     if (o > 0 && !per_shape) {
         *out = o;
         return GBNORM_OK;
     }
-    if (v.staged_rows() || v.kind == kTmaCl || v.kind == kRowsS || (v.kind == kWide && dyn_smem > 0)) {
+    if (v.staged_rows() || v.kind == kTmaCl || v.kind == kRowsS || v.kind == kWtma || (v.kind == kWide && dyn_smem > 0)) {
         std::atomic<uint64_t> &cache = g_occ_tma[dev][c.is_ln][c.dir][c.dtype][idx];
         const uint64_t hit = cache.load(std::memory_order_relaxed);
         if (hit != 0 && (hit >> 16) == (uint64_t)dyn_smem) {
@@ -386,6 +438,7 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
     if (v.kind == kTmaCl && !tmac_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kWide && !wide_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kRowsS && !rows_s_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
+    if (v.kind == kWtma && !wtma_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     int occ = 0;
     int st = occupancy(c, idx, dev, pl->dyn_smem, &occ);
     if (st != GBNORM_OK) return st;
@@ -394,6 +447,14 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
         // Element-wise kernels: one CTA per row at a time.  The backward keeps
         // one partial row per CTA, so it is held to one CTA per SM.
         int64_t cap = c.dir == 0 ? (int64_t)occ * sms : (int64_t)sms;
+        if (limit > 0 && limit < cap) cap = limit;
+        pl->grid = c.M < cap ? c.M : cap;
+        pl->P = pl->grid;
+        return GBNORM_OK;
+    }
+    if (v.kind == kWtma) {
+        // one row per CTA at a time
+        int64_t cap = (int64_t)occ * sms;
         if (limit > 0 && limit < cap) cap = limit;
         pl->grid = c.M < cap ? c.M : cap;
         pl->P = pl->grid;
@@ -446,7 +507,22 @@ int plan_call(const CallShape &c, int dev, Plan *pl) {
 int launch_kernel(const Variant &v, const Plan &pl, void *params, cudaStream_t s) {
     void *args[1] = {params};
     cudaError_t e;
-    if (v.cl == 1) {
+    if (v.fused) {
+        // Single-kernel variants wait for every CTA's partial row: a cooperative
+        // launch guarantees that all CTAs are resident together (the grid is
+        // capped at the measured occupancy), or fails instead of starting.
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.gridDim = dim3((unsigned)pl.grid);
+        cfg.blockDim = dim3(v.cta);
+        cfg.dynamicSmemBytes = pl.dyn_smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelExC(&cfg, v.kernel, args);
+    } else if (v.cl == 1) {
         e = cudaLaunchKernel(v.kernel, dim3((unsigned)pl.grid), dim3(v.cta), args, pl.dyn_smem, s);
     } else {
         cudaLaunchConfig_t cfg = {};
@@ -468,10 +544,6 @@ int launch_kernel(const Variant &v, const Plan &pl, void *params, cudaStream_t s
 }
 
 // ------------------------------------------------------------------ argument checks
-}  // namespace
-// Constant rows read in place of a NULL gamma (ones) or beta (zeros); defaults.cu.
-int default_params(int dtype, const void **ones, const void **zeros);
-namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -516,9 +588,7 @@ int do_fwd(int is_ln, const void *x, const void *gamma, const void *beta, void *
     if (!valid_shape(M, N, dtype)) return GBNORM_ERR_INVALID_ARG;
     if (M > 0 && (!x || !y)) return GBNORM_ERR_INVALID_ARG;
     if (!std::isfinite(eps) || eps < 0.f) return GBNORM_ERR_INVALID_ARG;
-    // A NULL gamma / beta reads the device's constant rows (gamma = 1, beta = 0).
-    const bool no_g = gamma == nullptr, no_b = is_ln && beta == nullptr;
-    if ((no_g || no_b) && N > GBNORM_DEFAULT_PARAM_MAX_N) return GBNORM_ERR_UNSUPPORTED;
+    // A NULL gamma / beta is passed through: the kernels use gamma = 1, beta = 0.
     const size_t b = (size_t)elem_size(dtype);
     const size_t mat = (size_t)M * (size_t)N * b, vec = (size_t)N * b, st = (size_t)M * 4;
     const Buf outs[3] = {{y, mat}, {rstd, st}, {is_ln ? mean : nullptr, st}};
@@ -528,13 +598,6 @@ int do_fwd(int is_ln, const void *x, const void *gamma, const void *beta, void *
     int s = current_device(&dev);
     if (s != GBNORM_OK) return s;
     if (M == 0) return GBNORM_OK;
-    if (no_g || no_b) {
-        const void *ones, *zeros;
-        s = default_params(dtype, &ones, &zeros);
-        if (s != GBNORM_OK) return s;
-        if (no_g) gamma = ones;
-        if (no_b) beta = zeros;
-    }
     CallShape c{is_ln, 0, dtype, M, N, false, true};
     c.vec = (vec % 16) == 0 && aligned16(x) && aligned16(y) && aligned16(gamma) &&
             (!is_ln || aligned16(beta));
@@ -558,21 +621,24 @@ size_t ws_bytes_for(int is_ln, int64_t M, int64_t N, int dtype, int dev, int *st
         Plan pl;
         *status = plan_call(c, dev, &pl);
         if (*status != GBNORM_OK) return 0;
-        const size_t need = (size_t)pl.P * (size_t)N * 4u * (is_ln ? 2u : 1u);
+        // [2][P][N] partial rows (one block for RMSNorm), then P flag words of
+        // the single-kernel variants
+        const size_t need = (size_t)pl.P * (size_t)N * 4u * (is_ln ? 2u : 1u) + (size_t)pl.P * 4u;
         if (need > best) best = need;
     }
     return (best + 255u) & ~(size_t)255u;
 }
+
+int launch_colreduce(int is_ln, const float *wsc, int64_t P, int64_t N, float *dgamma, float *dbeta, bool pdl,
+                     cudaStream_t stream);
 
 int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const float *mean,
            const float *rstd, void *dx, float *dgamma, float *dbeta, void *ws, size_t ws_bytes,
            int64_t M, int64_t N, int dtype, cudaStream_t stream) {
     if (!valid_shape(M, N, dtype)) return GBNORM_ERR_INVALID_ARG;
     if (M > 0 && (!dy || !x || !rstd || !dx || (is_ln && !mean))) return GBNORM_ERR_INVALID_ARG;
-    // A NULL gamma reads the device's row of ones; a NULL dgamma / dbeta is
-    // not produced.
-    const bool no_g = gamma == nullptr;
-    if (no_g && N > GBNORM_DEFAULT_PARAM_MAX_N) return GBNORM_ERR_UNSUPPORTED;
+    // A NULL gamma is passed through (the kernels use gamma = 1); a NULL
+    // dgamma / dbeta is not produced.
     if (!is_ln) dbeta = nullptr;
     const size_t b = (size_t)elem_size(dtype);
     const size_t mat = (size_t)M * (size_t)N * b, vec = (size_t)N * b, st = (size_t)M * 4,
@@ -590,12 +656,6 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
         const Buf all_out[4] = {outs[0], outs[1], outs[2], {ws, need}};
         if (bad_aliasing(all_out, 4, ins, 5, dx, dy)) return GBNORM_ERR_INVALID_ARG;
     }
-    if (no_g && M > 0) {
-        const void *ones, *zeros;
-        s = default_params(dtype, &ones, &zeros);
-        if (s != GBNORM_OK) return s;
-        gamma = ones;
-    }
     int64_t P = 0;
     if (M > 0) {
         CallShape c{is_ln, 1, dtype, M, N, false, false};
@@ -604,18 +664,255 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
         Plan pl;
         s = plan_call(c, dev, &pl);
         if (s != GBNORM_OK) return s;
-        BwdParams p{dy, x, gamma, is_ln ? mean : nullptr, rstd, dx, static_cast<float *>(ws), M, N, pl.tc};
-        s = launch_kernel(kTables[is_ln][1][dtype]->v[pl.idx], pl, &p, stream);
+        const Variant &v = kTables[is_ln][1][dtype]->v[pl.idx];
+        BwdParams p{dy, x, gamma, is_ln ? mean : nullptr, rstd, dx, static_cast<float *>(ws), M, N, pl.tc,
+                    nullptr, nullptr, 0u};
+        if (v.fused) {
+            // The kernel sums the partial rows itself; its flag words follow
+            // the partial rows in the workspace.
+            p.dgamma = dgamma;
+            p.dbeta = dbeta;
+            p.epoch = next_epoch();
+            return launch_kernel(v, pl, &p, stream);
+        }
+        s = launch_kernel(v, pl, &p, stream);
         if (s != GBNORM_OK) return s;
         P = pl.P;
     }
-    // Stage two: column sums of the P partial rows (P = 0 writes zeros); a
-    // NULL output's blocks return at once.
+    return launch_colreduce(is_ln, static_cast<const float *>(ws), P, N, dgamma, dbeta, M > 0, stream);
+}
+
+// ------------------------------------------------------------------ general form
+// Rows with their own strides, a storage type per tensor, a fused residual
+// add (norm_fwd_ex / norm_bwd_ex in include/gbnorm.h).
+
+// Bytes an [M, N] matrix with row stride ld spans.
+size_t span(int64_t M, int64_t N, int64_t ld, int dtype) {
+    return M > 0 ? ((size_t)(M - 1) * (size_t)ld + (size_t)N) * (size_t)elem_size(dtype) : 0;
+}
+
+bool valid_dtype(int d) { return d == GBNORM_F32 || d == GBNORM_F16 || d == GBNORM_BF16; }
+
+// A strided row tensor as the aliasing check sees it.
+struct Mat {
+    const void *p;
+    int64_t ld;
+    int dtype;
+    size_t bytes;
+};
+
+// Outputs may not overlap inputs or each other, except that an output may be
+// exactly an input (same base, row stride and element size): every element is
+// then read before it is written, by the thread that writes it.
+bool bad_aliasing_ex(const Mat *outs, int no, const Mat *ins, int ni) {
+    for (int i = 0; i < no; ++i) {
+        for (int j = 0; j < ni; ++j) {
+            if (outs[i].p && outs[i].p == ins[j].p && outs[i].ld == ins[j].ld &&
+                elem_size(outs[i].dtype) == elem_size(ins[j].dtype) && outs[i].bytes == ins[j].bytes)
+                continue;
+            if (overlap(outs[i].p, outs[i].bytes, ins[j].p, ins[j].bytes)) return true;
+        }
+        for (int j = i + 1; j < no; ++j)
+            if (overlap(outs[i].p, outs[i].bytes, outs[j].p, outs[j].bytes)) return true;
+    }
+    return false;
+}
+
+// 16-byte vectors for a row tensor: aligned base and row stride.
+bool vec_rows(const void *p, int64_t ld, int dtype) {
+    return !p || (aligned16(p) && ((size_t)ld * (size_t)elem_size(dtype)) % 16 == 0);
+}
+
+struct ExPlan {
+    const void *kernel;
+    int64_t grid;
+    size_t dyn;
+    int cta;
+};
+
+// Per (device, is_ln, dir, geometry; the last slot for the element-wise
+// kernel): the dynamic shared-memory limit raised, and the last (shared
+// memory, occupancy) pair.
+std::atomic<int> g_ex_smem_set[kMaxDev][2][2][17];
+std::atomic<uint64_t> g_ex_occ[kMaxDev][2][2][17];
+
+int ex_occupancy(int dev, int is_ln, int dir, int slot, const void *k, int cta, size_t dyn, int *occ) {
+    std::atomic<uint64_t> &cache = g_ex_occ[dev][is_ln][dir][slot];
+    const uint64_t hit = cache.load(std::memory_order_relaxed);
+    if (hit != 0 && (hit >> 16) == (uint64_t)dyn) {
+        *occ = (int)(hit & 0xffff);
+        return GBNORM_OK;
+    }
+    std::atomic<int> &set = g_ex_smem_set[dev][is_ln][dir][slot];
+    if (dyn > 0 && !set.load(std::memory_order_acquire)) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return GBNORM_ERR_CUDA;
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 g_dev[dev].smem_optin - (int)fa.sharedSizeBytes) != cudaSuccess)
+            return GBNORM_ERR_CUDA;
+        set.store(1, std::memory_order_release);
+    }
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, cta, dyn) != cudaSuccess) return GBNORM_ERR_CUDA;
+    if (o <= 0) return GBNORM_ERR_UNSUPPORTED;
+    if (o < 0xffff) cache.store(((uint64_t)dyn << 16) | (uint64_t)o, std::memory_order_relaxed);
+    *occ = o;
+    return GBNORM_OK;
+}
+
+// The smallest row-resident geometry that holds the row (vec: every row
+// tensor allows 16-byte vectors and N % 8 == 0), else the element-wise kernel.
+int ex_plan(int is_ln, int dir, int64_t M, int64_t N, bool vec, int dev, ExPlan *pl) {
+    const ExTable &t = kExTables[is_ln];
+    const int64_t limit = g_grid_limit.load(std::memory_order_relaxed);
+    const int sms = g_dev[dev].sms;
+    if (vec && N % 8 == 0) {
+        for (int i = 0; i < t.count && i < 16; ++i) {
+            const ExVariant &v = t.v[i];
+            if ((int64_t)v.tpr * v.vpt * 8 < N) continue;
+            // fp32 parameters (forward: gamma and beta; backward: gamma, then
+            // the row groups' partials of dgamma and dbeta)
+            const size_t dyn = (size_t)N * 4u * (is_ln ? 2u : 1u);
+            if (dyn + 4096 > (size_t)g_dev[dev].smem_optin) break;
+            const void *k = dir == 0 ? v.fwd : v.bwd;
+            int occ = 0;
+            const int st = ex_occupancy(dev, is_ln, dir, i, k, v.cta, dyn, &occ);
+            if (st != GBNORM_OK) return st;
+            const int64_t rows_per_cta = v.cta / v.tpr;
+            const int64_t units = (M + rows_per_cta - 1) / rows_per_cta;
+            int64_t cap = (int64_t)occ * sms;
+            if (limit > 0 && limit < cap) cap = limit;
+            *pl = ExPlan{k, units < cap ? units : cap, dyn, v.cta};
+            return GBNORM_OK;
+        }
+    }
+    const void *k = dir == 0 ? t.fwd_elem : t.bwd_elem;
+    int occ = 0;
+    const int st = ex_occupancy(dev, is_ln, dir, 16, k, kElemCTA, 0, &occ);
+    if (st != GBNORM_OK) return st;
+    // one partial row per CTA in the backward: at most one CTA per SM
+    int64_t cap = dir == 0 ? (int64_t)occ * sms : (int64_t)sms;
+    if (limit > 0 && limit < cap) cap = limit;
+    *pl = ExPlan{k, M < cap ? M : cap, 0, kElemCTA};
+    return GBNORM_OK;
+}
+
+int launch_ex(const ExPlan &pl, void *params, cudaStream_t s) {
+    void *args[1] = {params};
+    if (cudaLaunchKernel(pl.kernel, dim3((unsigned)pl.grid), dim3(pl.cta), args, pl.dyn, s) != cudaSuccess)
+        return GBNORM_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? GBNORM_OK : GBNORM_ERR_CUDA;
+}
+
+int do_fwd_ex(int is_ln, int64_t M, int64_t N, float eps, const void *x, int64_t ldx, int xdt,
+              const void *res, int64_t ldr, void *h, int64_t ldh, const void *gamma, const void *beta,
+              int pdt, void *y, int64_t ldy, int ydt, float *mean, float *rstd, cudaStream_t stream) {
+    if ((is_ln != 0 && is_ln != 1) || !valid_dtype(xdt) || !valid_dtype(pdt) || !valid_dtype(ydt))
+        return GBNORM_ERR_INVALID_ARG;
+    if (!valid_shape(M, N, xdt) || !std::isfinite(eps) || eps < 0.f) return GBNORM_ERR_INVALID_ARG;
+    if (!is_ln) {
+        beta = nullptr;
+        mean = nullptr;
+    }
+    if (!res && h) return GBNORM_ERR_INVALID_ARG;  // h is the residual sum: only with a residual
+    if (!res) ldr = N;
+    if (!h) ldh = N;
+    if (M > 0) {
+        if (!x || !y) return GBNORM_ERR_INVALID_ARG;
+        for (int64_t ld : {ldx, ldr, ldh, ldy})
+            if (ld < N || ld > (INT64_MAX / 16) / M) return GBNORM_ERR_INVALID_ARG;
+    }
+    const Mat outs[4] = {{y, ldy, ydt, span(M, N, ldy, ydt)}, {h, ldh, xdt, span(M, N, ldh, xdt)},
+                         {rstd, 1, GBNORM_F32, (size_t)M * 4}, {mean, 1, GBNORM_F32, (size_t)M * 4}};
+    const Mat ins[4] = {{x, ldx, xdt, span(M, N, ldx, xdt)}, {res, ldr, xdt, span(M, N, ldr, xdt)},
+                        {gamma, N, pdt, (size_t)N * elem_size(pdt)}, {beta, N, pdt, (size_t)N * elem_size(pdt)}};
+    if (bad_aliasing_ex(outs, 4, ins, 4)) return GBNORM_ERR_INVALID_ARG;
+    int dev;
+    int s = current_device(&dev);
+    if (s != GBNORM_OK) return s;
+    if (M == 0) return GBNORM_OK;
+    const bool vec = vec_rows(x, ldx, xdt) && vec_rows(res, ldr, xdt) && vec_rows(h, ldh, xdt) &&
+                     vec_rows(y, ldy, ydt) && aligned16(gamma) && aligned16(beta);
+    ExPlan pl;
+    s = ex_plan(is_ln, 0, M, N, vec, dev, &pl);
+    if (s != GBNORM_OK) return s;
+    ExFwdParams p{x, res, h, gamma, beta, y, mean, rstd, ldx, ldr, ldh, ldy, M, N, eps, xdt, pdt, ydt};
+    return launch_ex(pl, &p, stream);
+}
+
+size_t ex_ws_bytes(int is_ln, int64_t M, int64_t N, int dev, int *status) {
+    size_t best = 0;
+    for (bool vec : {false, true}) {
+        ExPlan pl;
+        *status = ex_plan(is_ln, 1, M, N, vec, dev, &pl);
+        if (*status != GBNORM_OK) return 0;
+        const size_t need = (size_t)pl.grid * (size_t)N * 4u * (is_ln ? 2u : 1u);
+        if (need > best) best = need;
+    }
+    return (best + 255u) & ~(size_t)255u;
+}
+
+int do_bwd_ex(int is_ln, int64_t M, int64_t N, const void *dy, int64_t lddy, int ydt, const void *x,
+              int64_t ldx, int xdt, const void *dres, int64_t lddres, const void *gamma, int pdt,
+              const float *mean, const float *rstd, void *dx, int64_t lddx, float *dgamma, float *dbeta,
+              void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if ((is_ln != 0 && is_ln != 1) || !valid_dtype(xdt) || !valid_dtype(pdt) || !valid_dtype(ydt))
+        return GBNORM_ERR_INVALID_ARG;
+    if (!valid_shape(M, N, xdt)) return GBNORM_ERR_INVALID_ARG;
+    if (!is_ln) {
+        dbeta = nullptr;
+        mean = nullptr;
+    }
+    if (!dres) lddres = N;
+    if (M > 0) {
+        if (!dy || !x || !rstd || !dx || (is_ln && !mean)) return GBNORM_ERR_INVALID_ARG;
+        for (int64_t ld : {lddy, ldx, lddres, lddx})
+            if (ld < N || ld > (INT64_MAX / 16) / M) return GBNORM_ERR_INVALID_ARG;
+    }
+    const Mat outs[3] = {{dx, lddx, xdt, span(M, N, lddx, xdt)}, {dgamma, N, GBNORM_F32, (size_t)N * 4},
+                         {dbeta, N, GBNORM_F32, (size_t)N * 4}};
+    const Mat ins[6] = {{dy, lddy, ydt, span(M, N, lddy, ydt)}, {x, ldx, xdt, span(M, N, ldx, xdt)},
+                        {dres, lddres, xdt, span(M, N, lddres, xdt)},
+                        {gamma, N, pdt, (size_t)N * elem_size(pdt)},
+                        {rstd, 1, GBNORM_F32, (size_t)M * 4}, {mean, 1, GBNORM_F32, (size_t)M * 4}};
+    if (bad_aliasing_ex(outs, 3, ins, 6)) return GBNORM_ERR_INVALID_ARG;
+    // only dx may coincide with an input, and only with dy or dres
+    if (dx && (dx == x || dx == static_cast<const void *>(rstd) || dx == static_cast<const void *>(mean) ||
+               dx == gamma))
+        return GBNORM_ERR_INVALID_ARG;
+    int dev;
+    int s = current_device(&dev);
+    if (s != GBNORM_OK) return s;
+    const size_t need = ex_ws_bytes(is_ln, M, N, dev, &s);
+    if (s != GBNORM_OK) return s;
+    int64_t P = 0;
+    if (M > 0) {
+        if (!ws || ws_bytes < need || !aligned16(ws)) return GBNORM_ERR_WORKSPACE;
+        const Mat all_out[4] = {outs[0], outs[1], outs[2], {ws, 1, GBNORM_F32, need}};
+        if (bad_aliasing_ex(all_out, 4, ins, 6)) return GBNORM_ERR_INVALID_ARG;
+        const bool vec = vec_rows(dy, lddy, ydt) && vec_rows(x, ldx, xdt) && vec_rows(dres, lddres, xdt) &&
+                         vec_rows(dx, lddx, xdt) && aligned16(gamma);
+        ExPlan pl;
+        s = ex_plan(is_ln, 1, M, N, vec, dev, &pl);
+        if (s != GBNORM_OK) return s;
+        ExBwdParams p{dy, x, dres, gamma, mean, rstd, dx, static_cast<float *>(ws), lddy, ldx, lddres, lddx,
+                      M, N, xdt, pdt, ydt};
+        s = launch_ex(pl, &p, stream);
+        if (s != GBNORM_OK) return s;
+        P = pl.grid;
+    }
+    return launch_colreduce(is_ln, static_cast<const float *>(ws), P, N, dgamma, dbeta, M > 0, stream);
+}
+
+// Stage two of every backward: column sums of the P partial rows of ws
+// (P = 0 writes zeros); a NULL output's blocks return at once.  After a row
+// kernel (pdl) it is launched with programmatic stream serialization.
+int launch_colreduce(int is_ln, const float *wsc, int64_t P, int64_t N, float *dgamma, float *dbeta, bool pdl,
+                     cudaStream_t stream) {
     if (!dgamma && !dbeta) return GBNORM_OK;
     const bool v4 = (N % 4) == 0;
     const int64_t cols_per_cta = 32 * (v4 ? 4 : 1);
     const dim3 grid2((unsigned)((N + cols_per_cta - 1) / cols_per_cta), is_ln ? 2u : 1u);
-    const float *wsc = static_cast<const float *>(ws);
     void *args[5] = {&wsc, &P, &N, &dgamma, &dbeta};
     // Programmatic stream serialization: the column reduce may be scheduled
     // while the row kernel drains; it waits (griddepcontrol.wait) for that
@@ -629,7 +926,7 @@ int do_bwd(int is_ln, const void *dy, const void *x, const void *gamma, const fl
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = M > 0 ? 1 : 0;
+    cfg.numAttrs = pdl ? 1 : 0;
     if (cudaLaunchKernelExC(&cfg, v4 ? kColReduceVec4 : kColReduceScalar, args) != cudaSuccess)
         return GBNORM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GBNORM_OK : GBNORM_ERR_CUDA;
@@ -678,6 +975,33 @@ int layernorm_bwd(const void *dy, const void *x, const void *gamma, const float 
                   gbnorm_stream_t stream) {
     return do_bwd(1, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, workspace, workspace_bytes, M, N,
                   dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int norm_fwd_ex(int is_layernorm, int64_t M, int64_t N, float eps, const void *x, int64_t ldx, int x_dtype,
+                const void *residual, int64_t ldr, void *h, int64_t ldh, const void *gamma, const void *beta,
+                int param_dtype, void *y, int64_t ldy, int y_dtype, float *mean, float *rstd,
+                gbnorm_stream_t stream) {
+    return do_fwd_ex(is_layernorm, M, N, eps, x, ldx, x_dtype, residual, ldr, h, ldh, gamma, beta, param_dtype,
+                     y, ldy, y_dtype, mean, rstd, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t norm_bwd_ex_workspace_size(int is_layernorm, int64_t M, int64_t N) {
+    if ((is_layernorm != 0 && is_layernorm != 1) || !valid_shape(M, N, GBNORM_F32)) return 0;
+    int dev;
+    if (current_device(&dev) != GBNORM_OK) return 0;
+    int st = GBNORM_OK;
+    const size_t b = ex_ws_bytes(is_layernorm, M, N, dev, &st);
+    if (st != GBNORM_OK) return 0;
+    return b > 256 ? b : 256;
+}
+
+int norm_bwd_ex(int is_layernorm, int64_t M, int64_t N, const void *dy, int64_t lddy, int y_dtype,
+                const void *x, int64_t ldx, int x_dtype, const void *dres, int64_t lddres, const void *gamma,
+                int param_dtype, const float *mean, const float *rstd, void *dx, int64_t lddx, float *dgamma,
+                float *dbeta, void *workspace, size_t workspace_bytes, gbnorm_stream_t stream) {
+    return do_bwd_ex(is_layernorm, M, N, dy, lddy, y_dtype, x, ldx, x_dtype, dres, lddres, gamma, param_dtype,
+                     mean, rstd, dx, lddx, dgamma, dbeta, workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *gbnorm_status_string(int status) {

@@ -83,6 +83,24 @@ __device__ __forceinline__ void st_vec(void *base, int64_t idx, const uint4 &v) 
     reinterpret_cast<uint4 *>(base)[idx] = v;
 }
 
+// A 16-byte vector of ones of T (the value of an absent gamma).
+template <typename T> __device__ __forceinline__ uint4 ones_vec();
+template <> __device__ __forceinline__ uint4 ones_vec<float>() {
+    return make_uint4(0x3F800000u, 0x3F800000u, 0x3F800000u, 0x3F800000u);
+}
+template <> __device__ __forceinline__ uint4 ones_vec<__half>() {
+    return make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+}
+template <> __device__ __forceinline__ uint4 ones_vec<__nv_bfloat16>() {
+    return make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+}
+// Vector v of a parameter row; a null row stands for the constant row of
+// ones (gamma, one = true) or zeros (beta).
+template <typename T>
+__device__ __forceinline__ uint4 param_vec(const void *row, int64_t v, bool one) {
+    return row ? ld_vec(row, v) : (one ? ones_vec<T>() : make_uint4(0, 0, 0, 0));
+}
+
 // ---------------------------------------------------------------- cluster PTX
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -238,6 +256,16 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_
             return false;
         }
     }
+}
+
+// Release store / acquire load of a 32-bit word in global memory at GPU scope.
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.

@@ -1,0 +1,446 @@
+// ex_kernels.cuh -- RMSNorm / LayerNorm forward and backward for the general
+// form of the call: rows with their own strides, a storage type per tensor
+// (rows x, parameters gamma / beta, output y), and an optional residual add
+// fused in front of the norm.
+//
+// Same arithmetic as norm_kernels.cuh (the definitions on "SOTA
+// normalization performance with torch.compile", section "How Did
+// Torch.compile Catch Quack?", and "Fused RMSNorm", sections "What it is" /
+// "How it works": fp16/bf16 storage, fp32 accumulation, one rounding per
+// output).  The fusion follows the torch.compile page's paragraphs on
+// Inductor fusing a norm with its neighbouring operations: the residual sum
+// h = x + r is formed in fp32, rounded once to the storage type of x and r,
+// stored if asked for, and normalised -- the values an unfused h = x + r
+// followed by the norm would give, with one read of x and r instead of a
+// write and a re-read of h.  Backward: dx = rstd (g - c1 - xhat c2) + dres,
+// where dres is the gradient reaching h from the residual stream; dx is the
+// gradient of both x and r.
+//
+// Storage types are runtime arguments: every load and store of a row goes
+// through ld8 / st8 (eight elements: one 16-byte vector of 16-bit values, two
+// of fp32), whose branch on the type is uniform over the grid, so one kernel
+// serves every combination of types.  Rows are held in fp32 registers by row
+// groups of TPR threads (thread t owns 8-element chunks k * TPR + t), gamma
+// (and beta) are widened once per CTA into shared memory (plane-major float4,
+// conflict-free), the grid is persistent and the backward keeps its
+// dgamma/dbeta partials in registers, one partial row per CTA, summed by the
+// column-reduce kernel.  fwd_exe / bwd_exe: one CTA per row, element by
+// element, for any N, stride and alignment.
+#pragma once
+
+#include "device_common.cuh"
+#include "params.h"
+
+namespace gbn {
+
+// Storage type codes (gbnorm_dtype_t).
+constexpr int kF32 = 0, kF16 = 1, kBF16 = 2;
+
+// 16-byte load through the coherent path: an output of these kernels may
+// overwrite the row it was computed from (in place), so rows are not read as
+// read-only data.
+__device__ __forceinline__ uint4 ld_row_vec(const void *base, int64_t idx) {
+    return reinterpret_cast<const uint4 *>(base)[idx];
+}
+
+// Eight consecutive elements of a row starting at element `off` (a multiple
+// of 8; the row 16-byte aligned), widened to fp32.
+__device__ __forceinline__ void ld8(const void *row, int64_t off, int dt, float (&f)[8]) {
+    if (dt == kF32) {
+        const uint4 a = ld_row_vec(row, off / 4), b = ld_row_vec(row, off / 4 + 1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[e] = vget<float>(a, e);
+            f[4 + e] = vget<float>(b, e);
+        }
+    } else {
+        const uint4 a = ld_row_vec(row, off / 8);
+        if (dt == kBF16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = vget<__nv_bfloat16>(a, e);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = vget<__half>(a, e);
+        }
+    }
+}
+__device__ __forceinline__ void st8(void *row, int64_t off, int dt, const float (&f)[8]) {
+    if (dt == kF32) {
+        st_vec(row, off / 4, vpack<float>(f));
+        st_vec(row, off / 4 + 1, vpack<float>(f + 4));
+    } else if (dt == kBF16) {
+        st_vec(row, off / 8, vpack<__nv_bfloat16>(f));
+    } else {
+        st_vec(row, off / 8, vpack<__half>(f));
+    }
+}
+// One element, any alignment.
+__device__ __forceinline__ float ld1(const void *row, int64_t j, int dt) {
+    if (dt == kF32) return static_cast<const float *>(row)[j];
+    if (dt == kBF16) return to_f(static_cast<const __nv_bfloat16 *>(row)[j]);
+    return to_f(static_cast<const __half *>(row)[j]);
+}
+__device__ __forceinline__ void st1(void *row, int64_t j, int dt, float v) {
+    if (dt == kF32) static_cast<float *>(row)[j] = v;
+    else if (dt == kBF16) static_cast<__nv_bfloat16 *>(row)[j] = from_f<__nv_bfloat16>(v);
+    else static_cast<__half *>(row)[j] = from_f<__half>(v);
+}
+// v rounded to storage type dt (round to nearest even) and widened back.
+__device__ __forceinline__ float round_to(float v, int dt) {
+    if (dt == kBF16) return __bfloat162float(__float2bfloat16_rn(v));
+    if (dt == kF16) return __half2float(__float2half_rn(v));
+    return v;
+}
+__device__ __forceinline__ int esize(int dt) { return dt == kF32 ? 4 : 2; }
+__device__ __forceinline__ const void *row_ptr(const void *base, int64_t row, int64_t ld, int dt) {
+    return static_cast<const unsigned char *>(base) + row * ld * esize(dt);
+}
+__device__ __forceinline__ void *row_ptr(void *base, int64_t row, int64_t ld, int dt) {
+    return static_cast<unsigned char *>(base) + row * ld * esize(dt);
+}
+
+// gamma (and beta) of the whole row, widened to fp32 into shared memory as
+// two planes of float4 per parameter: chunk c's elements 0-3 at [c], 4-7 at
+// [nc + c].  A null parameter row is the constant 1 (gamma) or 0 (beta).
+template <bool LN, int CTA>
+__device__ __forceinline__ void ex_load_params(float4 *pars, const void *gamma, const void *beta, int pdt,
+                                               int64_t nc) {
+    for (int64_t c = threadIdx.x; c < nc; c += CTA) {
+        float g[8], b[8];
+        if (gamma) {
+            ld8(gamma, 8 * c, pdt, g);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) g[e] = 1.f;
+        }
+        pars[c] = make_float4(g[0], g[1], g[2], g[3]);
+        pars[nc + c] = make_float4(g[4], g[5], g[6], g[7]);
+        if constexpr (LN) {
+            if (beta) {
+                ld8(beta, 8 * c, pdt, b);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) b[e] = 0.f;
+            }
+            pars[2 * nc + c] = make_float4(b[0], b[1], b[2], b[3]);
+            pars[3 * nc + c] = make_float4(b[4], b[5], b[6], b[7]);
+        }
+    }
+}
+__device__ __forceinline__ void ex_par8(const float4 *plane, int64_t nc, int64_t c, float (&f)[8]) {
+    const float4 a = plane[c], b = plane[nc + c];
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w;
+    f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+}
+
+// ============================================================================ forward
+template <bool LN, int TPR, int VPT, int CTA>
+__global__ void __launch_bounds__(CTA) fwd_ex(const ExFwdParams p) {
+    static_assert(CTA % TPR == 0 && TPR % 32 == 0, "row-group shape");
+    constexpr int RPC = CTA / TPR;
+    extern __shared__ __align__(16) float4 pars[];  // gamma planes, then beta planes
+    __shared__ RowReduceSmem<TPR, RPC, 1, 2> red2;
+    __shared__ RowReduceSmem<TPR, RPC, 1, 1> red1;
+    const int64_t nc = p.N / 8;
+    const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
+    const float n = (float)p.N;
+    const bool full = nc == (int64_t)TPR * VPT;  // every thread holds VPT chunks (uniform)
+    ex_load_params<LN, CTA>(pars, p.gamma, p.beta, p.pdt, nc);
+    __syncthreads();
+    int parity = 0;
+    for (int64_t base = (int64_t)blockIdx.x * RPC; base < p.M; base += (int64_t)gridDim.x * RPC) {
+        const int64_t row = base + grp;
+        const bool rok = row < p.M;
+        const int64_t rr = rok ? row : base;
+        float xf[VPT][8];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t c = (int64_t)k * TPR + t;
+            if (rok && c < nc) {
+                ld8(row_ptr(p.x, rr, p.ldx, p.xdt), 8 * c, p.xdt, xf[k]);
+                if (p.res) {
+                    // h = x + r in fp32, rounded once to the storage type
+                    float r8[8];
+                    ld8(row_ptr(p.res, rr, p.ldr, p.xdt), 8 * c, p.xdt, r8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xf[k][e] = round_to(xf[k][e] + r8[e], p.xdt);
+                    if (p.h) st8(row_ptr(p.h, rr, p.ldh, p.xdt), 8 * c, p.xdt, xf[k]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xf[k][e] = 0.f;
+            }
+        }
+        float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sa[e & 3] += LN ? xf[k][e] : xf[k][e] * xf[k][e];
+        const float s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
+        float mean = 0.f, rstd;
+        if (LN && full) {
+            // equal per-thread counts: local mean and M2, one exact combine
+            constexpr float kC = (float)(VPT * 8);
+            float mm[1] = {s * (1.f / kC)}, m2[1];
+            float qa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d = xf[k][e] - mm[0];
+                    qa[e & 3] += d * d;
+                }
+            m2[0] = (qa[0] + qa[1]) + (qa[2] + qa[3]);
+            row_meanvar_equal<TPR, RPC, 1>(mm, m2, kC, red2, parity);
+            mean = mm[0];
+            rstd = rsqrtf(m2[0] / n + p.eps);
+        } else {
+            float a[1] = {s};
+            row_allreduce<TPR, RPC, 1, 1>(a, red1, parity);
+            if constexpr (LN) {
+                // mean first, then the centred sum of squares from the registers
+                mean = a[0] / n;
+                a[0] = 0.f;
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    if ((int64_t)k * TPR + t >= nc) continue;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float d = xf[k][e] - mean;
+                        a[0] += d * d;
+                    }
+                }
+                row_allreduce<TPR, RPC, 1, 1>(a, red1, parity);
+            }
+            rstd = rsqrtf(a[0] / n + p.eps);
+        }
+        if (!rok) continue;  // uniform per row group; no collective below
+        if (t == 0) {
+            if (p.rstd) p.rstd[row] = rstd;
+            if (LN && p.mean) p.mean[row] = mean;
+        }
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t c = (int64_t)k * TPR + t;
+            if (c >= nc) continue;
+            float g[8], o[8];
+            ex_par8(pars, nc, c, g);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = ((xf[k][e] - mean) * rstd) * g[e];
+            if constexpr (LN) {
+                float b[8];
+                ex_par8(pars + 2 * nc, nc, c, b);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] += b[e];
+            }
+            st8(row_ptr(p.y, row, p.ldy, p.ydt), 8 * c, p.ydt, o);
+        }
+    }
+}
+
+// ============================================================================ backward
+template <bool LN, int TPR, int VPT, int CTA>
+__global__ void __launch_bounds__(CTA) bwd_ex(const ExBwdParams p) {
+    static_assert(CTA % TPR == 0 && TPR % 32 == 0, "row-group shape");
+    pdl_launch_dependents();  // the column reduce waits for this grid's completion
+    constexpr int RPC = CTA / TPR;
+    constexpr int NS = LN ? 2 : 1;
+    extern __shared__ __align__(16) float4 pars[];  // gamma planes; later the row groups' partials
+    __shared__ RowReduceSmem<TPR, RPC, 1, NS> red;
+    const int64_t nc = p.N / 8;
+    const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
+    const float n = (float)p.N;
+    ex_load_params<false, CTA>(pars, p.gamma, nullptr, p.pdt, nc);
+    __syncthreads();
+    float accg[VPT][8], accb[LN ? VPT : 1][8];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            accg[k][e] = 0.f;
+            if constexpr (LN) accb[k][e] = 0.f;
+        }
+    int parity = 0;
+    for (int64_t base = (int64_t)blockIdx.x * RPC; base < p.M; base += (int64_t)gridDim.x * RPC) {
+        const int64_t row = base + grp;
+        const bool rok = row < p.M;
+        const int64_t rr = rok ? row : base;
+        const float rstd = rok ? __ldg(p.rstd + row) : 0.f;
+        const float mean = (LN && rok) ? __ldg(p.mean + row) : 0.f;
+        // x - mean and dy of this thread's chunks (zeros outside the row)
+        float xc[VPT][8], dyv[VPT][8];
+        float sum[NS];
+#pragma unroll
+        for (int i = 0; i < NS; ++i) sum[i] = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t c = (int64_t)k * TPR + t;
+            if (rok && c < nc) {
+                ld8(row_ptr(p.x, rr, p.ldx, p.xdt), 8 * c, p.xdt, xc[k]);
+                ld8(row_ptr(p.dy, rr, p.lddy, p.ydt), 8 * c, p.ydt, dyv[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xc[k][e] = dyv[k][e] = 0.f;
+            }
+            float g8[8];
+            ex_par8(pars, nc, c < nc ? c : 0, g8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                xc[k][e] -= mean;
+                const float gg = dyv[k][e] * g8[e];
+                sum[0] += gg * xc[k][e];
+                if constexpr (LN) sum[NS - 1] += gg;
+            }
+        }
+        // masked slots hold dy = 0 and contribute nothing
+        row_allreduce<TPR, RPC, 1, NS>(sum, red, parity);
+        if (!rok) continue;  // uniform per row group; no collective below
+        // dx = rstd g - rstd c1 - (rstd c2) xhat (+ dres), c2 = rstd sum g (x - mean) / n
+        const float c2 = rstd * sum[0] / n;
+        const float rc1 = LN ? rstd * (sum[NS - 1] / n) : 0.f;
+        const float rc2 = rstd * c2;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t c = (int64_t)k * TPR + t;
+            if (c >= nc) continue;
+            float g8[8], o[8];
+            ex_par8(pars, nc, c, g8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float xh = xc[k][e] * rstd;
+                o[e] = fmaf(-rc2, xh, fmaf(rstd, dyv[k][e] * g8[e], -rc1));
+                accg[k][e] += dyv[k][e] * xh;
+                if constexpr (LN) accb[k][e] += dyv[k][e];
+            }
+            if (p.dres) {
+                float r8[8];
+                ld8(row_ptr(p.dres, row, p.lddres, p.xdt), 8 * c, p.xdt, r8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] += r8[e];
+            }
+            st8(row_ptr(p.dx, row, p.lddx, p.xdt), 8 * c, p.xdt, o);
+        }
+    }
+    // Epilogue: one partial row per CTA; the row groups (same columns) are
+    // added in group order through shared memory (the parameters are no
+    // longer needed).
+    float *wsg = p.ws + (int64_t)blockIdx.x * p.N;
+    float *wsb = p.ws + ((int64_t)gridDim.x + blockIdx.x) * p.N;
+    float *comb = reinterpret_cast<float *>(pars);  // [NS][N]
+    __syncthreads();
+    for (int gi = 0; gi < RPC; ++gi) {
+        if (grp == gi) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int64_t c = (int64_t)k * TPR + t;
+                if (c >= nc) continue;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int64_t j = 8 * c + e;
+                    comb[j] = gi == 0 ? accg[k][e] : comb[j] + accg[k][e];
+                    if constexpr (LN) comb[p.N + j] = gi == 0 ? accb[k][e] : comb[p.N + j] + accb[k][e];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    for (int64_t j = threadIdx.x; j < p.N; j += CTA) {
+        wsg[j] = comb[j];
+        if constexpr (LN) wsb[j] = comb[p.N + j];
+    }
+}
+
+// ============================================================================ element-wise (any N, stride, alignment)
+template <bool LN>
+__global__ void __launch_bounds__(kElemCTA) fwd_exe(const ExFwdParams p) {
+    __shared__ float red[2 * 1 * (kElemCTA / 32)];
+    const float n = (float)p.N;
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+        const void *xr = row_ptr(p.x, row, p.ldx, p.xdt);
+        const void *rr = p.res ? row_ptr(p.res, row, p.ldr, p.xdt) : nullptr;
+        void *hr = p.h ? row_ptr(p.h, row, p.ldh, p.xdt) : nullptr;
+        // the (rounded) residual sum of an element; once stored (pass 1) it is
+        // read back, which stays right when h overwrites x or r in place
+        // (each thread reads back only the elements it wrote)
+        auto hsum = [&](int64_t j) {
+            const float v = ld1(xr, j, p.xdt);
+            return rr ? round_to(v + ld1(rr, j, p.xdt), p.xdt) : v;
+        };
+        auto hval = [&](int64_t j) { return hr ? ld1(hr, j, p.xdt) : hsum(j); };
+        float s[1] = {0.f};
+        for (int64_t j = threadIdx.x; j < p.N; j += kElemCTA) {
+            const float f = hsum(j);
+            if (hr) st1(hr, j, p.xdt, f);
+            s[0] += LN ? f : f * f;
+        }
+        cta_allreduce<kElemCTA, 1>(s, red, parity);
+        float mean = 0.f;
+        if constexpr (LN) {
+            mean = s[0] / n;
+            s[0] = 0.f;
+            for (int64_t j = threadIdx.x; j < p.N; j += kElemCTA) {
+                const float d = hval(j) - mean;
+                s[0] += d * d;
+            }
+            cta_allreduce<kElemCTA, 1>(s, red, parity);
+        }
+        const float rstd = rsqrtf(s[0] / n + p.eps);
+        if (threadIdx.x == 0) {
+            if (p.rstd) p.rstd[row] = rstd;
+            if (LN && p.mean) p.mean[row] = mean;
+        }
+        void *yr = row_ptr(p.y, row, p.ldy, p.ydt);
+        for (int64_t j = threadIdx.x; j < p.N; j += kElemCTA) {
+            float o = ((hval(j) - mean) * rstd) * (p.gamma ? ld1(p.gamma, j, p.pdt) : 1.f);
+            if (LN && p.beta) o += ld1(p.beta, j, p.pdt);
+            st1(yr, j, p.ydt, o);
+        }
+    }
+}
+
+// Each CTA accumulates its partial dgamma/dbeta row in its own workspace row.
+template <bool LN>
+__global__ void __launch_bounds__(kElemCTA) bwd_exe(const ExBwdParams p) {
+    pdl_launch_dependents();
+    __shared__ float red[2 * 2 * (kElemCTA / 32)];
+    const float n = (float)p.N;
+    const int64_t P = gridDim.x;
+    float *wsg = p.ws + (int64_t)blockIdx.x * p.N;
+    float *wsb = p.ws + (P + blockIdx.x) * p.N;
+    for (int64_t j = threadIdx.x; j < p.N; j += kElemCTA) {
+        wsg[j] = 0.f;
+        if constexpr (LN) wsb[j] = 0.f;
+    }
+    auto gam = [&](int64_t j) { return p.gamma ? ld1(p.gamma, j, p.pdt) : 1.f; };
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+        const void *xr = row_ptr(p.x, row, p.ldx, p.xdt);
+        const void *dyr = row_ptr(p.dy, row, p.lddy, p.ydt);
+        const float rstd = __ldg(p.rstd + row);
+        const float mean = LN ? __ldg(p.mean + row) : 0.f;
+        float s[2] = {0.f, 0.f};
+        for (int64_t j = threadIdx.x; j < p.N; j += kElemCTA) {
+            const float xh = (ld1(xr, j, p.xdt) - mean) * rstd;
+            const float g = ld1(dyr, j, p.ydt) * gam(j);
+            s[0] += g * xh;
+            s[1] += g;
+        }
+        cta_allreduce<kElemCTA, 2>(s, red, parity);
+        const float c2 = s[0] / n;
+        const float c1 = LN ? s[1] / n : 0.f;
+        void *dxr = row_ptr(p.dx, row, p.lddx, p.xdt);
+        const void *drr = p.dres ? row_ptr(p.dres, row, p.lddres, p.xdt) : nullptr;
+        for (int64_t j = threadIdx.x; j < p.N; j += kElemCTA) {
+            const float xh = (ld1(xr, j, p.xdt) - mean) * rstd;
+            const float dyv = ld1(dyr, j, p.ydt);
+            float o = rstd * (dyv * gam(j) - c1 - xh * c2);
+            if (drr) o += ld1(drr, j, p.xdt);
+            st1(dxr, j, p.xdt, o);
+            wsg[j] += dyv * xh;
+            if constexpr (LN) wsb[j] += dyv;
+        }
+    }
+}
+
+}  // namespace gbn

@@ -5,6 +5,7 @@
 #include "tma_kernels.cuh"
 #include "tma_cluster_kernels.cuh"
 #include "wide_kernels.cuh"
+#include "wtma_kernels.cuh"
 #include "variants.inc"
 
 namespace gbn {
@@ -43,7 +44,13 @@ namespace gbn {
             VPT, 0, 1, NT, VecTraits<GBN_T>::E, 1, 32768},
 #define GBN_FP_RMS(TPR, VPT, NT) GBN_FTMP(false, TPR, VPT, NT)
 #define GBN_FP_LN(TPR, VPT, NT) GBN_FTMP(true, TPR, VPT, NT)
+#define GBN_WTMA(LN, CW, U)                                                                    \
+    Variant{GBN_WTMA_VNAME(CW, U), (const void *)&fwd_wtma<GBN_T, LN, CW, U>, kWtma, (CW) * 32, U, 0, 1, \
+            ((CW) + 1) * 32, VecTraits<GBN_T>::E, 1, 0},
+#define GBN_WT_RMS(CW, U) GBN_WTMA(false, CW, U)
+#define GBN_WT_LN(CW, U) GBN_WTMA(true, CW, U)
 static const Variant rms_variants[] = {
+    GBN_WTMA_FWD_GEOMS(GBN_WT_RMS)
     GBN_TMP_FWD_GEOMS(GBN_FP_RMS)
     GBN_TMA_FWD_GEOMS(GBN_T_RMS)
     GBN_TMAC_FWD_GEOMS(GBN_C_RMS)
@@ -52,6 +59,7 @@ static const Variant rms_variants[] = {
     GBN_FWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
+    GBN_WTMA_FWD_GEOMS(GBN_WT_LN)
     GBN_TMP_FWD_GEOMS(GBN_FP_LN)
     GBN_TMA_FWD_GEOMS(GBN_T_LN)
     GBN_TMAC_FWD_GEOMS(GBN_C_LN)
@@ -79,6 +87,9 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_FTMP
 #undef GBN_FP_RMS
 #undef GBN_FP_LN
+#undef GBN_WTMA
+#undef GBN_WT_RMS
+#undef GBN_WT_LN
 #endif
 
 #ifdef GBN_BWD
@@ -108,9 +119,22 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
             VPT, 0, 1, NT, VecTraits<GBN_T>::E, 1, 32768},
 #define GBN_P_RMS(TPR, VPT, NT) GBN_TMP(false, TPR, VPT, NT)
 #define GBN_P_LN(TPR, VPT, NT) GBN_TMP(true, TPR, VPT, NT)
+// single-kernel variants: the same kernels summing their partial rows themselves
+#define GBN_SKTMA(LN, TPR, VPT, CW)                                                            \
+    Variant{"sk" GBN_TMA_VNAME(TPR, VPT, CW), (const void *)&bwd_tma<GBN_T, LN, TPR, VPT, CW, true>, kTma, \
+            TPR, VPT, 0, 1, (CW + 1) * 32, VecTraits<GBN_T>::E, 1, 32768, 1},
+#define GBN_SKT_RMS(TPR, VPT, CW) GBN_SKTMA(false, TPR, VPT, CW)
+#define GBN_SKT_LN(TPR, VPT, CW) GBN_SKTMA(true, TPR, VPT, CW)
+#define GBN_SKTMP(LN, TPR, VPT, NT)                                                            \
+    Variant{"sk" GBN_TMP_VNAME(TPR, VPT, NT), (const void *)&bwd_tmp<GBN_T, LN, TPR, VPT, NT, true>, kTmaP, \
+            TPR, VPT, 0, 1, NT, VecTraits<GBN_T>::E, 1, 32768, 1},
+#define GBN_SKP_RMS(TPR, VPT, NT) GBN_SKTMP(false, TPR, VPT, NT)
+#define GBN_SKP_LN(TPR, VPT, NT) GBN_SKTMP(true, TPR, VPT, NT)
 static const Variant rms_variants[] = {
     GBN_TMA_BWD_GEOMS(GBN_T_RMS)
     GBN_TMP_BWD_GEOMS(GBN_P_RMS)
+    GBN_SK_TMA_BWD_GEOMS(GBN_SKT_RMS)
+    GBN_SK_TMP_BWD_GEOMS(GBN_SKP_RMS)
     GBN_TMAC_BWD_GEOMS(GBN_C_RMS)
     GBN_WIDE_BWD_GEOMS(GBN_W_RMS)
     GBN_BWD_GEOMS(GBN_X_RMS)
@@ -118,6 +142,8 @@ static const Variant rms_variants[] = {
 static const Variant ln_variants[] = {
     GBN_TMA_BWD_GEOMS(GBN_T_LN)
     GBN_TMP_BWD_GEOMS(GBN_P_LN)
+    GBN_SK_TMA_BWD_GEOMS(GBN_SKT_LN)
+    GBN_SK_TMP_BWD_GEOMS(GBN_SKP_LN)
     GBN_TMAC_BWD_GEOMS(GBN_C_LN)
     GBN_WIDE_BWD_GEOMS(GBN_W_LN)
     GBN_BWD_GEOMS(GBN_X_LN)
@@ -130,6 +156,12 @@ const VariantTable GBN_CAT(kBwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_TMP
 #undef GBN_P_RMS
 #undef GBN_P_LN
+#undef GBN_SKTMA
+#undef GBN_SKT_RMS
+#undef GBN_SKT_LN
+#undef GBN_SKTMP
+#undef GBN_SKP_RMS
+#undef GBN_SKP_LN
 #endif
 
 }  // namespace gbn

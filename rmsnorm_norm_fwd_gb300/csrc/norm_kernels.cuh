@@ -59,8 +59,8 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
     for (int k = 0; k < VPT; ++k) {
         vid[k] = ((int64_t)k * CL + rank) * TPR + t;
         vok[k] = vid[k] < nv;
-        gv[k] = vok[k] ? ld_vec(p.gamma, vid[k]) : make_uint4(0, 0, 0, 0);
-        if constexpr (LN) bv[k] = vok[k] ? ld_vec(p.beta, vid[k]) : make_uint4(0, 0, 0, 0);
+        gv[k] = vok[k] ? param_vec<T>(p.gamma, vid[k], true) : make_uint4(0, 0, 0, 0);
+        if constexpr (LN) bv[k] = vok[k] ? param_vec<T>(p.beta, vid[k], false) : make_uint4(0, 0, 0, 0);
     }
 
     int parity = 0;
@@ -199,9 +199,9 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
     const bool full = nv == (int64_t)TPR * VPT;  // uniform over the grid
 
     for (int64_t v = threadIdx.x; v < nv; v += CTA) {
-        const uint4 g = ld_vec(p.gamma, v);
+        const uint4 g = param_vec<T>(p.gamma, v, true);
         uint4 b = make_uint4(0, 0, 0, 0);
-        if constexpr (LN) b = ld_vec(p.beta, v);
+        if constexpr (LN) b = param_vec<T>(p.beta, v, false);
 #pragma unroll
         for (int h = 0; h < H; ++h) {
             pars[h * nv + v] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(CTA) bwd_rows(const BwdParams p) {
     for (int k = 0; k < VPT; ++k) {
         vid[k] = ((int64_t)k * CL + rank) * TPR + t;
         vok[k] = vid[k] < nv;
-        gv[k] = vok[k] ? ld_vec(p.gamma, vid[k]) : make_uint4(0, 0, 0, 0);
+        gv[k] = vok[k] ? param_vec<T>(p.gamma, vid[k], true) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
             accg[k][e] = 0.f;
@@ -489,8 +489,8 @@ __global__ void __launch_bounds__(kElemCTA) fwd_elem(const FwdParams p) {
         }
         T *yr = y + row * p.N;
         for (int64_t j = threadIdx.x; j < p.N; j += kElemCTA) {
-            float o = ((to_f(xr[j]) - mean) * rstd) * to_f(gamma[j]);
-            if constexpr (LN) o += to_f(beta[j]);
+            float o = ((to_f(xr[j]) - mean) * rstd) * (gamma ? to_f(gamma[j]) : 1.f);
+            if (LN && beta) o += to_f(beta[j]);
             yr[j] = from_f<T>(o);
         }
     }
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(kElemCTA) bwd_elem(const BwdParams p) {
         float s[2] = {0.f, 0.f};
         for (int64_t j = threadIdx.x; j < p.N; j += kElemCTA) {
             const float xh = (to_f(xr[j]) - mean) * rstd;
-            const float g = to_f(dyr[j]) * to_f(gamma[j]);
+            const float g = to_f(dyr[j]) * (gamma ? to_f(gamma[j]) : 1.f);
             s[0] += g * xh;
             s[1] += g;
         }
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kElemCTA) bwd_elem(const BwdParams p) {
         for (int64_t j = threadIdx.x; j < p.N; j += kElemCTA) {
             const float xh = (to_f(xr[j]) - mean) * rstd;
             const float dyv = to_f(dyr[j]);
-            const float g = dyv * to_f(gamma[j]);
+            const float g = dyv * (gamma ? to_f(gamma[j]) : 1.f);
             dxr[j] = from_f<T>(rstd * (g - c1 - xh * c2));
             wsg[j] += dyv * xh;
             if constexpr (LN) wsb[j] += dyv;

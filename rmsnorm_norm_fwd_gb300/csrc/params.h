@@ -11,6 +11,7 @@ constexpr int kElemCTA = 256;  // threads per CTA of the element-wise kernels
 constexpr int kColCTA = 512;   // threads per CTA of the column-reduce kernel
 constexpr int kTmaHeaderBytes = 2048;  // TMA kernels: barriers, abort flag, reduction scratch
 constexpr int kTmaMaxStages = 8;       // TMA kernels: deepest shared-memory ring
+constexpr int kSkPartBytes = 16 * 128 * 4;  // single-kernel column reduce: band sums in shared memory
 
 // Pipeline geometry of the TMA-staged kernels, chosen by the host per call.
 struct TileCfg {
@@ -39,9 +40,44 @@ struct BwdParams {
     const float *mean;  // [M] (LayerNorm only)
     const float *rstd;  // [M]
     void *dx;           // [M, N] T
-    float *ws;          // [2][P][N] float partial rows (second block: dbeta)
+    float *ws;          // [2][P][N] float partial rows (second block: dbeta), then P flag words
     int64_t M, N;
     TileCfg tc;         // used by the TMA-staged kernels only
+    // Single-kernel variants only (they reduce the partial rows themselves):
+    float *dgamma;      // [N] or null
+    float *dbeta;       // [N] or null
+    uint32_t epoch;     // nonzero, different for every call of the process
+};
+
+// General form (strided rows, a storage type per tensor, fused residual
+// add).  Strides (ld*) are in elements; dtypes are gbnorm_dtype_t codes.
+struct ExFwdParams {
+    const void *x;      // [M, ldx] xdt
+    const void *res;    // [M, ldr] xdt, or null (no residual add)
+    void *h;            // [M, ldh] xdt: x + res as normalised, or null (not stored)
+    const void *gamma;  // [N] pdt, or null (1)
+    const void *beta;   // [N] pdt, or null (0; LayerNorm only)
+    void *y;            // [M, ldy] ydt
+    float *mean;        // [M] or null (LayerNorm only)
+    float *rstd;        // [M] or null
+    int64_t ldx, ldr, ldh, ldy;
+    int64_t M, N;
+    float eps;
+    int xdt, pdt, ydt;
+};
+
+struct ExBwdParams {
+    const void *dy;     // [M, lddy] ydt
+    const void *x;      // [M, ldx] xdt: the normalised rows (h with a residual add)
+    const void *dres;   // [M, lddres] xdt: gradient reaching x from elsewhere, or null
+    const void *gamma;  // [N] pdt, or null (1)
+    const float *mean;  // [M] (LayerNorm only)
+    const float *rstd;  // [M]
+    void *dx;           // [M, lddx] xdt
+    float *ws;          // [2][P][N] float partial rows (second block: dbeta)
+    int64_t lddy, ldx, lddres, lddx;
+    int64_t M, N;
+    int xdt, pdt, ydt;
 };
 
 enum VariantKind : int {
@@ -52,6 +88,7 @@ enum VariantKind : int {
     kWide = 4,  // one CTA per row, the row streamed twice (DRAM, then L2); any row length
     kRowsS = 5, // as kRows (no cluster), gamma/beta in shared memory as fp32
     kTmaP = 6,  // as kTma without a producer warp (one thread of the CTA refills the ring)
+    kWtma = 7,  // one CTA per row, the row streamed twice through a bulk-copy ring (forward)
 };
 
 // One compiled kernel and the geometry the host needs to launch it.
@@ -67,13 +104,15 @@ struct Variant {
     int elems_per_vec;   // E (16 bytes / sizeof(T)); 1 for element-wise kernels
     int ctas_per_sm;     // kTma: CTAs meant to share an SM (shared-memory budget split); kWide: launch bound
     int stage_target;    // kTma: bytes of one stage the host aims for
+    int fused = 0;       // 1: the kernel also sums the partial rows (cooperative launch, no column reduce)
 
     // Longest row (elements) this variant can hold.
     int64_t max_n() const {
-        return (kind == kElem || kind == kWide) ? INT64_MAX : (int64_t)tpr * vpt * cl * elems_per_vec;
+        return (kind == kElem || kind == kWide || kind == kWtma) ? INT64_MAX
+                                                                 : (int64_t)tpr * vpt * cl * elems_per_vec;
     }
     // Threads of a CTA that work on rows (TMA kinds add one producer warp).
-    int consumers() const { return (kind == kTma || kind == kTmaCl) ? cta - 32 : cta; }
+    int consumers() const { return (kind == kTma || kind == kTmaCl || kind == kWtma) ? cta - 32 : cta; }
     bool staged_rows() const { return kind == kTma || kind == kTmaP; }
     int rows_per_cta_iter() const {
         return (kind == kRows || kind == kRowsS) ? (cta / tpr) * rows : (kind == kWide && cl == 1) ? rows : 1;
@@ -91,5 +130,19 @@ extern const VariantTable kFwdRms_f16, kFwdLn_f16, kBwdRms_f16, kBwdLn_f16;
 extern const VariantTable kFwdRms_bf16, kFwdLn_bf16, kBwdRms_bf16, kBwdLn_bf16;
 extern const void *const kColReduceVec4;
 extern const void *const kColReduceScalar;
+
+// General-form kernels (ex_kernels.cuh): row-resident geometries by row
+// capacity, and the element-wise kernels; [is_ln].
+struct ExVariant {
+    const char *name;
+    const void *fwd, *bwd;
+    int tpr, vpt, cta;  // capacity tpr * vpt * 8 elements
+};
+struct ExTable {
+    const ExVariant *v;
+    int count;
+    const void *fwd_elem, *bwd_elem;
+};
+extern const ExTable kExTables[2];
 
 }  // namespace gbn

@@ -173,8 +173,9 @@ __global__ void __launch_bounds__((kTmacCW + 1) * 32, 1) fwd_tmac(const FwdParam
 
     if (warp == kTmacCW) {
         if (lane == 0) {
-            load_params(&h.pbar, gs, bs, static_cast<const uint4 *>(p.gamma) + v0,
-                        LN ? static_cast<const uint4 *>(p.beta) + v0 : nullptr, (uint32_t)cnt * 16u);
+            load_params(&h.pbar, gs, bs, p.gamma ? static_cast<const uint4 *>(p.gamma) + v0 : nullptr,
+                        (LN && p.beta) ? static_cast<const uint4 *>(p.beta) + v0 : nullptr,
+                        (uint32_t)cnt * 16u);
             tmac_produce<false, LN>(h, stages, p.tc, M, row_bytes, v0, cnt, slice_al, p.x, nullptr,
                                     nullptr, nullptr);
         }
@@ -300,9 +301,10 @@ __global__ void __launch_bounds__((kTmacCW + 1) * 32, 1) fwd_tmac(const FwdParam
             for (int q = 0; q < VPT; ++q) {
                 const int lv = q * NT + t;
                 if (lv >= cnt) continue;
-                const uint4 x = lds128(xs + lv), g = lds128(gs + lv);
+                const uint4 x = lds128(xs + lv);
+                const uint4 g = p.gamma ? lds128(gs + lv) : ones_vec<T>();
                 uint4 bb;
-                if constexpr (LN) bb = lds128(bs + lv);
+                if constexpr (LN) bb = p.beta ? lds128(bs + lv) : make_uint4(0, 0, 0, 0);
                 float o[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
@@ -362,8 +364,8 @@ __global__ void __launch_bounds__((kTmacCW + 1) * 32, 1) bwd_tmac(const BwdParam
 
     if (warp == kTmacCW) {
         if (lane == 0) {
-            load_params(&h.pbar, gs, nullptr, static_cast<const uint4 *>(p.gamma) + v0, nullptr,
-                        (uint32_t)cnt * 16u);
+            load_params(&h.pbar, gs, nullptr, p.gamma ? static_cast<const uint4 *>(p.gamma) + v0 : nullptr,
+                        nullptr, (uint32_t)cnt * 16u);
             tmac_produce<true, LN>(h, stages, p.tc, M, row_bytes, v0, cnt, slice_al, p.x, p.dy, p.rstd,
                                    p.mean);
         }
@@ -418,7 +420,8 @@ __global__ void __launch_bounds__((kTmacCW + 1) * 32, 1) bwd_tmac(const BwdParam
             for (int q = 0; q < VPT; ++q) {
                 const int lv = q * NT + t;
                 if (lv >= cnt) continue;
-                const uint4 x = lds128(xs + lv), d = lds128(ds + lv), g = lds128(gs + lv);
+                const uint4 x = lds128(xs + lv), d = lds128(ds + lv);
+                const uint4 g = p.gamma ? lds128(gs + lv) : ones_vec<T>();
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const float xh = (vget<T>(x, e) - mean) * rstd;
@@ -462,7 +465,8 @@ __global__ void __launch_bounds__((kTmacCW + 1) * 32, 1) bwd_tmac(const BwdParam
             for (int q = 0; q < VPT; ++q) {
                 const int lv = q * NT + t;
                 if (lv >= cnt) continue;
-                const uint4 x = lds128(xs + lv), d = lds128(ds + lv), g = lds128(gs + lv);
+                const uint4 x = lds128(xs + lv), d = lds128(ds + lv);
+                const uint4 g = p.gamma ? lds128(gs + lv) : ones_vec<T>();
                 float o[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e) {

@@ -111,11 +111,12 @@ __device__ __forceinline__ void tma_produce(TmaHeader &h, unsigned char *stages,
 
 // gamma (and beta) for the whole row are brought into shared memory once per
 // CTA by the producer's bulk copies, completing h.pbar: every row reads them
-// again, and registers are kept for the backward's dgamma/dbeta partials.
+// again, and registers are kept for the backward's dgamma/dbeta partials.  A
+// null row is not copied (the consumers use the constant it stands for).
 __device__ __forceinline__ void load_params(uint64_t *pbar, void *gdst, void *bdst, const void *g,
                                             const void *b, uint32_t bytes) {
-    mbar_arrive_expect_tx(pbar, bytes * (b ? 2u : 1u));
-    bulk_g2s(gdst, g, bytes, pbar);
+    mbar_arrive_expect_tx(pbar, bytes * ((g ? 1u : 0u) + (b ? 1u : 0u)));
+    if (g) bulk_g2s(gdst, g, bytes, pbar);
     if (b) bulk_g2s(bdst, b, bytes, pbar);
 }
 
@@ -248,9 +249,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * TPR + t;
                 if (v >= nv) continue;
-                const uint4 q = lds128(xs + v), g = lds128(gs + v);
+                const uint4 q = lds128(xs + v);
+                const uint4 g = p.gamma ? lds128(gs + v) : ones_vec<T>();
                 uint4 b;
-                if constexpr (LN) b = lds128(bs + v);
+                if constexpr (LN) b = p.beta ? lds128(bs + v) : make_uint4(0, 0, 0, 0);
                 float o[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
@@ -265,8 +267,112 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_tma(const FwdParams p) {
     }
 }
 
+// ============================================================================ single-kernel column reduce
+// The second stage of the dgamma/dbeta reduction run by the backward kernel
+// itself ("Fused RMSNorm", sections "What didn't work" / "Next": per-block
+// partials, then a vectorised column sum -- here without a second launch).
+// The kernel is launched cooperatively, so all P CTAs are resident.  After
+// writing its partial row, each CTA publishes the call's epoch in its flag
+// word (release, after a fence by every thread); one warp per CTA waits,
+// bounded, until all P flags carry the epoch (acquire), then the CTA sums its
+// share of the columns over the P partial rows: column groups of 32 lanes x VW
+// (4 floats, or 1 when N % 4 != 0), group c taken by CTA c mod P, the rows
+// split into 16 bands summed in row order and the band sums added in band
+// order -- the order of colreduce, so the result is bit-identical to the
+// two-kernel path with the same P.  The flags sit after the partial rows in
+// the workspace (after NB = 1 or 2 blocks of them); stale flags from earlier
+// calls carry other epochs.  `part` is 16 x 128 floats of idle shared
+// memory; NT threads (bar_id) take part.
+template <int NT, int NB>
+__device__ __forceinline__ void sk_column_reduce(const BwdParams &p, float *part, volatile int *abort,
+                                                 int bar_id) {
+    constexpr int W = NT / 32;
+    constexpr int kBands = kColCTA / 32;
+    const int64_t P = gridDim.x, N = p.N;
+    if (!p.dgamma && !p.dbeta) return;  // uniform: nothing to sum
+    uint32_t *flags = reinterpret_cast<uint32_t *>(p.ws + NB * P * N);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __threadfence();
+    named_sync(bar_id, NT);
+    if (threadIdx.x == 0) st_release_gpu(flags + blockIdx.x, p.epoch);
+    if (warp == 0) {
+        const long long t0 = clock64();
+        while (true) {
+            bool mine = true;
+            for (int64_t q = lane; q < P; q += 32) mine = mine && ld_acquire_gpu(flags + q) == p.epoch;
+            if (__all_sync(0xffffffffu, mine)) break;
+            if (*abort || clock64() - t0 > kWaitLimitCycles) {
+                if (lane == 0) {
+                    *abort = 1;
+                    if (p.tc.fault) atomicExch(p.tc.fault, 1);
+                }
+                break;
+            }
+        }
+    }
+    named_sync(bar_id, NT);
+    if (*abort) return;
+    __threadfence();
+    const int VW = (N & 3) == 0 ? 4 : 1;
+    const int64_t ngroups = (N + 32 * VW - 1) / (32 * VW);
+    for (int64_t cg = blockIdx.x; cg < ngroups; cg += P) {
+        const int64_t col = (cg * 32 + lane) * VW;
+        const bool ok = col < N;
+#pragma unroll 1
+        for (int s = 0; s < NB; ++s) {
+            float *out = s ? p.dbeta : p.dgamma;
+            if (!out) continue;  // uniform
+            const float *src = p.ws + (int64_t)s * P * N;
+            for (int band = warp; band < kBands; band += W) {
+                const int64_t p0 = P * band / kBands, p1 = P * (band + 1) / kBands;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                if (ok) {
+                    constexpr int kB = 16;
+                    for (int64_t q0 = p0; q0 < p1; q0 += kB) {
+                        if (VW == 4) {
+                            float4 a[kB];
+#pragma unroll
+                            for (int i = 0; i < kB; ++i)
+                                a[i] = q0 + i < p1 ? __ldcg(reinterpret_cast<const float4 *>(src + (q0 + i) * N + col))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int i = 0; i < kB; ++i) {
+                                acc[0] += a[i].x;
+                                acc[1] += a[i].y;
+                                acc[2] += a[i].z;
+                                acc[3] += a[i].w;
+                            }
+                        } else {
+                            float a[kB];
+#pragma unroll
+                            for (int i = 0; i < kB; ++i) a[i] = q0 + i < p1 ? __ldcg(src + (q0 + i) * N + col) : 0.f;
+#pragma unroll
+                            for (int i = 0; i < kB; ++i) acc[0] += a[i];
+                        }
+                    }
+                }
+                for (int v = 0; v < VW; ++v) part[band * 128 + lane * VW + v] = acc[v];
+            }
+            named_sync(bar_id, NT);
+            if (warp == 0 && ok) {
+                float r[4];
+                for (int v = 0; v < VW; ++v) {
+                    r[v] = 0.f;
+                    for (int b = 0; b < kBands; ++b) r[v] += part[b * 128 + lane * VW + v];
+                }
+                if (VW == 4 && (reinterpret_cast<uintptr_t>(out + col) & 15) == 0) {
+                    *reinterpret_cast<float4 *>(out + col) = make_float4(r[0], r[1], r[2], r[3]);
+                } else {
+                    for (int v = 0; v < VW; ++v) out[col + v] = r[v];
+                }
+            }
+            named_sync(bar_id, NT);
+        }
+    }
+}
+
 // ============================================================================ backward
-template <typename T, bool LN, int TPR, int VPT, int CW>
+template <typename T, bool LN, int TPR, int VPT, int CW, bool SK = false>
 __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
     pdl_launch_dependents();  // the column reduce waits for this grid's completion
     constexpr int E = VecTraits<T>::E;
@@ -308,7 +414,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
 
     // gamma, widened to fp32 once per CTA by the consumers.
     for (int64_t v = threadIdx.x; v < nv; v += NT) {
-        const uint4 g = ld_vec(p.gamma, v);
+        const uint4 g = param_vec<T>(p.gamma, v, true);
 #pragma unroll
         for (int hh = 0; hh < H; ++hh)
             gpar[hh * nv + v] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
@@ -498,6 +604,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
             }
         }
     }
+    if constexpr (SK) sk_column_reduce<NT, NS>(p, reinterpret_cast<float *>(stages), &h.abort, kTmaBarAll);
 }
 
 // ============================================================================ forward, no producer warp
@@ -555,9 +662,9 @@ __global__ void __launch_bounds__(NT, 1) fwd_tmp(const FwdParams p) {
     if (t == 0)
         for (int j = 0; j < SG; ++j) issue(j);
     for (int64_t v = threadIdx.x; v < nv; v += NT) {
-        const uint4 g = ld_vec(p.gamma, v);
+        const uint4 g = param_vec<T>(p.gamma, v, true);
         uint4 b = make_uint4(0, 0, 0, 0);
-        if constexpr (LN) b = ld_vec(p.beta, v);
+        if constexpr (LN) b = param_vec<T>(p.beta, v, false);
 #pragma unroll
         for (int hh = 0; hh < H; ++hh) {
             gpar[hh * nv + v] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
@@ -685,7 +792,7 @@ __global__ void __launch_bounds__(NT, 1) fwd_tmp(const FwdParams p) {
 // Without a 17th warp the register budget is 65536 / NT per thread (128 for
 // 512 threads), which holds the dgamma and dbeta partials and, for up to 24
 // elements per thread, the pass-1 values (x - mean, g and dy) for pass 2.
-template <typename T, bool LN, int TPR, int VPT, int NT>
+template <typename T, bool LN, int TPR, int VPT, int NT, bool SK = false>
 __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
     pdl_launch_dependents();  // the column reduce waits for this grid's completion
     constexpr int E = VecTraits<T>::E;
@@ -747,7 +854,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
     if (t == 0)
         for (int j = 0; j < SG; ++j) issue(j);
     for (int64_t v = threadIdx.x; v < nv; v += NT) {
-        const uint4 g = ld_vec(p.gamma, v);
+        const uint4 g = param_vec<T>(p.gamma, v, true);
 #pragma unroll
         for (int hh = 0; hh < H; ++hh)
             gpar[hh * nv + v] = make_float4(vget<T>(g, 4 * hh), vget<T>(g, 4 * hh + 1), vget<T>(g, 4 * hh + 2),
@@ -938,6 +1045,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
             }
         }
     }
+    if constexpr (SK) sk_column_reduce<NT, NS>(p, reinterpret_cast<float *>(stages), &h.abort, kTmaBarAll);
 }
 
 }  // namespace gbn

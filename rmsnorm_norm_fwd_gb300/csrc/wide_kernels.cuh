@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wide(const FwdParams p) {
             for (int u = 0; u < U2; ++u) {
                 const int64_t v = b + (int64_t)u * NT;
                 if (v < nv) {
-                    g[u] = ld_l2hint(gam + v, keep);
-                    if constexpr (LN) bb[u] = ld_l2hint(bet + v, keep);
+                    g[u] = gam ? ld_l2hint(gam + v, keep) : ones_vec<T>();
+                    if constexpr (LN) bb[u] = bet ? ld_l2hint(bet + v, keep) : make_uint4(0, 0, 0, 0);
 #pragma unroll
                     for (int r = 0; r < R; ++r)
                         if (ok[r]) q[r][u] = ld_l2hint(xr[r] + v, drop);
@@ -385,7 +385,7 @@ __device__ __forceinline__ void wide_bwd_sweep(int t, int cnt, int64_t slice, co
         for (int u = 0; u < U; ++u) {
             const int vv = b + u * NT;
             if (vv < cnt) {
-                g[u] = ld_l2hint(gr + vv, keep);
+                g[u] = gr ? ld_l2hint(gr + vv, keep) : ones_vec<T>();
                 if constexpr (P1) {
                     px[u] = ld_l2hint(x1 + vv, keep);
                     pd[u] = ld_l2hint(d1 + vv, keep);
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wide(const BwdParams p) {
     const int cnt = (int)(nv - v0 < slice ? nv - v0 : slice);
     const float n = (float)p.N;
     const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
-    const uint4 *gr = static_cast<const uint4 *>(p.gamma) + v0;
+    const uint4 *gr = p.gamma ? static_cast<const uint4 *>(p.gamma) + v0 : nullptr;  // null: gamma = 1
     const size_t slice_bytes = (size_t)cnt * 16;
 
     for (int64_t i = t; i < (int64_t)NVAL * H * slice; i += NT) accs[i] = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -4,8 +4,10 @@ This module holds no normalisation arithmetic: it only draws random tensors.
 Both sides of every parity check read the same host tensors, so the oracle
 sees exactly the dtype-rounded values the kernels see.
 
-Recipe (one ``torch.Generator`` on the CPU per tensor, seeded from ``seed``
-and the tensor's slot, so adding a tensor never shifts another's draws):
+Recipe (one ``torch.Generator`` per tensor, seeded from ``seed`` and the
+tensor's slot, so adding a tensor never shifts another's draws; on the CPU for
+every parity check, optionally on the GPU for timing runs, where the same
+recipe gives other draws of the same distributions):
   * draw in float32, apply the distribution, then round once to the dtype;
   * ``dist="rms"``:  x ~ N(0, 1)
   * ``dist="ln"``:   x ~ N(0.5, 2^2)
@@ -28,8 +30,8 @@ DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
 _SLOT = {"x": 0, "gamma": 1, "beta": 2, "dy": 3, "rows": 4, "elems": 5, "signs": 6}
 
 
-def _gen(seed: int, slot: str) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, slot: str, device: str = "cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(seed * 16 + _SLOT[slot])
     return g
 
@@ -52,30 +54,38 @@ def default_eps(op: str) -> float:
 
 def make_inputs(M: int, N: int, dtype: str = "bf16", dist: str = "rms", op: str = "rms",
                 seed: int = DEFAULT_SEED, eps: float | None = None,
-                with_dy: bool = True) -> NormInputs:
-    """Draw one seeded problem of shape [M, N] (see the module docstring)."""
+                with_dy: bool = True, device: str = "cpu", param_dtype: str | None = None,
+                dy_dtype: str | None = None) -> NormInputs:
+    """Draw one seeded problem of shape [M, N] (see the module docstring).
+    device: where the draws happen and the tensors live ("cpu" for anything the
+    oracle reads).  gamma / beta are rounded to param_dtype and dy to dy_dtype
+    (default: dtype, the type of x)."""
     t = DTYPES[dtype]
-    x = torch.randn(M, N, generator=_gen(seed, "x"), dtype=torch.float32)
+    tp = DTYPES[param_dtype or dtype]
+    td = DTYPES[dy_dtype or dtype]
+    dev = torch.device(device)
+    gen = (lambda slot: _gen(seed, slot, dev.type if dev.type == "cpu" else str(dev)))
+    x = torch.randn(M, N, generator=gen("x"), dtype=torch.float32, device=dev)
     if dist == "ln":
         x = x * 2.0 + 0.5
     elif dist == "llm":
         n_rows = max(1, (M + 99) // 100) if M > 0 else 0
         if n_rows:
-            rows = torch.randperm(M, generator=_gen(seed, "rows"))[:n_rows]
+            rows = torch.randperm(M, generator=gen("rows"), device=dev)[:n_rows]
             x[rows] *= 100.0
         n_el = (M * N) // 1000
         if n_el:
             flat = x.view(-1)
-            idx = torch.randint(0, M * N, (n_el,), generator=_gen(seed, "elems"))
-            sgn = torch.randint(0, 2, (n_el,), generator=_gen(seed, "signs")).float() * 2.0 - 1.0
+            idx = torch.randint(0, M * N, (n_el,), generator=gen("elems"), device=dev)
+            sgn = torch.randint(0, 2, (n_el,), generator=gen("signs"), device=dev).float() * 2.0 - 1.0
             flat[idx] = 60.0 * sgn
     elif dist != "rms":
         raise ValueError(f"unknown dist {dist!r}")
-    gamma = 1.0 + 0.1 * torch.randn(N, generator=_gen(seed, "gamma"), dtype=torch.float32)
-    beta = 0.1 * torch.randn(N, generator=_gen(seed, "beta"), dtype=torch.float32)
+    gamma = 1.0 + 0.1 * torch.randn(N, generator=gen("gamma"), dtype=torch.float32, device=dev)
+    beta = 0.1 * torch.randn(N, generator=gen("beta"), dtype=torch.float32, device=dev)
     if with_dy:
-        dy = torch.randn(M, N, generator=_gen(seed, "dy"), dtype=torch.float32).to(t)
+        dy = torch.randn(M, N, generator=gen("dy"), dtype=torch.float32, device=dev).to(td)
     else:
-        dy = torch.empty(0, dtype=t)
-    return NormInputs(x=x.to(t), gamma=gamma.to(t), beta=beta.to(t), dy=dy,
+        dy = torch.empty(0, dtype=td, device=dev)
+    return NormInputs(x=x.to(t), gamma=gamma.to(tp), beta=beta.to(tp), dy=dy,
                       eps=default_eps(op) if eps is None else float(eps), dtype=dtype, dist=dist)

@@ -6,7 +6,10 @@ measured rows of csrc/dispatch_table.inc.
 
 Each (op, direction, dtype, N, M) is timed for every variant that can serve
 it (forced through gbnorm_force_variant), with L2 flushed before every timed
-call (1 GiB write, then 512 MiB read), CUDA events on the launching stream, median of --reps calls.  Effective
+call (1 GiB write, then 512 MiB read), CUDA events on the launching stream,
+median of --reps calls.  The table is keyed on the row count too: shapes with
+M <= SMALL_M are measured separately and written as rows that apply only to
+calls with at most SMALL_M rows, ahead of the rows for any M.  Effective
 bandwidth uses the algorithmic bytes only (b = element size):
     RMS fwd 2MNb + Nb + 4M     LN fwd 2MNb + 2Nb + 8M
     RMS bwd 3MNb + Nb + 4M + 4N   LN bwd 3MNb + Nb + 8M + 8N
@@ -23,9 +26,13 @@ import sys
 DTYPE_CODE = {"fp32": 0, "fp16": 1, "bf16": 2}
 ELEM = {"fp32": 4, "fp16": 2, "bf16": 2}
 
-# (op, dtype, M, N) of the workloads.
+# Calls with at most this many rows have their own measured rows.
+SMALL_M = 1024
+
+# (op, dtype, M, N) of the workloads, and the small-M bucket of the short and
+# LLM-shaped rows.
 SHAPES = (
-    [("rms", "bf16", 1024, 1024)]
+    [(op, "bf16", SMALL_M, n) for op in ("rms", "ln") for n in (256, 512, 1024, 2048, 4096, 8192)]
     + [("rms", "bf16", 65536, n) for n in (256, 384, 512, 768, 1024, 2048)]
     + [("ln", "bf16", 16384, n) for n in (4096, 8192)]
     + [(op, "bf16", 2048, n) for op in ("rms", "ln") for n in (16384, 32768, 65536, 131072)]
@@ -124,16 +131,21 @@ def sweep(reps: int, only=None, dirs=(0, 1)):
     return out
 
 
-ROW_RE = re.compile(r'^\{(\d+), (\d+), (\d+), (\d+), "[^"]+"\},.*$')
+ROW_RE = re.compile(r'^\{(\d+), (\d+), (\d+), (-?\d+), (\d+), "[^"]+"\},.*$')
+
+
+def m_bucket(M: int) -> int:
+    """m_max of the table row a measurement at M rows belongs to (-1: any M)."""
+    return SMALL_M if M <= SMALL_M else -1
 
 
 def emit(results, table_path):
     """Merge sweep results into the measured block of the dispatch table: a
-    (op, direction, dtype, N) the sweep measured gets its fastest variant; the
-    other measured rows stay as they are."""
+    (op, direction, dtype, M bucket, N) the sweep measured gets its fastest
+    variant; the other measured rows stay as they are."""
     best = {}
     for r in results:
-        key = (r["op"], r["dir"], r["dtype"], r["N"])
+        key = (r["op"], r["dir"], r["dtype"], m_bucket(r["M"]), r["N"])
         if key not in best or r["gbs"] > best[key]["gbs"]:
             best[key] = r
     text = open(table_path).read()
@@ -144,11 +156,13 @@ def emit(results, table_path):
         m = ROW_RE.match(line)
         if m:
             rows[tuple(int(v) for v in m.groups())] = line
-    for (op, d, dt, n), r in best.items():
-        key = (1 if op == "ln" else 0, d, DTYPE_CODE[dt], n * ELEM[dt] // 16)
-        rows[key] = (f'{{{key[0]}, {d}, {key[2]}, {key[3]}, "{r["variant"]}"}},'
+    for (op, d, dt, mb, n), r in best.items():
+        key = (1 if op == "ln" else 0, d, DTYPE_CODE[dt], mb, n * ELEM[dt] // 16)
+        rows[key] = (f'{{{key[0]}, {d}, {key[2]}, {key[3]}, {key[4]}, "{r["variant"]}"}},'
                      f'  // {op} {"fwd" if d == 0 else "bwd"} {dt} M={r["M"]} N={n}: {r["gbs"]:.0f} GB/s')
-    order = sorted(rows, key=lambda k: (-k[0], k[1], -k[2], k[3]))
+    # by row length; for one row length the small-M row first (the first
+    # matching row wins)
+    order = sorted(rows, key=lambda k: (-k[0], k[1], -k[2], k[4], k[3] < 0, k[3]))
     block = "// ---- measured rows (tune.py) ----\n" + "\n".join(rows[k] for k in order) + "\n"
     open(table_path, "w").write(text[:start] + block + text[end:])
     return [rows[k] for k in order]

@@ -61,11 +61,15 @@ def test_status_strings(lib):
 
 def test_variant_tables(lib):
     from rmsnorm_norm_fwd_gb300 import binding as b
+    src = open(os.path.join(ROOT, "rmsnorm_norm_fwd_gb300", "csrc", "api.cu")).read()
+    cap = int(re.search(r"constexpr int kMaxVariants = (\d+);", src).group(1))
     for ln in (False, True):
         for d in (0, 1):
             for dt in ("fp32", "fp16", "bf16"):
                 names = b.variants(ln, d, dt)
                 assert "elem" in names and len(names) == len(set(names)) >= 10
+                # the host's per-variant caches are indexed by variant
+                assert len(names) <= cap, (ln, d, dt, len(names), cap)
     assert lib.gbnorm_force_variant(0, 0, 2, b"no-such-variant") == 1
     assert lib.gbnorm_force_variant(0, 0, 2, None) == 0
     assert lib.gbnorm_variant_at(0, 0, 2, 10_000) is None
@@ -82,7 +86,6 @@ def test_forward_rejects_bad_arguments(lib):
     assert f(V(A), V(B), V(C), V(D), 4, 0, bf16, 1e-6, None) == 1            # N = 0
     assert f(V(A), V(B), V(C), V(D), -1, 8, bf16, 1e-6, None) == 1           # M < 0
     assert f(V(A), V(B), V(C), V(D), 4, 8, 7, 1e-6, None) == 1               # dtype
-    assert f(V(A), None, V(C), V(D), 4, (1 << 18) + 8, bf16, 1e-6, None) == 2  # NULL gamma, N too large
     assert f(None, V(B), V(C), V(D), 4, 8, bf16, 1e-6, None) == 1            # x null
     assert f(V(A), V(B), V(C), V(D), 4, 8, bf16, float("nan"), None) == 1    # eps
     assert f(V(A), V(B), V(C), V(D), 4, 8, bf16, -1.0, None) == 1            # eps < 0
@@ -90,7 +93,6 @@ def test_forward_rejects_bad_arguments(lib):
     assert f(V(A), V(B), V(C), V(C + 4), 4, 8, bf16, 1e-6, None) == 1        # rstd overlaps y
     assert f(V(A), V(B), V(C), V(D), 4, (1 << 24) + 1, bf16, 1e-6, None) == 1  # N too large
     g = lib.layernorm_fwd
-    assert g(V(A), V(B), None, V(C), V(D), V(E_), 4, (1 << 18) + 8, bf16, 1e-5, None) == 2  # NULL beta, N too large
     assert g(V(A), V(B), V(F), V(C), V(D), V(D), 4, 8, bf16, 1e-5, None) == 1   # mean == rstd
 
 
@@ -99,8 +101,6 @@ def test_backward_rejects_bad_arguments(lib):
     f = lib.rmsnorm_bwd
     # dx overlapping x (not the permitted in-place pair dx == dy)
     assert f(V(A), V(B), V(C), V(D), V(B), V(E_), V(F), 1 << 20, 4, 8, bf16, None) == 1
-    assert f(V(A), V(B), None, V(D), V(E_), V(G), V(F), 1 << 20, 4, (1 << 18) + 8, bf16,
-             None) == 2  # NULL gamma, N too large
     assert f(V(A), V(B), V(C), None, V(E_), V(G), V(F), 1 << 20, 4, 8, bf16, None) == 1  # rstd
     assert f(V(A), V(B), V(C), V(D), V(E_), V(G), V(F), 1 << 20, 4, 0, bf16, None) == 1  # N
     g = lib.layernorm_bwd
@@ -110,9 +110,9 @@ def test_backward_rejects_bad_arguments(lib):
 
 
 def test_null_parameters_are_accepted(lib):
-    """gamma / beta / dgamma / dbeta may be NULL (defaults, or sums not
-    produced): such calls pass the argument checks; without a usable device
-    they report CUDA or unsupported, never invalid arguments."""
+    """gamma / beta / dgamma / dbeta may be NULL (the constants 1 / 0, or sums
+    not produced), at any N: such calls pass the argument checks; without a
+    usable device they report CUDA or unsupported, never invalid arguments."""
     import torch
     if torch.cuda.is_available():
         pytest.skip("a CUDA device is present")
@@ -123,6 +123,12 @@ def test_null_parameters_are_accepted(lib):
                            None) in (2, 4)
     assert lib.layernorm_bwd(V(A), V(B), None, V(C), V(D), V(E_), None, None, V(H), 1 << 20, 4, 8,
                              bf16, None) in (2, 4)
+    # no limit on N for the missing rows: nothing is read for them (buffers
+    # 2^40 bytes apart, so that the wide rows do not overlap)
+    far = [V(k << 40) for k in range(1, 7)]
+    assert lib.rmsnorm_fwd(far[0], None, far[1], far[2], 4, (1 << 20) + 8, bf16, 1e-6, None) in (2, 4)
+    assert lib.layernorm_fwd(far[0], far[3], None, far[1], far[2], far[4], 4, (1 << 20) + 8, bf16,
+                             1e-5, None) in (2, 4)
 
 
 def test_valid_call_without_device_reports_cuda_or_unsupported(lib):
@@ -160,12 +166,48 @@ def test_dispatch_table_names_compiled_variants(lib):
     next row."""
     from rmsnorm_norm_fwd_gb300 import binding as b
     table = os.path.join(ROOT, "rmsnorm_norm_fwd_gb300", "csrc", "dispatch_table.inc")
-    rows = re.findall(r'^\{(-?\d+), (\d+), (-?\d+), (\d+), "([^"]+)"\}', open(table).read(), re.M)
+    rows = re.findall(r'^\{(-?\d+), (\d+), (-?\d+), (-?\d+), (\d+), "([^"]+)"\}', open(table).read(), re.M)
     assert len(rows) > 50
     names = {0: "fp32", 1: "fp16", 2: "bf16"}
-    for ln, d, dt, nv, variant in rows:
+    for ln, d, dt, m_max, nv, variant in rows:
+        assert int(m_max) == -1 or int(m_max) > 0
         for is_ln in ((0, 1) if ln == "-1" else (int(ln),)):
             for code in ((0, 1, 2) if dt == "-1" else (int(dt),)):
                 assert variant in b.variants(bool(is_ln), int(d), names[code]), \
                     (variant, is_ln, d, names[code])
         assert int(nv) > 0
+
+
+def test_general_form_rejects_bad_arguments(lib):
+    """norm_fwd_ex / norm_bwd_ex argument checks (before any device use)."""
+    bf16, f32 = 2, 0
+    I64 = ctypes.c_int64
+    lib.norm_fwd_ex.argtypes = [ctypes.c_int, I64, I64, ctypes.c_float, V, I64, ctypes.c_int, V, I64, V, I64, V,
+                                V, ctypes.c_int, V, I64, ctypes.c_int, V, V, V]
+    f = lib.norm_fwd_ex
+    far = [V(k << 40) for k in range(1, 9)]
+    M, N = 4, 64
+    ok = dict(x=far[0], ldx=N, r=None, ldr=N, h=None, ldh=N, y=far[1], ldy=N)
+
+    def fwd(**kw):
+        a = {**ok, **kw}
+        return f(0, M, N, 1e-6, a["x"], a["ldx"], bf16, a["r"], a["ldr"], a["h"], a["ldh"], far[2], None, f32,
+                 a["y"], a["ldy"], bf16, None, far[3], None)
+    assert fwd(h=far[4]) == 1                   # h without a residual
+    assert fwd(ldx=N - 1) == 1                  # row stride below N
+    assert fwd(ldy=N - 8) == 1
+    assert fwd(y=V((1 << 40) + 64)) == 1        # y overlaps x (not the same rows)
+    assert fwd(r=far[4], h=V((5 << 40) + 2)) == 1  # h overlaps the residual, not exactly
+    assert f(0, M, N, 1e-6, far[0], N, 5, None, N, None, N, None, None, f32, far[1], N, bf16, None, None,
+             None) == 1                          # x dtype
+    assert f(0, M, N, float("nan"), far[0], N, bf16, None, N, None, N, None, None, f32, far[1], N, bf16, None,
+             None, None) == 1                    # eps
+    lib.norm_bwd_ex.argtypes = [ctypes.c_int, I64, I64, V, I64, ctypes.c_int, V, I64, ctypes.c_int, V, I64, V,
+                                ctypes.c_int, V, V, V, I64, V, V, V, ctypes.c_size_t, V]
+    b = lib.norm_bwd_ex
+    assert b(0, M, N, far[0], N, bf16, far[1], N, bf16, None, N, None, bf16, None, far[2], far[1], N, None, None,
+             far[3], 1 << 20, None) == 1         # dx over x
+    assert b(0, M, N, far[0], N, bf16, far[1], N, bf16, None, N, None, bf16, None, None, far[4], N, None, None,
+             far[3], 1 << 20, None) == 1         # rstd missing
+    assert b(0, M, N, far[0], N - 1, bf16, far[1], N, bf16, None, N, None, bf16, None, far[2], far[4], N, None,
+             None, far[3], 1 << 20, None) == 1   # dy row stride below N

@@ -1,0 +1,181 @@
+"""The general form (norm_fwd_ex / norm_bwd_ex through the C ABI) against the
+fp64 oracle: a storage type per tensor (rows, parameters, output), rows with
+their own strides, and the fused residual add, forward and backward, on the
+vector path and the element-wise path (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import compare, ex_variant
+from rmsnorm_norm_fwd_gb300.inputs import DTYPES, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _no_device_fault():
+    import rmsnorm_norm_fwd_gb300 as g
+    g.read_fault(reset=True)
+    yield
+    assert g.read_fault(reset=True) == 0
+
+
+def _strided(t, pad):
+    """t on the GPU as a view with row stride N + pad (the padding holds NaN)."""
+    M, N = t.shape
+    buf = torch.full((M, N + pad), float("nan"), dtype=t.dtype, device="cuda")
+    v = buf[:, :N]
+    v.copy_(t.to("cuda"))
+    return v
+
+
+def _vec(*ts):
+    return all(t is None or (t.data_ptr() % 16 == 0 and (t.stride(0) * t.element_size()) % 16 == 0)
+               for t in ts)
+
+
+def run_ex(op, inp, pad=0, y_dtype=None, residual=None, dres=None, store_h=True):
+    """Forward and backward through the general form; returns (host outputs,
+    variants).  With a residual, inp.x is x and the backward differentiates at
+    the stored h; without one, x itself."""
+    import rmsnorm_norm_fwd_gb300 as g
+    ln = op == "ln"
+    x = _strided(inp.x, pad)
+    r = _strided(residual, pad) if residual is not None else None
+    gam, bet = inp.gamma.cuda(), inp.beta.cuda() if ln else None
+    y = _strided(torch.empty(inp.x.shape, dtype=DTYPES[y_dtype or inp.dtype]), pad + 8)
+    y, h, mean, rstd = g.norm_fwd_ex(ln, x, gam, bet, inp.eps, residual=r, store_h=store_h, y=y)
+    dy = _strided(inp.dy, pad)
+    xb = h if h is not None else x
+    if residual is not None and h is None:  # h not stored: the oracle's, for the backward
+        xb = _strided(oracle.residual_add(inp.x, residual, inp.dtype), pad)
+    dr = _strided(dres, pad) if dres is not None else None
+    dx = _strided(torch.empty(inp.x.shape, dtype=inp.x.dtype), pad + 16)
+    dx, dg, db = g.norm_bwd_ex(ln, dy, xb, gam, mean, rstd, dres=dr, dx=dx)
+    torch.cuda.synchronize()
+    N = inp.x.shape[1]
+    out = {"y": y.cpu(), "rstd": rstd.cpu(), "dx": dx.cpu(), "dgamma": dg.cpu()}
+    if ln:
+        out.update(mean=mean.cpu(), dbeta=db.cpu())
+    if h is not None:
+        out["h"] = h.cpu()
+    vf = ex_variant(N, _vec(x, r, h, y) and gam.data_ptr() % 16 == 0)
+    vb = ex_variant(N, _vec(dy, xb, dr, dx))
+    return out, (vf, vb)
+
+
+MIXED = [("bf16", "fp32", "bf16"), ("fp16", "fp32", "fp16"), ("fp32", "fp32", "bf16"),
+         ("bf16", "bf16", "fp32"), ("fp32", "bf16", "fp16")]
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("types", MIXED, ids=["-".join(t) for t in MIXED])
+@pytest.mark.parametrize("N", [1000, 4096, 5120, 16384, 32768])
+def test_mixed_dtypes(op, types, N):
+    """Rows, parameters and output each in their own type (x / gamma / y):
+    y is held to its own type's tolerance, dx to x's."""
+    xdt, pdt, ydt = types
+    M = 301 if N <= 8192 else 37
+    inp = make_inputs(M, N, dtype=xdt, dist="llm" if N >= 4096 else op, op=op, param_dtype=pdt, dy_dtype=ydt)
+    out, variants = run_ex(op, inp, y_dtype=ydt)
+    compare(op, inp, out, variants=variants, y_dtype=ydt).assert_ok()
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("N,pad", [(384, 8), (384, 3), (4096, 64), (4096, 1), (65536, 8)])
+def test_strided_rows(op, dtype, N, pad):
+    """Rows inside wider buffers (x, y, dy and dx each with its own stride);
+    a padding that breaks 16-byte rows takes the element-wise kernels."""
+    M = 129 if N <= 4096 else 9
+    inp = make_inputs(M, N, dtype=dtype, dist="llm" if N >= 4096 else op, op=op)
+    out, variants = run_ex(op, inp, pad=pad)
+    if (pad * inp.x.element_size()) % 16 == 0 and N % 8 == 0:
+        assert variants[0] != "exe" or N > 16384
+    compare(op, inp, out, variants=variants).assert_ok()
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("N", [1000, 2048, 8192])
+@pytest.mark.parametrize("store_h", [True, False])
+def test_residual_add(op, dtype, N, store_h):
+    """h = x + r rounded once to the storage type, stored (bit-identical to the
+    oracle's), normalised; backward at h with the residual stream's gradient
+    added into dx."""
+    M = 211
+    inp = make_inputs(M, N, dtype=dtype, dist=op, op=op)
+    res = make_inputs(M, N, dtype=dtype, dist="rms", op=op, seed=99).x
+    dres = make_inputs(M, N, dtype=dtype, dist="rms", op=op, seed=98).dy
+    out, variants = run_ex(op, inp, residual=res, dres=dres, store_h=store_h)
+    h_ref = oracle.residual_add(inp.x, res, dtype)
+    if store_h:
+        assert torch.equal(out["h"], h_ref)
+    inp_h = make_inputs(M, N, dtype=dtype, dist=op, op=op)
+    inp_h.x = h_ref
+    compare(op, inp_h, out, variants=variants, dres=dres).assert_ok()
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+def test_residual_in_place(op):
+    """h written over r and dx over dres (the usual layout of a residual
+    stream): the same results as with separate buffers."""
+    import rmsnorm_norm_fwd_gb300 as g
+    ln = op == "ln"
+    M, N = 333, 4096
+    inp = make_inputs(M, N, dtype="bf16", op=op, dist=op)
+    x, gam = inp.x.cuda(), inp.gamma.cuda()
+    bet = inp.beta.cuda() if ln else None
+    r = make_inputs(M, N, dtype="bf16", seed=7).x.cuda()
+    dres = make_inputs(M, N, dtype="bf16", seed=8).dy.cuda()
+    dy = inp.dy.cuda()
+    y1, h1, m1, r1 = g.norm_fwd_ex(ln, x, gam, bet, inp.eps, residual=r)
+    dx1, dg1, db1 = g.norm_bwd_ex(ln, dy, h1, gam, m1, r1, dres=dres)
+    r2, dres2 = r.clone(), dres.clone()
+    y2, h2, m2, s2 = g.norm_fwd_ex(ln, x, gam, bet, inp.eps, residual=r2, h=r2)
+    assert h2.data_ptr() == r2.data_ptr()
+    dx2, dg2, db2 = g.norm_bwd_ex(ln, dy, h2, gam, m2, s2, dres=dres2, dx=dres2)
+    torch.cuda.synchronize()
+    assert torch.equal(h1, r2) and torch.equal(y1, y2) and torch.equal(dx1, dres2)
+    assert torch.equal(dg1, dg2) and (not ln or torch.equal(db1, db2))
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+def test_optional_parameters_and_empty(op):
+    """NULL gamma / beta are 1 / 0; M = 0 launches nothing and gives zero
+    parameter gradients."""
+    import rmsnorm_norm_fwd_gb300 as g
+    ln = op == "ln"
+    M, N = 64, 2048
+    inp = make_inputs(M, N, dtype="bf16", op=op, dist=op)
+    inp.gamma = torch.ones_like(inp.gamma)
+    inp.beta = torch.zeros_like(inp.beta)
+    x, dy = inp.x.cuda(), inp.dy.cuda()
+    y, _, mean, rstd = g.norm_fwd_ex(ln, x, None, None, inp.eps)
+    dx, dg, db = g.norm_bwd_ex(ln, dy, x, None, mean, rstd)
+    torch.cuda.synchronize()
+    out = {"y": y.cpu(), "rstd": rstd.cpu(), "dx": dx.cpu(), "dgamma": dg.cpu()}
+    if ln:
+        out.update(mean=mean.cpu(), dbeta=db.cpu())
+    v = ex_variant(N, True)
+    compare(op, inp, out, variants=(v, v)).assert_ok()
+    e = torch.empty(0, N, device="cuda", dtype=torch.bfloat16)
+    dge = torch.full((N,), 5.0, device="cuda")
+    _, _, me, re_ = g.norm_fwd_ex(ln, e, None, None, inp.eps)
+    g.norm_bwd_ex(ln, e, e, None, me, re_, dgamma=dge)
+    torch.cuda.synchronize()
+    assert torch.all(dge == 0)
+
+
+def test_ex_deterministic():
+    import rmsnorm_norm_fwd_gb300 as g
+    inp = make_inputs(1000, 5120, dtype="bf16", op="ln", dist="llm", param_dtype="fp32")
+    x, gam, bet, dy = inp.x.cuda(), inp.gamma.cuda(), inp.beta.cuda(), inp.dy.cuda()
+    outs = []
+    for _ in range(2):
+        y, _, m, r = g.norm_fwd_ex(True, x, gam, bet, inp.eps)
+        outs.append((y, m, r) + g.norm_bwd_ex(True, dy, x, gam, m, r))
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)

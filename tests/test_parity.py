@@ -33,6 +33,8 @@ def test_small_shapes(op, dtype, N):
 
 def _geom(name):
     """(tpr, vpt, rows, cluster, cta, is_tma) of a vector variant, None for 'elem'."""
+    if name.startswith("sk"):  # single-kernel backward: the staged kernel's geometry
+        return _geom(name[2:])
     m = re.fullmatch(r"(\d+)x(\d+)r(\d+)c(\d+)b(\d+)", name)
     if m:
         return tuple(int(v) for v in m.groups()) + (False,)
@@ -56,6 +58,10 @@ def _geom(name):
     if m:
         nt, u, _, _, _ = (int(v) for v in m.groups())
         return ("wide", nt, u, 1)
+    m = re.fullmatch(r"wtma(\d+)x(\d+)", name)
+    if m:
+        cw, u = (int(v) for v in m.groups())
+        return ("wide", 32 * cw, u, 1)
     m = re.fullmatch(r"bwide(\d+)u(\d+)c(\d+)p(\d+)f(\d+)m(\d+)", name)
     if m:
         nt, u, cl, _, _, _ = (int(v) for v in m.groups())
@@ -114,6 +120,8 @@ def test_forced_variant(op, direction, dtype, variant):
         nt, u, cl = geo[1], geo[2], geo[3]
         full = cl * 2 * nt * u * E
         shapes = [(9, full), (9, full - E), (7, cl * (nt * E + 5 * E)), (5, cl * 3 * E)]
+        if variant.startswith("wtma"):  # several ring jobs per pass, a ragged last one
+            shapes.append((3, 7 * nt * u * E + 3 * E))
     else:
         tpr, vpt, r, cl, cta, tma = geo
         cap = tpr * vpt * cl * E
@@ -222,7 +230,8 @@ def test_deterministic(op, N):
     a = gpu_run(op, inp)
     b = gpu_run(op, inp)
     for k in a:
-        assert torch.equal(a[k], b[k]), k
+        if k != "variants":
+            assert torch.equal(a[k], b[k]), k
 
 
 def test_rms_scale_equivariance():
@@ -351,7 +360,11 @@ def test_unaligned_stats_fall_back_from_tma():
     dx, dg, db = g.layernorm_bwd(dy, x, gam, mean_u, rstd_u)
     torch.cuda.synchronize()
     out = {"y": y, "mean": mean, "rstd": rstd, "dx": dx, "dgamma": dg, "dbeta": db}
-    compare("ln", inp, out).assert_ok()
+    # the backward that ran is not the one aligned statistics select: take the
+    # deeper of the two sums
+    vf = g.variant_name(True, 0, M, N, "bf16")
+    vb = [g.variant_name(True, 1, M, N, "bf16"), g.variant_name(True, 1, M, N, "bf16", aligned=False)]
+    compare("ln", inp, out, variants=(vf, vb)).assert_ok()
 
 
 @pytest.mark.parametrize("op", ["rms", "ln"])
@@ -383,3 +396,81 @@ def test_optional_parameters(op, dtype, N):
     torch.cuda.synchronize()
     assert torch.equal(dx, dx2)
     compare(op, inp, out).assert_ok()
+
+
+# Single-kernel backward variants, each against the two-kernel variant of the
+# same geometry: (op, variant, dtype, M, N).
+SK_CASES = [("rms", "sktma32x4w8", "bf16", 1024, 1024), ("ln", "sktma32x4w8", "bf16", 1024, 1024),
+            ("rms", "sktma16x2w8", "bf16", 1001, 256), ("ln", "sktma128x4w8", "fp32", 300, 2048),
+            ("rms", "sktma256x8w8", "bf16", 200, 16384), ("ln", "sktmp256x4b512", "bf16", 513, 8192),
+            ("rms", "sktmp128x4b512", "fp16", 77, 4096), ("ln", "sktmp512x4b512", "fp32", 129, 8192)]
+
+
+@pytest.mark.parametrize("op,variant,dtype,M,N", SK_CASES, ids=[f"{c[0]}-{c[1]}-{c[2]}-{c[3]}x{c[4]}" for c in SK_CASES])
+@pytest.mark.parametrize("limit", [0, 1, 5])
+def test_single_kernel_backward(op, variant, dtype, M, N, limit):
+    """The single-kernel backward (cooperative launch; the kernel sums the
+    partial rows itself once every CTA's flag carries the call's epoch) gives
+    dx, dgamma and dbeta bit-identical to the two-kernel path with the same
+    grid, twice in a row on one workspace (the second call meets the first
+    call's flags), under a grid cap (several tiles per CTA; one CTA alone),
+    with a sum not asked for, and within tolerance of the oracle."""
+    import rmsnorm_norm_fwd_gb300 as g
+    ln = op == "ln"
+    inp = make_inputs(M, N, dtype=dtype, dist="llm" if N >= 4096 else op, op=op)
+    x, dy, gam, bet = (t.cuda() for t in (inp.x, inp.dy, inp.gamma, inp.beta))
+    if ln:
+        y, mean, rstd = g.layernorm_fwd(x, gam, bet, inp.eps)
+    else:
+        (y, rstd), mean = g.rmsnorm_fwd(x, gam, inp.eps), None
+
+    def bwd(ws, **kw):
+        if ln:
+            return g.layernorm_bwd(dy, x, gam, mean, rstd, workspace=ws, **kw)
+        return g.rmsnorm_bwd(dy, x, gam, rstd, workspace=ws, **kw)
+
+    runs = {}
+    try:
+        g.set_grid_limit(limit)
+        for v in (variant[2:], variant):
+            g.force_variant(ln, 1, dtype, v)
+            assert g.variant_name(ln, 1, M, N, dtype) == v
+            ws = torch.empty(g.norm_bwd_workspace_size(ln, M, N, dtype), device="cuda", dtype=torch.uint8)
+            runs[v] = [bwd(ws), bwd(ws)]
+            if ln:
+                runs[v].append(bwd(ws, need_dgamma=False))
+        torch.cuda.synchronize()
+    finally:
+        g.set_grid_limit(0)
+        g.force_variant(ln, 1, dtype, None)
+    ref = runs[variant[2:]][0]
+    for got in runs[variant][:2] + runs[variant[2:]][1:2]:
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
+    if ln:  # dbeta alone, dgamma not produced: the same dx and dbeta
+        dx3, dg3, db3 = runs[variant][2]
+        assert dg3 is None and torch.equal(dx3, ref[0]) and torch.equal(db3, ref[2])
+    out = {"y": y, "rstd": rstd, "dx": ref[0], "dgamma": ref[1]}
+    if ln:
+        out.update(mean=mean, dbeta=ref[2])
+    compare(op, inp, out, variants=(g.variant_name(ln, 0, M, N, dtype), variant)).assert_ok()
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("variant", ["wtma16x2", "wtma8x2"])
+@pytest.mark.parametrize("limit", [1, 3])
+def test_wide_ring_wraps(op, variant, limit):
+    """The bulk-copy wide forward under a grid cap: each CTA walks many rows,
+    so every ring stage goes through many phases, with pass-1 and pass-2 jobs
+    of different sizes interleaved (row length not a multiple of a chunk)."""
+    import rmsnorm_norm_fwd_gb300 as g
+    M, N = 23, 3 * 8192 + 40
+    try:
+        g.force_variant(op == "ln", 0, "bf16", variant)
+        g.set_grid_limit(limit)
+        assert g.variant_name(op == "ln", 0, M, N, "bf16") == variant
+        rep, _, _ = run_case(op, "bf16", M, N)
+        rep.assert_ok()
+    finally:
+        g.set_grid_limit(0)
+        g.force_variant(op == "ln", 0, "bf16", None)
