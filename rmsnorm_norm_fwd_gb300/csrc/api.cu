@@ -229,6 +229,42 @@ bool wtma_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, s
     return true;
 }
 
+// Ring of a bulk-copy wide-row backward: stages of one chunk of x and one of dy
+// (tpr vectors each); false unless each CTA's column slice fits in vpt chunks.
+bool wtmac_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, size_t *dyn_smem) {
+    if (c.dir != 1) return false;
+    const int64_t nv = c.N / v.elems_per_vec;
+    const int64_t slice = (nv + v.cl - 1) / v.cl;
+    if (slice > (int64_t)v.tpr * v.vpt) return false;
+    const size_t stage = 2u * (size_t)v.tpr * 16u;
+    const size_t gam = (size_t)v.tpr * v.vpt * 16u;  // gamma of the slice
+    // the kernel's static shared memory (exchange slots, barriers) stays below 1 KB
+    const size_t budget = (size_t)g_dev[dev].smem_optin - kTmaHeaderBytes - gam - 1024;
+    int stages = (int)(budget / stage);
+    if (stages > kTmaMaxStages) stages = kTmaMaxStages;
+    if (stages < 2) return false;
+    tc->rows = 1;
+    tc->stages = stages;
+    tc->stride = (uint32_t)stage;
+    tc->fault = g_dev[dev].fault;
+    *dyn_smem = kTmaHeaderBytes + gam + (size_t)stages * stage;
+    return true;
+}
+
+// Shared memory of a register-sum wide backward: gamma of the slice as fp32
+// (E / 4 planes of tpr * vpt float4); false if a CTA's slice exceeds vpt
+// vectors per thread.
+bool wider_geometry(const Variant &v, const CallShape &c, int dev, size_t *dyn_smem) {
+    if (c.dir != 1) return false;
+    const int64_t nv = c.N / v.elems_per_vec;
+    const int64_t slice = (nv + v.cl - 1) / v.cl;
+    if (slice > (int64_t)v.tpr * v.vpt) return false;
+    const size_t bytes = (size_t)(v.elems_per_vec / 4) * (size_t)v.tpr * v.vpt * 16u;
+    if (bytes + 4096 > (size_t)g_dev[dev].smem_optin) return false;
+    *dyn_smem = bytes;
+    return true;
+}
+
 // Shared memory of a wide-row variant: none for the forward; for the
 // backward each CTA's column slice of dgamma (and dbeta) sums in fp32.  False
 // if a CTA of the cluster would get no columns or the sums do not fit.
@@ -265,6 +301,15 @@ bool can_serve(const Variant &v, const CallShape &c, int dev) {
         TileCfg tc;
         size_t dyn;
         return wtma_geometry(v, c, dev, &tc, &dyn);
+    }
+    if (v.kind == kWtmaC) {
+        TileCfg tc;
+        size_t dyn;
+        return wtmac_geometry(v, c, dev, &tc, &dyn);
+    }
+    if (v.kind == kWideR) {
+        size_t dyn;
+        return wider_geometry(v, c, dev, &dyn);
     }
     if (v.kind == kRowsS) {
         size_t dyn;
@@ -353,12 +398,14 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
     int o = slot.load(std::memory_order_relaxed);
     const Variant &v = kTables[c.is_ln][c.dir][c.dtype]->v[idx];
     // Kinds whose shared memory (and so occupancy) depends on the shape.
-    const bool per_shape = v.staged_rows() || v.kind == kRowsS || v.kind == kWtma || (v.kind == kWide && dyn_smem > 0);
+    const bool per_shape = v.staged_rows() || v.kind == kRowsS || v.kind == kWtma || v.kind == kWtmaC ||
+                           v.kind == kWideR || (v.kind == kWide && dyn_smem > 0);
     if (o > 0 && !per_shape) {
         *out = o;
         return GBNORM_OK;
     }
-    if (v.staged_rows() || v.kind == kTmaCl || v.kind == kRowsS || v.kind == kWtma || (v.kind == kWide && dyn_smem > 0)) {
+    if (v.staged_rows() || v.kind == kTmaCl || v.kind == kRowsS || v.kind == kWtma || v.kind == kWtmaC ||
+        v.kind == kWideR || (v.kind == kWide && dyn_smem > 0)) {
         std::atomic<uint64_t> &cache = g_occ_tma[dev][c.is_ln][c.dir][c.dtype][idx];
         const uint64_t hit = cache.load(std::memory_order_relaxed);
         if (hit != 0 && (hit >> 16) == (uint64_t)dyn_smem) {
@@ -439,6 +486,8 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
     if (v.kind == kWide && !wide_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kRowsS && !rows_s_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kWtma && !wtma_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
+    if (v.kind == kWtmaC && !wtmac_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
+    if (v.kind == kWideR && !wider_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     int occ = 0;
     int st = occupancy(c, idx, dev, pl->dyn_smem, &occ);
     if (st != GBNORM_OK) return st;
@@ -450,6 +499,18 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
         if (limit > 0 && limit < cap) cap = limit;
         pl->grid = c.M < cap ? c.M : cap;
         pl->P = pl->grid;
+        return GBNORM_OK;
+    }
+    if (v.kind == kWtmaC) {
+        // occ = clusters that fit on the GPU at once; one row per cluster at a time
+        int64_t cap = occ;
+        if (limit > 0) {
+            const int64_t lc = limit / v.cl > 0 ? limit / v.cl : 1;
+            if (lc < cap) cap = lc;
+        }
+        const int64_t ncl = c.M < cap ? c.M : cap;
+        pl->grid = ncl * v.cl;
+        pl->P = ncl;
         return GBNORM_OK;
     }
     if (v.kind == kWtma) {
@@ -763,7 +824,7 @@ int ex_occupancy(int dev, int is_ln, int dir, int slot, const void *k, int cta, 
 // The smallest row-resident geometry that holds the row (vec: every row
 // tensor allows 16-byte vectors and N % 8 == 0), else the element-wise kernel.
 int ex_plan(int is_ln, int dir, int64_t M, int64_t N, bool vec, int dev, ExPlan *pl) {
-    const ExTable &t = kExTables[is_ln];
+    const ExTable &t = kExTables[is_ln][dir];
     const int64_t limit = g_grid_limit.load(std::memory_order_relaxed);
     const int sms = g_dev[dev].sms;
     if (vec && N % 8 == 0) {
@@ -774,7 +835,7 @@ int ex_plan(int is_ln, int dir, int64_t M, int64_t N, bool vec, int dev, ExPlan 
             // the row groups' partials of dgamma and dbeta)
             const size_t dyn = (size_t)N * 4u * (is_ln ? 2u : 1u);
             if (dyn + 4096 > (size_t)g_dev[dev].smem_optin) break;
-            const void *k = dir == 0 ? v.fwd : v.bwd;
+            const void *k = v.kernel;
             int occ = 0;
             const int st = ex_occupancy(dev, is_ln, dir, i, k, v.cta, dyn, &occ);
             if (st != GBNORM_OK) return st;
@@ -786,7 +847,7 @@ int ex_plan(int is_ln, int dir, int64_t M, int64_t N, bool vec, int dev, ExPlan 
             return GBNORM_OK;
         }
     }
-    const void *k = dir == 0 ? t.fwd_elem : t.bwd_elem;
+    const void *k = t.elem;
     int occ = 0;
     const int st = ex_occupancy(dev, is_ln, dir, 16, k, kElemCTA, 0, &occ);
     if (st != GBNORM_OK) return st;

@@ -134,8 +134,8 @@ __device__ __forceinline__ void ex_par8(const float4 *plane, int64_t nc, int64_t
 }
 
 // ============================================================================ forward
-template <bool LN, int TPR, int VPT, int CTA>
-__global__ void __launch_bounds__(CTA) fwd_ex(const ExFwdParams p) {
+template <bool LN, int TPR, int VPT, int CTA, int MINB>
+__global__ void __launch_bounds__(CTA, MINB) fwd_ex(const ExFwdParams p) {
     static_assert(CTA % TPR == 0 && TPR % 32 == 0, "row-group shape");
     constexpr int RPC = CTA / TPR;
     extern __shared__ __align__(16) float4 pars[];  // gamma planes, then beta planes
@@ -239,8 +239,8 @@ __global__ void __launch_bounds__(CTA) fwd_ex(const ExFwdParams p) {
 }
 
 // ============================================================================ backward
-template <bool LN, int TPR, int VPT, int CTA>
-__global__ void __launch_bounds__(CTA) bwd_ex(const ExBwdParams p) {
+template <bool LN, int TPR, int VPT, int CTA, int MINB>
+__global__ void __launch_bounds__(CTA, MINB) bwd_ex(const ExBwdParams p) {
     static_assert(CTA % TPR == 0 && TPR % 32 == 0, "row-group shape");
     pdl_launch_dependents();  // the column reduce waits for this grid's completion
     constexpr int RPC = CTA / TPR;

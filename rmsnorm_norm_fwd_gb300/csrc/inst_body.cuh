@@ -130,7 +130,19 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
             TPR, VPT, 0, 1, NT, VecTraits<GBN_T>::E, 1, 32768, 1},
 #define GBN_SKP_RMS(TPR, VPT, NT) GBN_SKTMP(false, TPR, VPT, NT)
 #define GBN_SKP_LN(TPR, VPT, NT) GBN_SKTMP(true, TPR, VPT, NT)
+#define GBN_BWTMA(LN, CL, K)                                                                   \
+    Variant{GBN_BWTMA_VNAME(CL, K), (const void *)&bwd_wtma<GBN_T, LN, CL, K>, kWtmaC, 512, K, 0, CL, 544, \
+            VecTraits<GBN_T>::E, 1, 0},
+#define GBN_BWT_RMS(CL, K) GBN_BWTMA(false, CL, K)
+#define GBN_BWT_LN(CL, K) GBN_BWTMA(true, CL, K)
+#define GBN_WIDER(LN, NT, K, CL, PF, MINB)                                                     \
+    Variant{GBN_WIDER_VNAME(NT, K, CL, PF, MINB), (const void *)&bwd_wider<GBN_T, LN, NT, K, CL, PF, MINB>, kWideR, \
+            NT, K, 1, CL, NT, VecTraits<GBN_T>::E, MINB, 0},
+#define GBN_WR_RMS(NT, K, CL, PF, MINB) GBN_WIDER(false, NT, K, CL, PF, MINB)
+#define GBN_WR_LN(NT, K, CL, PF, MINB) GBN_WIDER(true, NT, K, CL, PF, MINB)
 static const Variant rms_variants[] = {
+    GBN_WIDER_BWD_GEOMS(GBN_WR_RMS)
+    GBN_BWTMA_BWD_GEOMS(GBN_BWT_RMS)
     GBN_TMA_BWD_GEOMS(GBN_T_RMS)
     GBN_TMP_BWD_GEOMS(GBN_P_RMS)
     GBN_SK_TMA_BWD_GEOMS(GBN_SKT_RMS)
@@ -140,6 +152,8 @@ static const Variant rms_variants[] = {
     GBN_BWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&bwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
+    GBN_WIDER_BWD_GEOMS(GBN_WR_LN)
+    GBN_BWTMA_BWD_GEOMS(GBN_BWT_LN)
     GBN_TMA_BWD_GEOMS(GBN_T_LN)
     GBN_TMP_BWD_GEOMS(GBN_P_LN)
     GBN_SK_TMA_BWD_GEOMS(GBN_SKT_LN)
@@ -156,6 +170,12 @@ const VariantTable GBN_CAT(kBwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_TMP
 #undef GBN_P_RMS
 #undef GBN_P_LN
+#undef GBN_BWTMA
+#undef GBN_BWT_RMS
+#undef GBN_BWT_LN
+#undef GBN_WIDER
+#undef GBN_WR_RMS
+#undef GBN_WR_LN
 #undef GBN_SKTMA
 #undef GBN_SKT_RMS
 #undef GBN_SKT_LN

@@ -5,30 +5,46 @@
 
 namespace gbn {
 
-// (TPR, VPT, CTA): capacity TPR * VPT * 8 elements per row.
-#define GBN_EX_GEOMS(X) \
-    X(32, 1, 256)       \
-    X(32, 2, 256)       \
-    X(64, 2, 256)       \
-    X(128, 2, 256)      \
-    X(128, 4, 256)      \
-    X(256, 4, 256)      \
-    X(512, 4, 512)
+// (TPR, VPT, CTA, MINB): capacity TPR * VPT * 8 elements, MINB CTAs per SM of
+// the launch bound.  The backward holds four arrays of VPT * 8 floats per
+// thread (x - mean, dy, dgamma and dbeta sums): more threads per row, fewer
+// chunks each.
+#define GBN_EXF_GEOMS(X) \
+    X(32, 1, 256, 4)     \
+    X(32, 2, 256, 4)     \
+    X(64, 2, 256, 4)     \
+    X(128, 2, 256, 4)    \
+    X(128, 4, 256, 2)    \
+    X(256, 4, 256, 2)    \
+    X(512, 4, 512, 1)
 
-#define GBN_EX(LN, TPR, VPT, CTA)                                                                     \
-    ExVariant{"ex" #TPR "x" #VPT "b" #CTA, (const void *)&fwd_ex<LN, TPR, VPT, CTA>,                 \
-              (const void *)&bwd_ex<LN, TPR, VPT, CTA>, TPR, VPT, CTA},
-#define GBN_EX_RMS(TPR, VPT, CTA) GBN_EX(false, TPR, VPT, CTA)
-#define GBN_EX_LN(TPR, VPT, CTA) GBN_EX(true, TPR, VPT, CTA)
+#define GBN_EXB_GEOMS(X) \
+    X(32, 1, 256, 4)     \
+    X(64, 1, 256, 4)     \
+    X(128, 1, 256, 4)    \
+    X(256, 1, 256, 4)    \
+    X(512, 1, 512, 2)    \
+    X(512, 2, 512, 1)    \
+    X(512, 4, 512, 1)
 
-static const ExVariant ex_rms[] = {GBN_EX_GEOMS(GBN_EX_RMS)};
-static const ExVariant ex_ln[] = {GBN_EX_GEOMS(GBN_EX_LN)};
+#define GBN_EXF(LN, TPR, VPT, CTA, MINB) \
+    ExVariant{"exf" #TPR "x" #VPT "b" #CTA, (const void *)&fwd_ex<LN, TPR, VPT, CTA, MINB>, TPR, VPT, CTA},
+#define GBN_EXB(LN, TPR, VPT, CTA, MINB) \
+    ExVariant{"exb" #TPR "x" #VPT "b" #CTA, (const void *)&bwd_ex<LN, TPR, VPT, CTA, MINB>, TPR, VPT, CTA},
+#define GBN_EXF_RMS(TPR, VPT, CTA, MINB) GBN_EXF(false, TPR, VPT, CTA, MINB)
+#define GBN_EXF_LN(TPR, VPT, CTA, MINB) GBN_EXF(true, TPR, VPT, CTA, MINB)
+#define GBN_EXB_RMS(TPR, VPT, CTA, MINB) GBN_EXB(false, TPR, VPT, CTA, MINB)
+#define GBN_EXB_LN(TPR, VPT, CTA, MINB) GBN_EXB(true, TPR, VPT, CTA, MINB)
 
-const ExTable kExTables[2] = {
-    {ex_rms, (int)(sizeof(ex_rms) / sizeof(ExVariant)), (const void *)&fwd_exe<false>,
-     (const void *)&bwd_exe<false>},
-    {ex_ln, (int)(sizeof(ex_ln) / sizeof(ExVariant)), (const void *)&fwd_exe<true>,
-     (const void *)&bwd_exe<true>},
+static const ExVariant exf_rms[] = {GBN_EXF_GEOMS(GBN_EXF_RMS)};
+static const ExVariant exf_ln[] = {GBN_EXF_GEOMS(GBN_EXF_LN)};
+static const ExVariant exb_rms[] = {GBN_EXB_GEOMS(GBN_EXB_RMS)};
+static const ExVariant exb_ln[] = {GBN_EXB_GEOMS(GBN_EXB_LN)};
+
+#define GBN_N(a) (int)(sizeof(a) / sizeof(ExVariant))
+const ExTable kExTables[2][2] = {
+    {{exf_rms, GBN_N(exf_rms), (const void *)&fwd_exe<false>}, {exb_rms, GBN_N(exb_rms), (const void *)&bwd_exe<false>}},
+    {{exf_ln, GBN_N(exf_ln), (const void *)&fwd_exe<true>}, {exb_ln, GBN_N(exb_ln), (const void *)&bwd_exe<true>}},
 };
 
 }  // namespace gbn

@@ -89,6 +89,8 @@ enum VariantKind : int {
     kRowsS = 5, // as kRows (no cluster), gamma/beta in shared memory as fp32
     kTmaP = 6,  // as kTma without a producer warp (one thread of the CTA refills the ring)
     kWtma = 7,  // one CTA per row, the row streamed twice through a bulk-copy ring (forward)
+    kWtmaC = 8, // column slices of a cluster streamed twice through a bulk-copy ring (backward)
+    kWideR = 9, // as kWide (backward), the dgamma/dbeta sums in registers, gamma in shared memory
 };
 
 // One compiled kernel and the geometry the host needs to launch it.
@@ -110,12 +112,16 @@ struct Variant {
     int64_t max_n() const {
         return (kind == kElem || kind == kWide || kind == kWtma) ? INT64_MAX
                                                                  : (int64_t)tpr * vpt * cl * elems_per_vec;
+        // (kWtmaC: tpr = consumer threads, vpt = chunks per slice)
     }
     // Threads of a CTA that work on rows (TMA kinds add one producer warp).
-    int consumers() const { return (kind == kTma || kind == kTmaCl || kind == kWtma) ? cta - 32 : cta; }
+    int consumers() const {
+        return (kind == kTma || kind == kTmaCl || kind == kWtma || kind == kWtmaC) ? cta - 32 : cta;
+    }
     bool staged_rows() const { return kind == kTma || kind == kTmaP; }
     int rows_per_cta_iter() const {
-        return (kind == kRows || kind == kRowsS) ? (cta / tpr) * rows : (kind == kWide && cl == 1) ? rows : 1;
+        return (kind == kRows || kind == kRowsS) ? (cta / tpr) * rows
+                                                 : ((kind == kWide || kind == kWideR) && cl == 1) ? rows : 1;
     }
 };
 
@@ -131,18 +137,18 @@ extern const VariantTable kFwdRms_bf16, kFwdLn_bf16, kBwdRms_bf16, kBwdLn_bf16;
 extern const void *const kColReduceVec4;
 extern const void *const kColReduceScalar;
 
-// General-form kernels (ex_kernels.cuh): row-resident geometries by row
-// capacity, and the element-wise kernels; [is_ln].
+// General-form kernels (ex_kernels.cuh): row-resident geometries in order of
+// row capacity, and the element-wise kernel; [is_ln][dir].
 struct ExVariant {
     const char *name;
-    const void *fwd, *bwd;
+    const void *kernel;
     int tpr, vpt, cta;  // capacity tpr * vpt * 8 elements
 };
 struct ExTable {
     const ExVariant *v;
     int count;
-    const void *fwd_elem, *bwd_elem;
+    const void *elem;
 };
-extern const ExTable kExTables[2];
+extern const ExTable kExTables[2][2];
 
 }  // namespace gbn

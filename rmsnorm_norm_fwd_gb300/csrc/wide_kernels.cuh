@@ -638,3 +638,245 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wide(const BwdParams p) {
 }
 
 }  // namespace gbn
+
+namespace gbn {
+
+// ============================================================================ backward, register sums
+// As bwd_wide (a cluster of CL CTAs per row, CTA `rank` owning a contiguous
+// column slice; pass 1 from DRAM, exchange of the row sums through
+// distributed shared memory in four slots, pass 2 from L2; pass 1 of row k + 1
+// before pass 2 of row k), with the dgamma/dbeta sums in registers instead of
+// shared memory: thread t owns vectors t + k * NT (k < K) of the slice, so
+// each element's sums cost two FMAs instead of shared-memory read-modify-
+// writes, and gamma of the slice is widened once to fp32 in shared memory
+// (plane-major float4).  Per element: two conversions, the pass-1 partials
+// and, in pass 2, dx and the two sums -- about half the instructions of
+// bwd_wide, whose sums live in shared memory.  Loads go in batches of KB
+// vectors per tensor (registers: K * E sums per plane plus 2 * KB vectors).
+// MINB: CTAs per SM of the launch bound (registers 65536 / (NT * MINB)); two
+// CTAs of a cluster on one SM let one CTA's exchange or memory wait overlap
+// the other's work.
+template <typename T, bool LN, int NT, int K, int CL, int PF, int MINB>
+__global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
+    pdl_launch_dependents();  // the column reduce waits for this grid's completion
+    constexpr int E = VecTraits<T>::E;
+    constexpr int H = E / 4;
+    constexpr int W = NT / 32;
+    constexpr int NVAL = LN ? 2 : 1;
+    constexpr int NS = 4;
+    constexpr int KB = K < 4 ? K : 4;  // vectors per tensor in flight per thread
+    static_assert(NT % 32 == 0 && NT <= 1024 && CL >= 1 && CL <= 16 && K % KB == 0, "shape");
+    extern __shared__ __align__(16) float4 gsm[];  // gamma of the slice, [H][K * NT] float4
+    __shared__ float red[2][NVAL][W];
+    __shared__ float slot[NS][CL][NVAL];
+    __shared__ __align__(8) uint64_t xch[NS];
+    __shared__ int abort_flag;
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+    const int64_t cid = CL > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
+    const int64_t ncl = CL > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
+    const int64_t M = p.M, nv = p.N / E;
+    const int64_t slice = (nv + CL - 1) / CL;
+    const int64_t v0 = rank * slice;
+    const int64_t cnt = nv - v0 < slice ? (nv - v0 > 0 ? nv - v0 : 0) : slice;
+    const float n = (float)p.N;
+    const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
+    constexpr int KNT = K * NT;
+
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int64_t lv = (int64_t)k * NT + t;
+        const uint4 g = lv < cnt ? param_vec<T>(p.gamma, v0 + lv, true) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int h = 0; h < H; ++h)
+            gsm[h * KNT + lv] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
+                                            vget<T>(g, 4 * h + 3));
+    }
+    if (t == 0) {
+        abort_flag = 0;
+        if (CL > 1) {
+            for (int j = 0; j < NS; ++j) mbar_init(&xch[j], CL);
+            fence_mbar_init();
+        }
+    }
+    // every CTA's barriers exist before any peer arrives on them
+    if constexpr (CL > 1) cluster_sync_all();
+    else __syncthreads();
+
+    float accg[K][E], accb[LN ? K : 1][E];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            accg[k][e] = 0.f;
+            if constexpr (LN) accb[k][e] = 0.f;
+        }
+
+    const int64_t nrows = cid < M ? (M - cid + ncl - 1) / ncl : 0;
+    auto row_of = [&](int64_t k) { return cid + k * ncl; };
+    auto row_x = [&](int64_t k) { return static_cast<const uint4 *>(p.x) + row_of(k) * nv + v0; };
+    auto row_dy = [&](int64_t k) { return static_cast<const uint4 *>(p.dy) + row_of(k) * nv + v0; };
+    auto prefetch = [&](int64_t k) {
+        if (warp == 0 && k < nrows && cnt > 0) {
+            prefetch_row(row_x(k), (size_t)cnt * 16, lane, keep);
+            prefetch_row(row_dy(k), (size_t)cnt * 16, lane, keep);
+        }
+    };
+    auto gam = [&](int k, float (&g)[E]) {
+        const int64_t lv = (int64_t)k * NT + t;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const float4 q = gsm[h * KNT + lv];
+            g[4 * h] = q.x, g[4 * h + 1] = q.y, g[4 * h + 2] = q.z, g[4 * h + 3] = q.w;
+        }
+    };
+    int parity = 0;
+    float cst[3][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // (c1, c2) of row k at [k % 3]
+
+    // pass 1 of row k: this thread's sum g (x - mean) (and sum g), then the
+    // CTA's, sent to the cluster (or, alone, turned into c1, c2)
+    auto pass1 = [&](int64_t kr) {
+        const float rstd = __ldg(p.rstd + row_of(kr));
+        const float mean = LN ? __ldg(p.mean + row_of(kr)) : 0.f;
+        const uint4 *xr = row_x(kr), *dr = row_dy(kr);
+        float v[NVAL];
+        float a2[2] = {0.f, 0.f}, a1[2] = {0.f, 0.f};
+#pragma unroll
+        for (int kb = 0; kb < K; kb += KB) {
+            uint4 qx[KB], qd[KB];
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                const int64_t lv = (int64_t)(kb + i) * NT + t;
+                qx[i] = lv < cnt ? ld_l2hint(xr + lv, keep) : make_uint4(0, 0, 0, 0);
+                qd[i] = lv < cnt ? ld_l2hint(dr + lv, keep) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                float g[E];
+                gam(kb + i, g);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float gg = vget<T>(qd[i], e) * g[e];  // zero past the slice
+                    a2[e & 1] += gg * (vget<T>(qx[i], e) - mean);
+                    if constexpr (LN) a1[e & 1] += gg;
+                }
+            }
+        }
+        v[0] = (a2[0] + a2[1]) * rstd;  // sum g xhat = rstd sum g (x - mean)
+        if constexpr (LN) v[NVAL - 1] = a1[0] + a1[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < NVAL; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < NVAL; ++i) red[parity][i][warp] = v[i];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NVAL; ++i) {
+            float s = 0.f;
+#pragma unroll 4
+            for (int w = 0; w < W; ++w) s += red[parity][i][w];
+            v[i] = s;
+        }
+        parity ^= 1;
+        if constexpr (CL > 1) {
+            if (t < CL) {
+                const int sp = (int)(kr % NS);
+                const uint32_t dst = map_to_rank(smem_u32(&slot[sp][rank][0]), (uint32_t)t);
+#pragma unroll
+                for (int i = 0; i < NVAL; ++i) st_cluster_f32(dst + 4u * i, v[i]);
+                mbar_arrive_remote(map_to_rank(smem_u32(&xch[sp]), (uint32_t)t));
+            }
+        } else {
+            cst[kr % 3][0] = LN ? v[NVAL - 1] / n : 0.f;
+            cst[kr % 3][1] = v[0] / n;
+        }
+    };
+    auto recv = [&](int64_t kr) {
+        if constexpr (CL > 1) {
+            const int sp = (int)(kr % NS);
+            mbar_wait_cluster_bounded(&xch[sp], (uint32_t)((kr / NS) & 1), &abort_flag, p.tc.fault);
+            float s[NVAL];
+#pragma unroll
+            for (int i = 0; i < NVAL; ++i) {
+                s[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) s[i] += slot[sp][c][i];
+            }
+            cst[kr % 3][0] = LN ? s[NVAL - 1] / n : 0.f;
+            cst[kr % 3][1] = s[0] / n;
+        }
+    };
+    // pass 2 of row k: dx and this thread's dgamma/dbeta sums
+    auto pass2 = [&](int64_t kr) {
+        const float rstd = __ldg(p.rstd + row_of(kr));
+        const float mean = LN ? __ldg(p.mean + row_of(kr)) : 0.f;
+        const float rc1 = rstd * cst[kr % 3][0], rc2 = rstd * cst[kr % 3][1];
+        const uint4 *xr = row_x(kr), *dr = row_dy(kr);
+        uint4 *dxr = static_cast<uint4 *>(p.dx) + row_of(kr) * nv + v0;
+#pragma unroll
+        for (int kb = 0; kb < K; kb += KB) {
+            uint4 qx[KB], qd[KB];
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                const int64_t lv = (int64_t)(kb + i) * NT + t;
+                qx[i] = lv < cnt ? ld_l2hint(xr + lv, drop) : make_uint4(0, 0, 0, 0);
+                qd[i] = lv < cnt ? ld_l2hint(dr + lv, drop) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                const int64_t lv = (int64_t)(kb + i) * NT + t;
+                float g[E], o[E];
+                gam(kb + i, g);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float xh = (vget<T>(qx[i], e) - mean) * rstd;
+                    const float dyv = vget<T>(qd[i], e);
+                    o[e] = fmaf(-rc2, xh, fmaf(rstd, dyv * g[e], -rc1));
+                    accg[kb + i][e] += dyv * xh;  // zero past the slice (dy = 0)
+                    if constexpr (LN) accb[kb + i][e] += dyv;
+                }
+                if (lv < cnt) st_l2hint(dxr + lv, vpack<T>(o), drop);
+            }
+        }
+    };
+
+    if (PF == 2) prefetch(0);
+    if (nrows > 0) {
+        if (PF == 1) prefetch(0);
+        pass1(0);
+    }
+    for (int64_t kr = 0; kr < nrows; ++kr) {
+        if (kr + 1 < nrows) {
+            if (PF == 1) prefetch(kr + 1);
+            if (PF == 2) prefetch(kr + 2);
+            pass1(kr + 1);
+        }
+        recv(kr);
+        pass2(kr);
+    }
+    // no CTA leaves while a peer could still write into its shared memory
+    if constexpr (CL > 1) cluster_sync_all();
+
+    // this CTA's slice of the cluster's partial row (P = clusters)
+    float *wsg = p.ws + cid * p.N + v0 * E;
+    float *wsb = p.ws + (ncl + cid) * p.N + v0 * E;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int64_t lv = (int64_t)k * NT + t;
+        if (lv >= cnt) continue;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            reinterpret_cast<float4 *>(wsg + lv * E)[h] =
+                make_float4(accg[k][4 * h], accg[k][4 * h + 1], accg[k][4 * h + 2], accg[k][4 * h + 3]);
+            if constexpr (LN)
+                reinterpret_cast<float4 *>(wsb + lv * E)[h] =
+                    make_float4(accb[k][4 * h], accb[k][4 * h + 1], accb[k][4 * h + 2], accb[k][4 * h + 3]);
+        }
+    }
+}
+
+}  // namespace gbn

@@ -277,3 +277,270 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) fwd_wtma(const FwdParams p) 
 }
 
 }  // namespace gbn
+
+namespace gbn {
+
+// ============================================================================ backward
+// Wide rows, backward: a cluster of CL CTAs shares each row, CTA `rank`
+// owning a column slice of SL = ceil(nv / CL) 16-byte vectors, cut into K
+// chunks of NT vectors; consumer thread t owns vector k * NT + t of every
+// chunk, for every row the cluster visits, so its dgamma/dbeta sums (K * E
+// floats each) stay in registers (gamma of the slice sits in shared memory,
+// read by each thread at its own vectors: registers are the limit here).  The
+// slice of each row is streamed twice through the bulk-copy ring (x and dy
+// chunks per stage): pass 1 from DRAM (evict_last) for the partial sums
+// sum g (x - mean) and sum g, which the CTA reduces and sends to every CTA
+// of the cluster through distributed shared memory; pass 2 from L2
+// (evict_first) for dx and the sums.  The order of the passes, the same for
+// producer and consumers, is P1(0), then for i = 1..n: P1(i) (if any) and
+// P2(i - 1), so each row's exchange has a whole pass of the next row to
+// complete.  Exchange slots and barriers are reused every fourth row, as in
+// bwd_wide (a peer sends row k + 4 only after receiving row k + 2 from this
+// CTA, which this CTA sends after a CTA barrier that follows its reads of
+// row k's slots).
+template <typename T, bool LN, int CL, int K>
+__global__ void __launch_bounds__(17 * 32, 1) bwd_wtma(const BwdParams p) {
+    pdl_launch_dependents();  // the column reduce waits for this grid's completion
+    constexpr int E = VecTraits<T>::E;
+    constexpr int CW = 16;
+    constexpr int NT = CW * 32;
+    constexpr int NVAL = LN ? 2 : 1;
+    constexpr int NS = 4;  // exchange slots
+    static_assert(CL >= 1 && CL <= 16, "cluster size");
+    extern __shared__ __align__(128) unsigned char smem[];
+    WtmaHeader &h = *reinterpret_cast<WtmaHeader *>(smem);
+    uint4 *gs = reinterpret_cast<uint4 *>(smem + kTmaHeaderBytes);  // gamma of the slice, [K * NT]
+    unsigned char *ring = smem + kTmaHeaderBytes + (size_t)K * NT * 16;
+    __shared__ float slot[NS][CL][NVAL];
+    __shared__ __align__(8) uint64_t xch[NS];
+    const int S = p.tc.stages;
+    const uint32_t stage_bytes = p.tc.stride;  // 2 * NT * 16: a chunk of x, then of dy
+    const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+    const int64_t cid = CL > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
+    const int64_t ncl = CL > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
+    const int64_t M = p.M, nv = p.N / E;
+    const int64_t SL = (nv + CL - 1) / CL;
+    const int64_t v0 = rank * SL;
+    const int64_t cnt = nv - v0 < SL ? (nv - v0 > 0 ? nv - v0 : 0) : SL;  // this CTA's vectors
+    const int64_t nrows = cid < M ? (M - cid + ncl - 1) / ncl : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort_flag = &h.abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&h.full[s], 1);
+            mbar_init(&h.empty[s], CW);
+        }
+        if (CL > 1)
+            for (int j = 0; j < NS; ++j) mbar_init(&xch[j], CL);
+        h.abort = 0;
+        fence_mbar_init();
+    }
+    // every CTA's barriers exist before any peer arrives on them
+    if constexpr (CL > 1) cluster_sync_all();
+    else __syncthreads();
+
+    // jobs: step i < nrows: pass 1 of row i (K jobs); step i >= 1: pass 2 of row i - 1 (K jobs)
+    const int64_t njobs = nrows > 0 ? 2 * nrows * K : 0;
+    auto job = [&](int64_t j, int64_t &row, int &pass, int &k) {
+        // jobs of step 0: K (pass 1 only); of steps 1..nrows-1: 2K; of step nrows: K
+        if (j < K) {
+            row = 0, pass = 1, k = (int)j;
+            return;
+        }
+        const int64_t q = j - K;
+        const int64_t step = 1 + q / (2 * K);
+        const int r = (int)(q % (2 * K));
+        if (step < nrows && r < K) {
+            row = step, pass = 1, k = r;
+        } else {
+            row = step - 1, pass = 2, k = step < nrows ? r - K : r;
+        }
+    };
+
+    if (warp == CW) {
+        // ---- producer
+        if (lane == 0) {
+            const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
+            int64_t issued = 0;
+            for (int64_t j = 0; j < njobs; ++j, ++issued) {
+                const int s = (int)(j % S);
+                if (j >= S) mbar_wait_bounded(&h.empty[s], (uint32_t)(((j / S) - 1) & 1), abort_flag, p.tc.fault);
+                if (*abort_flag) break;
+                int64_t i;
+                int pass, k;
+                job(j, i, pass, k);
+                const int64_t row = cid + i * ncl;
+                const int64_t c0 = (int64_t)k * NT;  // first vector of the chunk within the slice
+                const int64_t vn = cnt - c0 < NT ? (cnt - c0 > 0 ? cnt - c0 : 0) : NT;
+                const uint32_t bytes = (uint32_t)vn * 16u;
+                unsigned char *dst = ring + (size_t)s * stage_bytes;
+                mbar_arrive_expect_tx(&h.full[s], 2 * bytes);
+                if (bytes > 0) {
+                    const size_t off = ((size_t)row * (size_t)nv + (size_t)(v0 + c0)) * 16;
+                    const uint64_t pol = pass == 1 ? keep : drop;
+                    bulk_g2s_hint(dst, static_cast<const unsigned char *>(p.x) + off, bytes, &h.full[s], pol);
+                    bulk_g2s_hint(dst + NT * 16, static_cast<const unsigned char *>(p.dy) + off, bytes, &h.full[s],
+                                  pol);
+                }
+            }
+            if (*abort_flag) {
+                int zero = 0;
+                for (int64_t j = issued > S ? issued - S : 0; j < issued; ++j)
+                    mbar_wait_bounded(&h.full[j % S], (uint32_t)((j / S) & 1),
+                                      reinterpret_cast<volatile int *>(&zero), nullptr);
+            }
+        }
+        return;
+    }
+
+    // ---- consumers
+    const int t = threadIdx.x;
+    const float n = (float)p.N;
+    float accg[K][E], accb[LN ? K : 1][E];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int64_t lv = (int64_t)k * NT + t;
+        gs[lv] = lv < cnt ? param_vec<T>(p.gamma, v0 + lv, true) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            accg[k][e] = 0.f;
+            if constexpr (LN) accb[k][e] = 0.f;
+        }
+    }
+    named_sync(1, NT);
+    const uint64_t drop = l2_policy_drop();
+    int parity = 0;
+    int64_t j = 0;
+    float c1s[NS], c2s[NS];  // (c1, c2) of the rows in the exchange slots (single-CTA clusters)
+
+    auto pass1 = [&](int64_t i) {
+        const int64_t row = cid + i * ncl;
+        const float rstd = __ldg(p.rstd + row);
+        const float mean = LN ? __ldg(p.mean + row) : 0.f;
+        float v[NVAL];
+#pragma unroll
+        for (int q = 0; q < NVAL; ++q) v[q] = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; ++k, ++j) {
+            const int s = (int)(j % S);
+            mbar_wait_bounded(&h.full[s], (uint32_t)((j / S) & 1), abort_flag, p.tc.fault);
+            const uint4 *st = reinterpret_cast<const uint4 *>(ring + (size_t)s * stage_bytes);
+            const int64_t lv = (int64_t)k * NT + t;
+            if (lv < cnt) {
+                const uint4 xq = lds128(st + t), dq = lds128(st + NT + t), gq = lds128(gs + lv);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float gg = vget<T>(dq, e) * vget<T>(gq, e);
+                    v[0] += gg * (vget<T>(xq, e) - mean);
+                    if constexpr (LN) v[NVAL - 1] += gg;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&h.empty[s]);
+        }
+        v[0] *= rstd;  // sum g xhat = rstd sum g (x - mean)
+        // CTA reduction over the NT consumers (identical bits in all)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+            for (int q = 0; q < NVAL; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+        if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < NVAL; ++q) h.red[parity][q][warp] = v[q];
+        }
+        named_sync(1, NT);
+#pragma unroll
+        for (int q = 0; q < NVAL; ++q) {
+            float sum = 0.f;
+#pragma unroll 4
+            for (int w = 0; w < CW; ++w) sum += h.red[parity][q][w];
+            v[q] = sum;
+        }
+        parity ^= 1;
+        const int sp = (int)(i % NS);
+        if constexpr (CL > 1) {
+            if (t < CL) {
+                const uint32_t dst = map_to_rank(smem_u32(&slot[sp][rank][0]), (uint32_t)t);
+#pragma unroll
+                for (int q = 0; q < NVAL; ++q) st_cluster_f32(dst + 4u * q, v[q]);
+                mbar_arrive_remote(map_to_rank(smem_u32(&xch[sp]), (uint32_t)t));
+            }
+        } else {
+            c2s[sp] = v[0] / n;
+            c1s[sp] = LN ? v[NVAL - 1] / n : 0.f;
+        }
+    };
+
+    auto pass2 = [&](int64_t i) {
+        const int64_t row = cid + i * ncl;
+        const float rstd = __ldg(p.rstd + row);
+        const float mean = LN ? __ldg(p.mean + row) : 0.f;
+        const int sp = (int)(i % NS);
+        float c1 = 0.f, c2 = 0.f;
+        if constexpr (CL > 1) {
+            mbar_wait_cluster_bounded(&xch[sp], (uint32_t)((i / NS) & 1), abort_flag, p.tc.fault);
+            float s2 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < CL; ++c) {
+                s2 += slot[sp][c][0];
+                if constexpr (LN) s1 += slot[sp][c][NVAL - 1];
+            }
+            c2 = s2 / n;
+            c1 = LN ? s1 / n : 0.f;
+        } else {
+            c2 = c2s[sp];
+            c1 = c1s[sp];
+        }
+        const float rc1 = rstd * c1, rc2 = rstd * c2;
+        uint4 *dxr = static_cast<uint4 *>(p.dx) + row * nv + v0;
+#pragma unroll
+        for (int k = 0; k < K; ++k, ++j) {
+            const int s = (int)(j % S);
+            mbar_wait_bounded(&h.full[s], (uint32_t)((j / S) & 1), abort_flag, p.tc.fault);
+            const uint4 *st = reinterpret_cast<const uint4 *>(ring + (size_t)s * stage_bytes);
+            const int64_t lv = (int64_t)k * NT + t;
+            if (lv < cnt) {
+                const uint4 xq = lds128(st + t), dq = lds128(st + NT + t), gq = lds128(gs + lv);
+                float o[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float xh = (vget<T>(xq, e) - mean) * rstd;
+                    const float dyv = vget<T>(dq, e);
+                    o[e] = fmaf(-rc2, xh, fmaf(rstd, dyv * vget<T>(gq, e), -rc1));
+                    accg[k][e] += dyv * xh;
+                    if constexpr (LN) accb[k][e] += dyv;
+                }
+                st_l2hint(dxr + lv, vpack<T>(o), drop);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&h.empty[s]);
+        }
+    };
+
+    for (int64_t i = 0; i <= nrows; ++i) {
+        if (i < nrows) pass1(i);
+        if (i >= 1) pass2(i - 1);
+    }
+    // no CTA leaves while a peer could still write into its shared memory
+    if constexpr (CL > 1) cluster_sync_all();
+
+    // this CTA's slice of the cluster's partial row (P = clusters)
+    float *wsg = p.ws + cid * p.N + v0 * E;
+    float *wsb = p.ws + (ncl + cid) * p.N + v0 * E;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int64_t lv = (int64_t)k * NT + t;
+        if (lv >= cnt) continue;
+#pragma unroll
+        for (int hh = 0; hh < E / 4; ++hh) {
+            reinterpret_cast<float4 *>(wsg + lv * E)[hh] =
+                make_float4(accg[k][4 * hh], accg[k][4 * hh + 1], accg[k][4 * hh + 2], accg[k][4 * hh + 3]);
+            if constexpr (LN)
+                reinterpret_cast<float4 *>(wsb + lv * E)[hh] =
+                    make_float4(accb[k][4 * hh], accb[k][4 * hh + 1], accb[k][4 * hh + 2], accb[k][4 * hh + 3]);
+        }
+    }
+}
+
+}  // namespace gbn

@@ -61,7 +61,7 @@ def run_ex(op, inp, pad=0, y_dtype=None, residual=None, dres=None, store_h=True)
     if h is not None:
         out["h"] = h.cpu()
     vf = ex_variant(N, _vec(x, r, h, y) and gam.data_ptr() % 16 == 0)
-    vb = ex_variant(N, _vec(dy, xb, dr, dx))
+    vb = ex_variant(N, _vec(dy, xb, dr, dx), "bwd")
     return out, (vf, vb)
 
 
@@ -158,8 +158,7 @@ def test_optional_parameters_and_empty(op):
     out = {"y": y.cpu(), "rstd": rstd.cpu(), "dx": dx.cpu(), "dgamma": dg.cpu()}
     if ln:
         out.update(mean=mean.cpu(), dbeta=db.cpu())
-    v = ex_variant(N, True)
-    compare(op, inp, out, variants=(v, v)).assert_ok()
+    compare(op, inp, out, variants=(ex_variant(N, True), ex_variant(N, True, "bwd"))).assert_ok()
     e = torch.empty(0, N, device="cuda", dtype=torch.bfloat16)
     dge = torch.full((N,), 5.0, device="cuda")
     _, _, me, re_ = g.norm_fwd_ex(ln, e, None, None, inp.eps)

@@ -58,6 +58,14 @@ def _geom(name):
     if m:
         nt, u, _, _, _ = (int(v) for v in m.groups())
         return ("wide", nt, u, 1)
+    m = re.fullmatch(r"bwtma(\d+)x(\d+)", name)
+    if m:
+        cl, k = (int(v) for v in m.groups())
+        return ("bwtma", 512, k, cl)
+    m = re.fullmatch(r"bwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)", name)
+    if m:
+        nt, k, cl, _, _ = (int(v) for v in m.groups())
+        return ("bwtma", nt, k, cl)
     m = re.fullmatch(r"wtma(\d+)x(\d+)", name)
     if m:
         cw, u = (int(v) for v in m.groups())
@@ -111,6 +119,12 @@ def test_forced_variant(op, direction, dtype, variant):
     geo = _geom(variant)
     if geo is None:  # the element-wise variant: odd N
         shapes = [(67, 1), (67, 77), (5, 3001)]
+    elif geo[0] == "bwtma":
+        # column slices of CL CTAs, K chunks of 512 vectors each: full slices,
+        # one vector short, a ragged last chunk, and CTAs left without columns
+        nt, k, cl = geo[1], geo[2], geo[3]
+        cap = cl * k * nt * E
+        shapes = [(9, cap), (9, cap - E), (7, cap // 2 + 3 * E), (5, cl * 3 * E), (3, (cl - 1) * E)]
     elif geo[0] == "wide":
         # any row length (per CTA of the cluster): two full load batches per
         # thread, one vector short of that, a slice where only part of the CTA
@@ -136,13 +150,15 @@ def test_forced_variant(op, direction, dtype, variant):
         shapes = [(M, cap), (M, cap - E)]
     try:
         g.force_variant(op == "ln", direction, dtype, variant)
+        if geo is not None and geo[0] == "bwtma":
+            shapes = [(m, n) for m, n in shapes if n >= E]
         if geo is not None and geo[0] == "wide" and direction == 1:
             # the widest of the rows above whose slice sums fit
             full = shapes[0][1]
             while full > geo[3] * E and g.variant_name(op == "ln", 1, 9, full, dtype) != variant:
                 full //= 2
             shapes = [(9, full), (9, full - E)] + shapes[2:]
-        if geo is not None and geo[0] != "wide" and geo[5]:
+        if geo is not None and geo[0] not in ("wide", "bwtma") and geo[5]:
             # A staged variant may hold fewer elements than its register
             # capacity when gamma/beta and two stages must fit in shared
             # memory: take the widest row it serves, at least a quarter of it.
@@ -474,3 +490,28 @@ def test_wide_ring_wraps(op, variant, limit):
     finally:
         g.set_grid_limit(0)
         g.force_variant(op == "ln", 0, "bf16", None)
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("variant,N", [("bwtma8x4", 131072), ("bwtma4x4", 65536 - 24), ("bwtma8x2", 40000),
+                                       ("bwr512k4c8p1m1", 131072), ("bwr512k8c4p1m1", 131072 - 24),
+                                       ("bwr256k4c16p1m2", 131072), ("bwr256k8c8p1m2", 131072 - 24),
+                                       ("bwr256k4c2p1m2", 3000), ("bwr512k4c1p1m1", 16384)])
+@pytest.mark.parametrize("limit", [1, 3])
+def test_wide_backward_ring_wraps(op, variant, N, limit):
+    """The bulk-copy wide backward under a grid cap (in clusters): each cluster
+    walks many rows, so the ring stages, the pass order (pass 1 one row ahead
+    of pass 2) and the four exchange slots go through many phases."""
+    import rmsnorm_norm_fwd_gb300 as g
+    cl = int(re.match(r"bwtma(\d+)x", variant).group(1)) if variant.startswith("bwtma") else \
+        int(re.search(r"c(\d+)p", variant).group(1))
+    M = 23
+    try:
+        g.force_variant(op == "ln", 1, "bf16", variant)
+        g.set_grid_limit(limit * cl)
+        assert g.variant_name(op == "ln", 1, M, N, "bf16") == variant
+        rep, _, _ = run_case(op, "bf16", M, N)
+        rep.assert_ok()
+    finally:
+        g.set_grid_limit(0)
+        g.force_variant(op == "ln", 1, "bf16", None)

@@ -103,14 +103,15 @@ def test_sample_includes_scaled_rows():
 
 
 def test_general_form_geometries_match_the_library():
-    """parity_util's list of general-form geometries (which the tests use to
-    name the kernel that ran) is the one compiled into the library."""
+    """parity_util's lists of general-form geometries (which the tests use to
+    name the kernel that ran) are the ones compiled into the library."""
     import os
     import re
     from parity_util import EX_GEOMS
     src = open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "rmsnorm_norm_fwd_gb300", "csrc",
                             "inst_ex.cu")).read()
-    block = src[src.index("#define GBN_EX_GEOMS(X)"):]
-    block = block[:block.index("\n\n")]
-    geoms = tuple(tuple(int(v) for v in m) for m in re.findall(r"X\((\d+), (\d+), (\d+)\)", block))
-    assert geoms == EX_GEOMS
+    for macro, d in (("GBN_EXF_GEOMS", "fwd"), ("GBN_EXB_GEOMS", "bwd")):
+        block = src[src.index(f"#define {macro}(X)"):]
+        block = block[:block.index("\n\n")]
+        geoms = tuple(tuple(int(v) for v in m) for m in re.findall(r"X\((\d+), (\d+), (\d+), \d+\)", block))
+        assert geoms == EX_GEOMS[d], d
