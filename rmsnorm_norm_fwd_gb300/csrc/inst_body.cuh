@@ -135,11 +135,11 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
             VecTraits<GBN_T>::E, 1, 0},
 #define GBN_BWT_RMS(CL, K) GBN_BWTMA(false, CL, K)
 #define GBN_BWT_LN(CL, K) GBN_BWTMA(true, CL, K)
-#define GBN_WIDER(LN, NT, K, CL, PF, MINB)                                                     \
-    Variant{GBN_WIDER_VNAME(NT, K, CL, PF, MINB), (const void *)&bwd_wider<GBN_T, LN, NT, K, CL, PF, MINB>, kWideR, \
-            NT, K, 1, CL, NT, VecTraits<GBN_T>::E, MINB, 0},
-#define GBN_WR_RMS(NT, K, CL, PF, MINB) GBN_WIDER(false, NT, K, CL, PF, MINB)
-#define GBN_WR_LN(NT, K, CL, PF, MINB) GBN_WIDER(true, NT, K, CL, PF, MINB)
+#define GBN_WIDER(LN, NT, K, CL, PF, MINB, F)                                                  \
+    Variant{GBN_WIDER_VNAME(NT, K, CL, PF, MINB, F), (const void *)&bwd_wider<GBN_T, LN, NT, K, CL, PF, MINB, F>, \
+            kWideR, NT, K, 1, CL, NT, VecTraits<GBN_T>::E, MINB, 0},
+#define GBN_WR_RMS(NT, K, CL, PF, MINB, F) GBN_WIDER(false, NT, K, CL, PF, MINB, F)
+#define GBN_WR_LN(NT, K, CL, PF, MINB, F) GBN_WIDER(true, NT, K, CL, PF, MINB, F)
 static const Variant rms_variants[] = {
     GBN_WIDER_BWD_GEOMS(GBN_WR_RMS)
     GBN_BWTMA_BWD_GEOMS(GBN_BWT_RMS)

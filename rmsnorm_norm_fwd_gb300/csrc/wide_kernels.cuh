@@ -656,7 +656,10 @@ namespace gbn {
 // MINB: CTAs per SM of the launch bound (registers 65536 / (NT * MINB)); two
 // CTAs of a cluster on one SM let one CTA's exchange or memory wait overlap
 // the other's work.
-template <typename T, bool LN, int NT, int K, int CL, int PF, int MINB>
+// FUSE: 1 pass 1 of row j in the same sweep as pass 2 of row j - 2 (both
+// rows' loads in flight together); 0 pass 1 of row k + 1, the exchange of row
+// k, then pass 2 of row k.
+template <typename T, bool LN, int NT, int K, int CL, int PF, int MINB, int FUSE>
 __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     pdl_launch_dependents();  // the column reduce waits for this grid's completion
     constexpr int E = VecTraits<T>::E;
@@ -664,7 +667,7 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     constexpr int W = NT / 32;
     constexpr int NVAL = LN ? 2 : 1;
     constexpr int NS = 4;
-    constexpr int KB = K < 4 ? K : 4;  // vectors per tensor in flight per thread
+    constexpr int KB = FUSE ? (K < 2 ? K : 2) : (K < 4 ? K : 4);  // vectors per tensor per batch
     static_assert(NT % 32 == 0 && NT <= 1024 && CL >= 1 && CL <= 16 && K % KB == 0, "shape");
     extern __shared__ __align__(16) float4 gsm[];  // gamma of the slice, [H][K * NT] float4
     __shared__ float red[2][NVAL][W];
@@ -734,37 +737,9 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     int parity = 0;
     float cst[3][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // (c1, c2) of row k at [k % 3]
 
-    // pass 1 of row k: this thread's sum g (x - mean) (and sum g), then the
-    // CTA's, sent to the cluster (or, alone, turned into c1, c2)
-    auto pass1 = [&](int64_t kr) {
-        const float rstd = __ldg(p.rstd + row_of(kr));
-        const float mean = LN ? __ldg(p.mean + row_of(kr)) : 0.f;
-        const uint4 *xr = row_x(kr), *dr = row_dy(kr);
-        float v[NVAL];
-        float a2[2] = {0.f, 0.f}, a1[2] = {0.f, 0.f};
-#pragma unroll
-        for (int kb = 0; kb < K; kb += KB) {
-            uint4 qx[KB], qd[KB];
-#pragma unroll
-            for (int i = 0; i < KB; ++i) {
-                const int64_t lv = (int64_t)(kb + i) * NT + t;
-                qx[i] = lv < cnt ? ld_l2hint(xr + lv, keep) : make_uint4(0, 0, 0, 0);
-                qd[i] = lv < cnt ? ld_l2hint(dr + lv, keep) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int i = 0; i < KB; ++i) {
-                float g[E];
-                gam(kb + i, g);
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float gg = vget<T>(qd[i], e) * g[e];  // zero past the slice
-                    a2[e & 1] += gg * (vget<T>(qx[i], e) - mean);
-                    if constexpr (LN) a1[e & 1] += gg;
-                }
-            }
-        }
-        v[0] = (a2[0] + a2[1]) * rstd;  // sum g xhat = rstd sum g (x - mean)
-        if constexpr (LN) v[NVAL - 1] = a1[0] + a1[1];
+    // The CTA's sum of this thread's pass-1 partials (identical bits in every
+    // thread), sent to the cluster (or, alone, turned into c1, c2).
+    auto finish1 = [&](int64_t kr, float (&v)[NVAL]) {
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1)
 #pragma unroll
@@ -810,53 +785,94 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
             cst[kr % 3][1] = s[0] / n;
         }
     };
-    // pass 2 of row k: dx and this thread's dgamma/dbeta sums
-    auto pass2 = [&](int64_t kr) {
-        const float rstd = __ldg(p.rstd + row_of(kr));
-        const float mean = LN ? __ldg(p.mean + row_of(kr)) : 0.f;
-        const float rc1 = rstd * cst[kr % 3][0], rc2 = rstd * cst[kr % 3][1];
-        const uint4 *xr = row_x(kr), *dr = row_dy(kr);
-        uint4 *dxr = static_cast<uint4 *>(p.dx) + row_of(kr) * nv + v0;
+    // One sweep over the slice: pass 1 of row k1 (if has1: this thread's
+    // partials into v) and pass 2 of row k2 (if has2: dx and the sums), their
+    // loads in the same batches so that both rows' latencies overlap.  The
+    // branches are uniform over the CTA.
+    auto sweep = [&](bool has1, int64_t k1, bool has2, int64_t k2, float (&v)[NVAL]) {
+        const float rstd1 = has1 ? __ldg(p.rstd + row_of(k1)) : 0.f;
+        const float mean1 = (LN && has1) ? __ldg(p.mean + row_of(k1)) : 0.f;
+        const float rstd2 = has2 ? __ldg(p.rstd + row_of(k2)) : 0.f;
+        const float mean2 = (LN && has2) ? __ldg(p.mean + row_of(k2)) : 0.f;
+        const float rc1 = rstd2 * cst[k2 % 3][0], rc2 = rstd2 * cst[k2 % 3][1];
+        const uint4 *x1 = row_x(has1 ? k1 : 0), *d1 = row_dy(has1 ? k1 : 0);
+        const uint4 *x2 = row_x(has2 ? k2 : 0), *d2 = row_dy(has2 ? k2 : 0);
+        uint4 *dx2 = static_cast<uint4 *>(p.dx) + row_of(has2 ? k2 : 0) * nv + v0;
+        float a2[2] = {0.f, 0.f}, a1[2] = {0.f, 0.f};
 #pragma unroll
         for (int kb = 0; kb < K; kb += KB) {
-            uint4 qx[KB], qd[KB];
+            uint4 px[KB], pd[KB], qx[KB], qd[KB];
 #pragma unroll
             for (int i = 0; i < KB; ++i) {
                 const int64_t lv = (int64_t)(kb + i) * NT + t;
-                qx[i] = lv < cnt ? ld_l2hint(xr + lv, drop) : make_uint4(0, 0, 0, 0);
-                qd[i] = lv < cnt ? ld_l2hint(dr + lv, drop) : make_uint4(0, 0, 0, 0);
+                const bool ok = lv < cnt;
+                px[i] = (has1 && ok) ? ld_l2hint(x1 + lv, keep) : make_uint4(0, 0, 0, 0);
+                pd[i] = (has1 && ok) ? ld_l2hint(d1 + lv, keep) : make_uint4(0, 0, 0, 0);
+                qx[i] = (has2 && ok) ? ld_l2hint(x2 + lv, drop) : make_uint4(0, 0, 0, 0);
+                qd[i] = (has2 && ok) ? ld_l2hint(d2 + lv, drop) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int i = 0; i < KB; ++i) {
                 const int64_t lv = (int64_t)(kb + i) * NT + t;
-                float g[E], o[E];
+                float g[E];
                 gam(kb + i, g);
+                if (has2) {
+                    float o[E];
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float xh = (vget<T>(qx[i], e) - mean) * rstd;
-                    const float dyv = vget<T>(qd[i], e);
-                    o[e] = fmaf(-rc2, xh, fmaf(rstd, dyv * g[e], -rc1));
-                    accg[kb + i][e] += dyv * xh;  // zero past the slice (dy = 0)
-                    if constexpr (LN) accb[kb + i][e] += dyv;
+                    for (int e = 0; e < E; ++e) {
+                        const float xh = (vget<T>(qx[i], e) - mean2) * rstd2;
+                        const float dyv = vget<T>(qd[i], e);
+                        o[e] = fmaf(-rc2, xh, fmaf(rstd2, dyv * g[e], -rc1));
+                        accg[kb + i][e] += dyv * xh;  // zero past the slice (dy = 0)
+                        if constexpr (LN) accb[kb + i][e] += dyv;
+                    }
+                    if (lv < cnt) st_l2hint(dx2 + lv, vpack<T>(o), drop);
                 }
-                if (lv < cnt) st_l2hint(dxr + lv, vpack<T>(o), drop);
+                if (has1) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float gg = vget<T>(pd[i], e) * g[e];  // zero past the slice
+                        a2[e & 1] += gg * (vget<T>(px[i], e) - mean1);
+                        if constexpr (LN) a1[e & 1] += gg;
+                    }
+                }
             }
         }
+        v[0] = (a2[0] + a2[1]) * rstd1;  // sum g xhat = rstd sum g (x - mean)
+        if constexpr (LN) v[NVAL - 1] = a1[0] + a1[1];
     };
 
-    if (PF == 2) prefetch(0);
-    if (nrows > 0) {
-        if (PF == 1) prefetch(0);
-        pass1(0);
-    }
-    for (int64_t kr = 0; kr < nrows; ++kr) {
-        if (kr + 1 < nrows) {
-            if (PF == 1) prefetch(kr + 1);
-            if (PF == 2) prefetch(kr + 2);
-            pass1(kr + 1);
+    float v[NVAL];
+    if constexpr (FUSE) {
+        // step j: pass 1 of row j with pass 2 of row j - 2, then row j's
+        // partials go out and row j - 1's come in (a whole sweep after they
+        // were sent)
+        if (PF == 2) prefetch(0);
+        for (int64_t j = 0; j < nrows + 2; ++j) {
+            const bool has1 = j < nrows, has2 = j >= 2;
+            if (PF >= 1) prefetch(j + (PF == 2 ? 1 : 0));
+            sweep(has1, j, has2, j - 2, v);
+            if (has1) finish1(j, v);
+            if (j >= 1 && j - 1 < nrows) recv(j - 1);
         }
-        recv(kr);
-        pass2(kr);
+    } else {
+        // pass 1 of row k + 1, then row k's exchange, then pass 2 of row k
+        if (PF == 2) prefetch(0);
+        if (nrows > 0) {
+            if (PF == 1) prefetch(0);
+            sweep(true, 0, false, 0, v);
+            finish1(0, v);
+        }
+        for (int64_t kr = 0; kr < nrows; ++kr) {
+            if (kr + 1 < nrows) {
+                if (PF == 1) prefetch(kr + 1);
+                if (PF == 2) prefetch(kr + 2);
+                sweep(true, kr + 1, false, 0, v);
+                finish1(kr + 1, v);
+            }
+            recv(kr);
+            sweep(false, 0, true, kr, v);
+        }
     }
     // no CTA leaves while a peer could still write into its shared memory
     if constexpr (CL > 1) cluster_sync_all();

@@ -62,9 +62,9 @@ def _geom(name):
     if m:
         cl, k = (int(v) for v in m.groups())
         return ("bwtma", 512, k, cl)
-    m = re.fullmatch(r"bwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)", name)
+    m = re.fullmatch(r"bwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)", name)
     if m:
-        nt, k, cl, _, _ = (int(v) for v in m.groups())
+        nt, k, cl, _, _, _ = (int(v) for v in m.groups())
         return ("bwtma", nt, k, cl)
     m = re.fullmatch(r"wtma(\d+)x(\d+)", name)
     if m:
@@ -494,9 +494,10 @@ def test_wide_ring_wraps(op, variant, limit):
 
 @pytest.mark.parametrize("op", ["rms", "ln"])
 @pytest.mark.parametrize("variant,N", [("bwtma8x4", 131072), ("bwtma4x4", 65536 - 24), ("bwtma8x2", 40000),
-                                       ("bwr512k4c8p1m1", 131072), ("bwr512k8c4p1m1", 131072 - 24),
-                                       ("bwr256k4c16p1m2", 131072), ("bwr256k8c8p1m2", 131072 - 24),
-                                       ("bwr256k4c2p1m2", 3000), ("bwr512k4c1p1m1", 16384)])
+                                       ("bwr512k4c8p1m1f1", 131072), ("bwr512k8c4p1m1f0", 131072 - 24),
+                                       ("bwr256k4c16p1m2f1", 131072), ("bwr256k8c8p1m2f0", 131072 - 24),
+                                       ("bwr256k4c2p1m2f1", 3000), ("bwr512k4c1p1m1f1", 16384),
+                                       ("bwr512k4c1p1m1f0", 16384)])
 @pytest.mark.parametrize("limit", [1, 3])
 def test_wide_backward_ring_wraps(op, variant, N, limit):
     """The bulk-copy wide backward under a grid cap (in clusters): each cluster
