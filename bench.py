@@ -656,7 +656,8 @@ def run_ex_families(gb, dev, stream, flush_l2, steps=5, warmup=3):
             ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
             nb = ex_bytes(op, d, m, n, ESIZE[xd], ESIZE[pd], ESIZE[yd], residual)
             gbs = nb / (ms * 1e-3) / 1e9
-            res[d] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "ms": round(ms, 5)}
+            res[d] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "ms": round(ms, 5),
+                      "variant": gb.ex_last_variant(0 if d == "fwd" else 1)}
         out[name] = res
         del inp, x, dy, r, dres, y, dx, h, wsb
     torch.cuda.empty_cache()

@@ -199,8 +199,11 @@ int layernorm_bwd(const void *dy, const void *x, const void *gamma, const float 
  * overlap of the spans [p, p + ((M - 1) * ld + N) * size) is rejected, and dx
  * may not be x.  With every row 16-byte aligned (base and stride), N a
  * multiple of 8 and 16-byte-aligned gamma / beta, rows move as 16-byte
- * vectors; anything else takes a correct element-wise path.  Status codes,
- * ownership, streams and threading as above.
+ * vectors: for rows up to 16384 elements they are staged through a
+ * shared-memory ring by bulk asynchronous copies (in the backward only when
+ * rstd, and mean for LayerNorm, are 16-byte aligned too), else read straight
+ * into registers; anything else takes a correct element-wise path.  Status
+ * codes, ownership, streams and threading as above.
  */
 int norm_fwd_ex(int is_layernorm, int64_t M, int64_t N, float eps, const void *x, int64_t ldx, int x_dtype,
                 const void *residual, int64_t ldr, void *h, int64_t ldh, const void *gamma, const void *beta,
@@ -275,6 +278,26 @@ int gbnorm_force_variant(int is_layernorm, int dir, int dtype, const char *name)
  */
 int gbnorm_variant_count(int is_layernorm, int dir, int dtype);
 const char *gbnorm_variant_at(int is_layernorm, int dir, int dtype, int index);
+
+/*
+ * The general form's kernels (norm_fwd_ex / norm_bwd_ex), for tests and
+ * tuning.  gbnorm_ex_variant_count gives how many there are for
+ * (is_layernorm, dir), the last being the element-wise kernel "exe";
+ * gbnorm_ex_variant_at the index-th name (static string; NULL if out of
+ * range).  gbnorm_ex_force_variant makes every later general-form call of
+ * (is_layernorm, dir) in this process launch the named kernel whenever it can
+ * serve the call (otherwise the usual choice is made); NULL or "" removes the
+ * override; GBNORM_ERR_INVALID_ARG for an unknown name.  Not to be changed
+ * while another host thread is calling the library.
+ * gbnorm_ex_last_variant writes into buf (NUL-terminated, at most len bytes)
+ * the name of the kernel that the calling thread's last norm_fwd_ex (dir 0)
+ * or norm_bwd_ex (dir 1) launched, "" if that call launched none (M = 0 or
+ * an error before the launch) or there was no such call.
+ */
+int gbnorm_ex_variant_count(int is_layernorm, int dir);
+const char *gbnorm_ex_variant_at(int is_layernorm, int dir, int index);
+int gbnorm_ex_force_variant(int is_layernorm, int dir, const char *name);
+int gbnorm_ex_last_variant(int dir, char *buf, size_t len);
 
 /*
  * Caps the persistent grid of every later launch at max_ctas CTAs (0 removes

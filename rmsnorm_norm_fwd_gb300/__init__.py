@@ -9,7 +9,8 @@ the ops without the built library raises ImportError.
 
 _OPS = ("rmsnorm_fwd", "layernorm_fwd", "rmsnorm_bwd", "layernorm_bwd", "norm_bwd_workspace_size",
         "norm_fwd_ex", "norm_bwd_ex", "norm_bwd_ex_workspace_size",
-        "variant_name", "force_variant", "variants", "read_fault", "set_grid_limit", "GbnormError", "lib")
+        "variant_name", "force_variant", "variants", "ex_variants", "ex_force_variant", "ex_last_variant",
+        "read_fault", "set_grid_limit", "GbnormError", "lib")
 
 __all__ = list(_OPS)
 

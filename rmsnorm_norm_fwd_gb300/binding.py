@@ -46,10 +46,16 @@ lib.gbnorm_variant_at.argtypes = [_int, _int, _int, _int]
 lib.gbnorm_variant_at.restype = ctypes.c_char_p
 lib.gbnorm_read_fault.argtypes = [_int, ctypes.POINTER(ctypes.c_int)]
 lib.gbnorm_set_grid_limit.argtypes = [_int]
+lib.gbnorm_ex_variant_count.argtypes = [_int, _int]
+lib.gbnorm_ex_variant_at.argtypes = [_int, _int, _int]
+lib.gbnorm_ex_variant_at.restype = ctypes.c_char_p
+lib.gbnorm_ex_force_variant.argtypes = [_int, _int, ctypes.c_char_p]
+lib.gbnorm_ex_last_variant.argtypes = [_int, ctypes.c_char_p, _sz]
 for _fn in ("rmsnorm_fwd", "layernorm_fwd", "rmsnorm_bwd", "layernorm_bwd", "norm_fwd_ex", "norm_bwd_ex",
             "gbnorm_variant_name",
             "gbnorm_force_variant", "gbnorm_variant_count", "gbnorm_read_fault",
-            "gbnorm_set_grid_limit"):
+            "gbnorm_set_grid_limit", "gbnorm_ex_variant_count", "gbnorm_ex_force_variant",
+            "gbnorm_ex_last_variant"):
     getattr(lib, _fn).restype = _int
 
 GBNORM_OK = 0
@@ -287,6 +293,25 @@ def variants(is_layernorm: bool, direction: int, dtype) -> list[str]:
     code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else DTYPE_NAME.get(dtype, dtype)
     n = lib.gbnorm_variant_count(int(bool(is_layernorm)), direction, code)
     return [lib.gbnorm_variant_at(int(bool(is_layernorm)), direction, code, i).decode() for i in range(n)]
+
+
+def ex_variants(is_layernorm: bool, direction: int) -> list[str]:
+    """Names of the general form's kernels for (op, direction); the last is "exe"."""
+    n = lib.gbnorm_ex_variant_count(int(bool(is_layernorm)), direction)
+    return [lib.gbnorm_ex_variant_at(int(bool(is_layernorm)), direction, i).decode() for i in range(n)]
+
+
+def ex_force_variant(is_layernorm: bool, direction: int, name: str | None) -> None:
+    """Make later general-form calls launch `name` where it can serve them (None: no override)."""
+    _check("gbnorm_ex_force_variant", lib.gbnorm_ex_force_variant(
+        int(bool(is_layernorm)), direction, None if not name else name.encode()))
+
+
+def ex_last_variant(direction: int) -> str:
+    """The kernel this thread's last norm_fwd_ex (0) / norm_bwd_ex (1) launched ("" for none)."""
+    buf = ctypes.create_string_buffer(64)
+    _check("gbnorm_ex_last_variant", lib.gbnorm_ex_last_variant(direction, buf, 64))
+    return buf.value.decode()
 
 
 def read_fault(reset: bool = True) -> int:

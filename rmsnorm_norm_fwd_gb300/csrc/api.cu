@@ -789,13 +789,33 @@ struct ExPlan {
     int64_t grid;
     size_t dyn;
     int cta;
+    TileCfg tc;        // ring kernels
+    const char *name;
 };
 
-// Per (device, is_ln, dir, geometry; the last slot for the element-wise
-// kernel): the dynamic shared-memory limit raised, and the last (shared
+// A general-form call as the planner sees it.
+struct ExCall {
+    int is_ln, dir;
+    int64_t M, N;
+    int xdt, ydt, pdt;
+    bool extra;    // residual rows (forward) or dres rows (backward)
+    bool vec;      // every row tensor allows 16-byte vectors, gamma (and beta) 16-byte aligned
+    bool stats16;  // backward: rstd (and mean) 16-byte aligned
+    bool no_ring;  // plan as if the ring kernels did not exist (workspace bound)
+};
+
+// Slots per (device, is_ln, dir): one per table entry, the last one for the
+// element-wise kernel.
+constexpr int kExSlots = 33;
+// Per slot: the dynamic shared-memory limit raised, and the last (shared
 // memory, occupancy) pair.
-std::atomic<int> g_ex_smem_set[kMaxDev][2][2][17];
-std::atomic<uint64_t> g_ex_occ[kMaxDev][2][2][17];
+std::atomic<int> g_ex_smem_set[kMaxDev][2][2][kExSlots];
+std::atomic<uint64_t> g_ex_occ[kMaxDev][2][2][kExSlots];
+// Forced general-form kernel per (is_ln, dir): table index + 1 (count + 1:
+// the element-wise kernel), 0 for none.
+std::atomic<int> g_ex_force[2][2];
+// Name of the kernel the calling thread's last general-form call launched.
+thread_local const char *g_ex_last[2] = {"", ""};
 
 int ex_occupancy(int dev, int is_ln, int dir, int slot, const void *k, int cta, size_t dyn, int *occ) {
     std::atomic<uint64_t> &cache = g_ex_occ[dev][is_ln][dir][slot];
@@ -821,40 +841,119 @@ int ex_occupancy(int dev, int is_ln, int dir, int slot, const void *k, int cta, 
     return GBNORM_OK;
 }
 
-// The smallest row-resident geometry that holds the row (vec: every row
-// tensor allows 16-byte vectors and N % 8 == 0), else the element-wise kernel.
-int ex_plan(int is_ln, int dir, int64_t M, int64_t N, bool vec, int dev, ExPlan *pl) {
-    const ExTable &t = kExTables[is_ln][dir];
+// Ring layout of a ring variant for this call: shared memory holds the
+// header, gamma (and beta, forward LayerNorm) in their storage type, then the
+// stages.  A stage is a tile of RT rows: x (then the residual rows), or x, dy
+// (then dres) and the statistics windows.  About 16 KB of rows per stage, at
+// least two stages per row group, at most kExRingMaxStages in all.  False if
+// that does not fit.
+bool exr_geometry(const ExVariant &v, const ExCall &c, int dev, TileCfg *tc, size_t *dyn) {
+    const int rpp = v.cta / v.tpr;
+    const int min_stages = 2 * rpp;
+    if (min_stages > kExRingMaxStages) return false;
+    const size_t params = exr_param_bytes(c.N, c.pdt, c.dir == 0 && c.is_ln);
+    const size_t optin = (size_t)g_dev[dev].smem_optin;
+    if (optin <= (size_t)kTmaHeaderBytes + params + 1024) return false;
+    const size_t budget = optin - kTmaHeaderBytes - params;
+    const size_t xrow = (size_t)c.N * elem_size(c.xdt), yrow = (size_t)c.N * elem_size(c.ydt);
+    auto stride_of = [&](int64_t rt) {
+        size_t st = exr_section((int)rt, c.N, c.xdt) * (c.extra ? 2 : 1);
+        if (c.dir == 1)
+            st += exr_section((int)rt, c.N, c.ydt) + ex_al128((size_t)exr_stat_floats((int)rt) * 4u * (c.is_ln ? 2u : 1u));
+        return st;
+    };
+    const size_t per_row = xrow * (c.extra ? 2 : 1) + (c.dir == 1 ? yrow : 0);
+    int64_t rt = (int64_t)((16u << 10) / per_row);
+    if (rt < 1) rt = 1;
+    if (rt > 64) rt = 64;
+    if (rt > c.M) rt = c.M > 0 ? c.M : 1;
+    while (rt > 1 && (size_t)min_stages * stride_of(rt) > budget) rt /= 2;
+    const size_t stride = stride_of(rt);
+    if ((size_t)min_stages * stride > budget) return false;
+    int stages = (int)(budget / stride);
+    if (stages > kExRingMaxStages) stages = kExRingMaxStages;
+    stages -= stages % rpp;
+    size_t ring = (size_t)stages * stride;
+    // the backward combines its row groups' partials in the idle ring
+    if (c.dir == 1 && rpp > 1) {
+        const size_t comb = (size_t)v.cta * v.vpt * 8u * 4u * (c.is_ln ? 2u : 1u);
+        if (comb > ring) ring = comb;
+    }
+    if (ring > budget) return false;
+    tc->rows = (int)rt;
+    tc->stages = stages;
+    tc->stride = (uint32_t)stride;
+    tc->fault = g_dev[dev].fault;
+    *dyn = kTmaHeaderBytes + params + ring;
+    return true;
+}
+
+// Plans variant i of the table for this call: false if it cannot serve it.
+int ex_try(const ExCall &c, int i, int dev, ExPlan *pl, bool *ok) {
+    *ok = false;
+    const ExTable &t = kExTables[c.is_ln][c.dir];
+    const ExVariant &v = t.v[i];
+    if ((int64_t)v.tpr * v.vpt * 8 < c.N) return GBNORM_OK;
     const int64_t limit = g_grid_limit.load(std::memory_order_relaxed);
     const int sms = g_dev[dev].sms;
-    if (vec && N % 8 == 0) {
-        for (int i = 0; i < t.count && i < 16; ++i) {
-            const ExVariant &v = t.v[i];
-            if ((int64_t)v.tpr * v.vpt * 8 < N) continue;
-            // fp32 parameters (forward: gamma and beta; backward: gamma, then
-            // the row groups' partials of dgamma and dbeta)
-            const size_t dyn = (size_t)N * 4u * (is_ln ? 2u : 1u);
-            if (dyn + 4096 > (size_t)g_dev[dev].smem_optin) break;
-            const void *k = v.kernel;
-            int occ = 0;
-            const int st = ex_occupancy(dev, is_ln, dir, i, k, v.cta, dyn, &occ);
-            if (st != GBNORM_OK) return st;
-            const int64_t rows_per_cta = v.cta / v.tpr;
-            const int64_t units = (M + rows_per_cta - 1) / rows_per_cta;
-            int64_t cap = (int64_t)occ * sms;
-            if (limit > 0 && limit < cap) cap = limit;
-            *pl = ExPlan{k, units < cap ? units : cap, dyn, v.cta};
-            return GBNORM_OK;
+    int occ = 0;
+    if (v.ring) {
+        if (c.no_ring || (c.dir == 1 && !c.stats16)) return GBNORM_OK;
+        TileCfg tc;
+        size_t dyn;
+        if (!exr_geometry(v, c, dev, &tc, &dyn)) return GBNORM_OK;
+        const int st = ex_occupancy(dev, c.is_ln, c.dir, i, v.kernel, v.cta, dyn, &occ);
+        if (st != GBNORM_OK) return st;
+        // persistent: at most one CTA per SM
+        const int64_t ntiles = (c.M + tc.rows - 1) / tc.rows;
+        int64_t cap = sms;
+        if (limit > 0 && limit < cap) cap = limit;
+        *pl = ExPlan{v.kernel, ntiles < cap ? ntiles : cap, dyn, v.cta, tc, v.name};
+        *ok = true;
+        return GBNORM_OK;
+    }
+    // fp32 parameters (forward: gamma and beta; backward: gamma, then the row
+    // groups' partials of dgamma and dbeta)
+    const size_t dyn = (size_t)c.N * 4u * (c.is_ln ? 2u : 1u);
+    if (dyn + 4096 > (size_t)g_dev[dev].smem_optin) return GBNORM_OK;
+    const int st = ex_occupancy(dev, c.is_ln, c.dir, i, v.kernel, v.cta, dyn, &occ);
+    if (st != GBNORM_OK) return st;
+    const int64_t rows_per_cta = v.cta / v.tpr;
+    const int64_t units = (c.M + rows_per_cta - 1) / rows_per_cta;
+    int64_t cap = (int64_t)occ * sms;
+    if (limit > 0 && limit < cap) cap = limit;
+    *pl = ExPlan{v.kernel, units < cap ? units : cap, dyn, v.cta, TileCfg{0, 0, 0, nullptr}, v.name};
+    *ok = true;
+    return GBNORM_OK;
+}
+
+// The first table entry that serves the call (ring kernels come first; a
+// forced entry is tried before all others), else the element-wise kernel.
+int ex_plan(const ExCall &c, int dev, ExPlan *pl) {
+    const ExTable &t = kExTables[c.is_ln][c.dir];
+    const int forced = g_ex_force[c.is_ln][c.dir].load(std::memory_order_relaxed) - 1;
+    if (c.vec && c.N % 8 == 0) {
+        bool ok = false;
+        if (forced >= 0 && forced < t.count) {
+            const int st = ex_try(c, forced, dev, pl, &ok);
+            if (st != GBNORM_OK || ok) return st;
+        }
+        if (forced != t.count) {
+            for (int i = 0; i < t.count; ++i) {
+                const int st = ex_try(c, i, dev, pl, &ok);
+                if (st != GBNORM_OK || ok) return st;
+            }
         }
     }
     const void *k = t.elem;
     int occ = 0;
-    const int st = ex_occupancy(dev, is_ln, dir, 16, k, kElemCTA, 0, &occ);
+    const int st = ex_occupancy(dev, c.is_ln, c.dir, kExSlots - 1, k, kElemCTA, 0, &occ);
     if (st != GBNORM_OK) return st;
     // one partial row per CTA in the backward: at most one CTA per SM
-    int64_t cap = dir == 0 ? (int64_t)occ * sms : (int64_t)sms;
+    int64_t cap = c.dir == 0 ? (int64_t)occ * g_dev[dev].sms : (int64_t)g_dev[dev].sms;
+    const int64_t limit = g_grid_limit.load(std::memory_order_relaxed);
     if (limit > 0 && limit < cap) cap = limit;
-    *pl = ExPlan{k, M < cap ? M : cap, 0, kElemCTA};
+    *pl = ExPlan{k, c.M < cap ? c.M : cap, 0, kElemCTA, TileCfg{0, 0, 0, nullptr}, "exe"};
     return GBNORM_OK;
 }
 
@@ -891,26 +990,34 @@ int do_fwd_ex(int is_ln, int64_t M, int64_t N, float eps, const void *x, int64_t
     int dev;
     int s = current_device(&dev);
     if (s != GBNORM_OK) return s;
+    g_ex_last[0] = "";
     if (M == 0) return GBNORM_OK;
     const bool vec = vec_rows(x, ldx, xdt) && vec_rows(res, ldr, xdt) && vec_rows(h, ldh, xdt) &&
                      vec_rows(y, ldy, ydt) && aligned16(gamma) && aligned16(beta);
     ExPlan pl;
-    s = ex_plan(is_ln, 0, M, N, vec, dev, &pl);
+    s = ex_plan(ExCall{is_ln, 0, M, N, xdt, ydt, pdt, res != nullptr, vec, true, false}, dev, &pl);
     if (s != GBNORM_OK) return s;
-    ExFwdParams p{x, res, h, gamma, beta, y, mean, rstd, ldx, ldr, ldh, ldy, M, N, eps, xdt, pdt, ydt};
+    g_ex_last[0] = pl.name;
+    ExFwdParams p{x, res, h, gamma, beta, y, mean, rstd, ldx, ldr, ldh, ldy, M, N, eps, xdt, pdt, ydt, pl.tc};
     return launch_ex(pl, &p, stream);
 }
 
+// Workspace of the general backward: the largest partial-row count any plan
+// of (is_ln, M, N) may use -- the element-wise and register plans, and the
+// ring plans' one CTA per SM (capped by the rows).  Independent of storage
+// types and extras.
 size_t ex_ws_bytes(int is_ln, int64_t M, int64_t N, int dev, int *status) {
-    size_t best = 0;
+    int64_t P = M < g_dev[dev].sms ? M : g_dev[dev].sms;
+    const int64_t limit = g_grid_limit.load(std::memory_order_relaxed);
+    if (limit > 0 && limit < P) P = limit;
     for (bool vec : {false, true}) {
         ExPlan pl;
-        *status = ex_plan(is_ln, 1, M, N, vec, dev, &pl);
+        *status = ex_plan(ExCall{is_ln, 1, M, N, GBNORM_F32, GBNORM_F32, GBNORM_F32, false, vec, true, true}, dev, &pl);
         if (*status != GBNORM_OK) return 0;
-        const size_t need = (size_t)pl.grid * (size_t)N * 4u * (is_ln ? 2u : 1u);
-        if (need > best) best = need;
+        if (pl.grid > P) P = pl.grid;
     }
-    return (best + 255u) & ~(size_t)255u;
+    const size_t need = (size_t)P * (size_t)N * 4u * (is_ln ? 2u : 1u);
+    return (need + 255u) & ~(size_t)255u;
 }
 
 int do_bwd_ex(int is_ln, int64_t M, int64_t N, const void *dy, int64_t lddy, int ydt, const void *x,
@@ -946,6 +1053,7 @@ int do_bwd_ex(int is_ln, int64_t M, int64_t N, const void *dy, int64_t lddy, int
     if (s != GBNORM_OK) return s;
     const size_t need = ex_ws_bytes(is_ln, M, N, dev, &s);
     if (s != GBNORM_OK) return s;
+    g_ex_last[1] = "";
     int64_t P = 0;
     if (M > 0) {
         if (!ws || ws_bytes < need || !aligned16(ws)) return GBNORM_ERR_WORKSPACE;
@@ -953,11 +1061,13 @@ int do_bwd_ex(int is_ln, int64_t M, int64_t N, const void *dy, int64_t lddy, int
         if (bad_aliasing_ex(all_out, 4, ins, 6)) return GBNORM_ERR_INVALID_ARG;
         const bool vec = vec_rows(dy, lddy, ydt) && vec_rows(x, ldx, xdt) && vec_rows(dres, lddres, xdt) &&
                          vec_rows(dx, lddx, xdt) && aligned16(gamma);
+        const bool stats16 = aligned16(rstd) && (!is_ln || aligned16(mean));
         ExPlan pl;
-        s = ex_plan(is_ln, 1, M, N, vec, dev, &pl);
+        s = ex_plan(ExCall{is_ln, 1, M, N, xdt, ydt, pdt, dres != nullptr, vec, stats16, false}, dev, &pl);
         if (s != GBNORM_OK) return s;
+        g_ex_last[1] = pl.name;
         ExBwdParams p{dy, x, dres, gamma, mean, rstd, dx, static_cast<float *>(ws), lddy, ldx, lddres, lddx,
-                      M, N, xdt, pdt, ydt};
+                      M, N, xdt, pdt, ydt, pl.tc};
         s = launch_ex(pl, &p, stream);
         if (s != GBNORM_OK) return s;
         P = pl.grid;
@@ -1114,6 +1224,41 @@ const char *gbnorm_variant_at(int is_layernorm, int dir, int dtype, int index) {
     if ((dir != 0 && dir != 1) || dtype < 0 || dtype > 2) return nullptr;
     const VariantTable &t = *kTables[is_layernorm ? 1 : 0][dir][dtype];
     return (index >= 0 && index < t.count) ? t.v[index].name : nullptr;
+}
+
+int gbnorm_ex_variant_count(int is_layernorm, int dir) {
+    if (dir != 0 && dir != 1) return 0;
+    return kExTables[is_layernorm ? 1 : 0][dir].count + 1;
+}
+
+const char *gbnorm_ex_variant_at(int is_layernorm, int dir, int index) {
+    if (dir != 0 && dir != 1) return nullptr;
+    const ExTable &t = kExTables[is_layernorm ? 1 : 0][dir];
+    if (index == t.count) return "exe";
+    return (index >= 0 && index < t.count) ? t.v[index].name : nullptr;
+}
+
+int gbnorm_ex_force_variant(int is_layernorm, int dir, const char *name) {
+    if (dir != 0 && dir != 1) return GBNORM_ERR_INVALID_ARG;
+    const int ln = is_layernorm ? 1 : 0;
+    if (!name || !name[0]) {
+        g_ex_force[ln][dir].store(0);
+        return GBNORM_OK;
+    }
+    const ExTable &t = kExTables[ln][dir];
+    for (int i = 0; i <= t.count; ++i) {
+        if (std::strcmp(gbnorm_ex_variant_at(ln, dir, i), name) == 0) {
+            g_ex_force[ln][dir].store(i + 1);
+            return GBNORM_OK;
+        }
+    }
+    return GBNORM_ERR_INVALID_ARG;
+}
+
+int gbnorm_ex_last_variant(int dir, char *buf, size_t len) {
+    if ((dir != 0 && dir != 1) || !buf || len == 0) return GBNORM_ERR_INVALID_ARG;
+    std::snprintf(buf, len, "%s", g_ex_last[dir]);
+    return GBNORM_OK;
 }
 
 int gbnorm_set_grid_limit(int max_ctas) {

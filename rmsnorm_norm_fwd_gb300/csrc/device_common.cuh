@@ -64,6 +64,41 @@ template <> __device__ __forceinline__ uint4 vpack<__half>(const float *f) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// ---------------------------------------------------------------- fp32 pairs
+// Blackwell issues two fp32 lanes as one instruction (__fadd2_rn, __fmul2_rn,
+// __ffma2_rn on float2).  Each lane is rounded exactly like the scalar
+// operation, so a computation on pairs gives the bits of the two scalar
+// computations in the same order, for half the issue slots.
+__device__ __forceinline__ float2 f2s(float s) { return make_float2(s, s); }
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// Elements 2i and 2i + 1 of a 16-byte vector, widened to float (exact).
+template <typename T> __device__ __forceinline__ float2 vpair(const uint4 &v, int i);
+template <> __device__ __forceinline__ float2 vpair<float>(const uint4 &v, int i) {
+    return make_float2(__uint_as_float(word(v, 2 * i)), __uint_as_float(word(v, 2 * i + 1)));
+}
+template <> __device__ __forceinline__ float2 vpair<__nv_bfloat16>(const uint4 &v, int i) {
+    const uint32_t w = word(v, i);
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <> __device__ __forceinline__ float2 vpair<__half>(const uint4 &v, int i) {
+    const uint32_t w = word(v, i);
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+// Pack E / 2 pairs into one 16-byte vector of T, each element rounded to
+// nearest even.
+template <typename T> __device__ __forceinline__ uint4 vpack2(const float2 *f) {
+    float o[VecTraits<T>::E];
+#pragma unroll
+    for (int i = 0; i < VecTraits<T>::E / 2; ++i) {
+        o[2 * i] = f[i].x;
+        o[2 * i + 1] = f[i].y;
+    }
+    return vpack<T>(o);
+}
+
 // Scalar element conversions for the element-wise (any-alignment) path.
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }

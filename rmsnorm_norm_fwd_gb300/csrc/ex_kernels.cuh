@@ -24,12 +24,16 @@
 // (and beta) are widened once per CTA into shared memory (plane-major float4,
 // conflict-free), the grid is persistent and the backward keeps its
 // dgamma/dbeta partials in registers, one partial row per CTA, summed by the
-// column-reduce kernel.  fwd_exe / bwd_exe: one CTA per row, element by
-// element, for any N, stride and alignment.
+// column-reduce kernel.  fwd_exr / bwd_exr: the same row groups fed through
+// a shared-memory ring by bulk asynchronous copies (one copy per row, or one
+// per tile when the rows are dense), for rows whose 16-byte vectors allow it.
+// fwd_exe / bwd_exe: one CTA per row, element by element, for any N, stride
+// and alignment.
 #pragma once
 
 #include "device_common.cuh"
 #include "params.h"
+#include "tma_kernels.cuh"
 
 namespace gbn {
 
@@ -439,6 +443,467 @@ __global__ void __launch_bounds__(kElemCTA) bwd_exe(const ExBwdParams p) {
             st1(dxr, j, p.xdt, o);
             wsg[j] += dyv * xh;
             if constexpr (LN) wsb[j] += dyv;
+        }
+    }
+}
+
+// ============================================================================ ring kernels
+// Rows are brought into a shared-memory ring by cp.async.bulk: a tile of RT
+// rows per stage, every row tensor of the tile in its own section of the
+// stage (rows packed at N * element-size bytes, each section 128-byte
+// aligned).  As in fwd_tmp / bwd_tmp, the CTA's NT threads form RPP = NT / TPR
+// row groups; group g walks the CTA's tiles g, g + RPP, ... through its own
+// SG = stages / RPP stages, and its first thread refills the stage of tile
+// j - 1 right after the group barrier of tile j's first row reduction (every
+// thread of the group has read tile j - 1 by then).  gamma (and beta) are
+// bulk-copied once per CTA in their storage type and widened on use; the
+// saved statistics of a backward tile come in with the tile (stat_window).
+
+struct ExRingHeader {
+    uint64_t full[kExRingMaxStages];
+    uint64_t pbar;  // gamma (and beta) landed
+    int abort;
+    int pad;
+    float red[(kTmaHeaderBytes - 8 * kExRingMaxStages - 16) / 4];  // row-group scratch
+};
+static_assert(sizeof(ExRingHeader) == kTmaHeaderBytes, "header layout");
+
+// Eight elements (8-element chunk c) of a row staged in shared memory in
+// storage type dt, widened to fp32.
+__device__ __forceinline__ void lds8(const unsigned char *row, int64_t c, int dt, float (&f)[8]) {
+    if (dt == kF32) {
+        const uint4 a = lds128(row + 32 * c), b = lds128(row + 32 * c + 16);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[e] = vget<float>(a, e);
+            f[4 + e] = vget<float>(b, e);
+        }
+    } else {
+        const uint4 a = lds128(row + 16 * c);
+        if (dt == kBF16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = vget<__nv_bfloat16>(a, e);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = vget<__half>(a, e);
+        }
+    }
+}
+// A parameter chunk from shared memory, or the constant a null row stands for.
+__device__ __forceinline__ void par8(const unsigned char *row, bool present, int64_t c, int dt, float one,
+                                     float (&f)[8]) {
+    if (present) {
+        lds8(row, c, dt, f);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = one;
+    }
+}
+
+// Rows [r0, r0 + rows) of a row tensor (row stride ld elements, row_bytes =
+// N * element size) into dst, packed at row_bytes: one copy when the rows are
+// dense, else one per row.  Every source row starts on a 16-byte boundary
+// (aligned base and row stride) and row_bytes is a multiple of 16.
+__device__ __forceinline__ void ex_copy_rows(unsigned char *dst, const void *base, int64_t ld, int es,
+                                             int64_t r0, int rows, size_t row_bytes, uint64_t *bar) {
+    const unsigned char *src = static_cast<const unsigned char *>(base) + r0 * ld * es;
+    const size_t pitch = (size_t)ld * (size_t)es;
+    if (pitch == row_bytes) {
+        bulk_g2s(dst, src, (uint32_t)(rows * row_bytes), bar);
+    } else {
+        for (int r = 0; r < rows; ++r) bulk_g2s(dst + r * row_bytes, src + r * pitch, (uint32_t)row_bytes, bar);
+    }
+}
+
+// Waits (bounded, regardless of the abort flag) for the copies a group leader
+// issued into its stages, so that none is still landing when the CTA exits.
+__device__ __forceinline__ void exr_drain(ExRingHeader &h, int grp, int SG, int issued) {
+    int zero = 0;
+    for (int j = issued > SG ? issued - SG : 0; j < issued; ++j)
+        mbar_wait_bounded(&h.full[grp * SG + j % SG], (uint32_t)((j / SG) & 1),
+                          reinterpret_cast<volatile int *>(&zero), nullptr);
+}
+
+template <bool LN, int TPR, int VPT, int NT>
+__global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
+    constexpr int RPP = NT / TPR;
+    constexpr int WPR = TPR / 32;
+    static_assert(NT % TPR == 0 && TPR % 32 == 0 && TPR > 32 && 2 * RPP <= kExRingMaxStages, "CTA shape");
+    static_assert(RPP * 2 * 2 * WPR <= (int)(sizeof(ExRingHeader::red) / 4), "scratch");
+    extern __shared__ __align__(128) unsigned char smem[];
+    ExRingHeader &h = *reinterpret_cast<ExRingHeader *>(smem);
+    const int64_t M = p.M, nc = p.N / 8;
+    const int xes = esize(p.xdt);
+    const size_t xrb = (size_t)p.N * xes;
+    unsigned char *gsm = smem + kTmaHeaderBytes;  // gamma, then beta
+    unsigned char *bsm = gsm + exr_param_bytes(p.N, p.pdt, false);
+    unsigned char *stages = smem + kTmaHeaderBytes + exr_param_bytes(p.N, p.pdt, LN);
+    const int SG = p.tc.stages / RPP, RT = p.tc.rows;
+    const size_t xsec = exr_section(RT, p.N, p.xdt);
+    const int64_t ntiles = (M + RT - 1) / RT;
+    const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
+    float *scratch = h.red + grp * (2 * 2 * WPR);
+    volatile int *abort_flag = &h.abort;
+    int issued = 0;
+
+    auto tile_of = [&](int64_t j) {
+        const int64_t tile = blockIdx.x + (grp + j * RPP) * (int64_t)gridDim.x;
+        return tile < ntiles ? tile : (int64_t)-1;
+    };
+    auto issue = [&](int64_t j) {
+        const int64_t tile = tile_of(j);
+        if (tile < 0) return;
+        const int s = grp * SG + (int)(j % SG);
+        const int64_t r0 = tile * RT;
+        const int rows = (int)(M - r0 < RT ? M - r0 : RT);
+        unsigned char *dst = stages + (size_t)s * p.tc.stride;
+        mbar_arrive_expect_tx(&h.full[s], (uint32_t)(rows * xrb) * (p.res ? 2u : 1u));
+        ex_copy_rows(dst, p.x, p.ldx, xes, r0, rows, xrb, &h.full[s]);
+        if (p.res) ex_copy_rows(dst + xsec, p.res, p.ldr, xes, r0, rows, xrb, &h.full[s]);
+        ++issued;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RPP * SG; ++s) mbar_init(&h.full[s], 1);
+        mbar_init(&h.pbar, 1);
+        h.abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        load_params(&h.pbar, gsm, bsm, p.gamma, LN ? p.beta : nullptr,
+                    (uint32_t)((size_t)p.N * esize(p.pdt)));
+    if (t == 0)
+        for (int j = 0; j < SG; ++j) issue(j);
+    mbar_wait_bounded(&h.pbar, 0, abort_flag, p.tc.fault);
+
+    const float n = (float)p.N;
+    const bool full = nc == (int64_t)TPR * VPT;  // every thread holds VPT chunks (uniform)
+    const bool has_g = p.gamma != nullptr, has_b = LN && p.beta != nullptr;
+    int parity = 0;
+    for (int64_t j = 0;; ++j) {
+        const int64_t tile = tile_of(j);
+        if (tile < 0) break;  // uniform per group (named barriers only)
+        const int s = grp * SG + (int)(j % SG);
+        mbar_wait_bounded(&h.full[s], (uint32_t)((j / SG) & 1), abort_flag, p.tc.fault);
+        const int64_t r0 = tile * RT;
+        const int rows = (int)(M - r0 < RT ? M - r0 : RT);
+        const unsigned char *tb = stages + (size_t)s * p.tc.stride;
+        for (int r = 0; r < rows; ++r) {  // every thread of the group works on the same row
+            const int64_t row = r0 + r;
+            const unsigned char *xs = tb + (size_t)r * xrb;
+            float xf[VPT][8];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int64_t c = (int64_t)k * TPR + t;
+                if (c < nc) {
+                    lds8(xs, c, p.xdt, xf[k]);
+                    if (p.res) {
+                        // h = x + r in fp32, rounded once to the storage type
+                        float r8[8];
+                        lds8(xs + xsec, c, p.xdt, r8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) xf[k][e] = round_to(xf[k][e] + r8[e], p.xdt);
+                        if (p.h) st8(row_ptr(p.h, row, p.ldh, p.xdt), 8 * c, p.xdt, xf[k]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xf[k][e] = 0.f;
+                }
+            }
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc += LN ? xf[k][e] : xf[k][e] * xf[k][e];
+            float mean = 0.f;
+            if (LN && full) {
+                constexpr float kC = (float)(VPT * 8);
+                mean = acc * (1.f / kC);
+                float m2 = 0.f;
+#pragma unroll
+                for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float d = xf[k][e] - mean;
+                        m2 += d * d;
+                    }
+                group_meanvar_equal<TPR>(mean, m2, kC, scratch, parity, 1 + grp);
+                acc = m2;
+            } else {
+                float a[1] = {acc};
+                group_allreduce<TPR, 1>(a, scratch, parity, 1 + grp);
+                acc = a[0];
+                if constexpr (LN) {
+                    mean = acc / n;
+                    a[0] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k) {
+                        if ((int64_t)k * TPR + t >= nc) continue;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float d = xf[k][e] - mean;
+                            a[0] += d * d;
+                        }
+                    }
+                    group_allreduce<TPR, 1>(a, scratch, parity, 1 + grp);
+                    acc = a[0];
+                }
+            }
+            if (r == 0 && j >= 1 && t == 0) {
+                // every thread of the group is past its last read of tile
+                // j - 1's stage: order those reads before the copy's writes
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(j - 1 + SG);
+            }
+            const float rstd = rsqrtf(acc / n + p.eps);
+            if (t == 0) {
+                if (p.rstd) p.rstd[row] = rstd;
+                if (LN && p.mean) p.mean[row] = mean;
+            }
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int64_t c = (int64_t)k * TPR + t;
+                if (c >= nc) continue;
+                float g[8], o[8];
+                par8(gsm, has_g, c, p.pdt, 1.f, g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = ((xf[k][e] - mean) * rstd) * g[e];
+                if constexpr (LN) {
+                    float b[8];
+                    par8(bsm, has_b, c, p.pdt, 0.f, b);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] += b[e];
+                }
+                st8(row_ptr(p.y, row, p.ldy, p.ydt), 8 * c, p.ydt, o);
+            }
+        }
+    }
+    if (t == 0 && *abort_flag) exr_drain(h, grp, SG, issued);
+}
+
+template <bool LN, int TPR, int VPT, int NT>
+__global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
+    pdl_launch_dependents();  // the column reduce waits for this grid's completion
+    constexpr int NS = LN ? 2 : 1;
+    constexpr int RPP = NT / TPR;
+    constexpr int WPR = TPR / 32;
+    // pass-1 values kept in registers for pass 2 (as long as the dgamma/dbeta
+    // sums leave room for them)
+    constexpr bool HOLD = LN ? VPT == 1 : VPT <= 2;
+    static_assert(NT % TPR == 0 && TPR % 32 == 0 && TPR > 32 && 2 * RPP <= kExRingMaxStages, "CTA shape");
+    static_assert(RPP * 2 * NS * WPR <= (int)(sizeof(ExRingHeader::red) / 4), "scratch");
+    extern __shared__ __align__(128) unsigned char smem[];
+    ExRingHeader &h = *reinterpret_cast<ExRingHeader *>(smem);
+    const int64_t M = p.M, nc = p.N / 8;
+    const int xes = esize(p.xdt), yes = esize(p.ydt);
+    const size_t xrb = (size_t)p.N * xes, yrb = (size_t)p.N * yes;
+    unsigned char *gsm = smem + kTmaHeaderBytes;  // gamma in its storage type
+    unsigned char *stages = smem + kTmaHeaderBytes + exr_param_bytes(p.N, p.pdt, false);
+    const int SG = p.tc.stages / RPP, RT = p.tc.rows;
+    // stage: x | dy | dres (if any) | rstd, mean windows
+    const size_t xsec = exr_section(RT, p.N, p.xdt), ysec = exr_section(RT, p.N, p.ydt);
+    const size_t rsec = p.dres ? xsec : 0;
+    const int64_t ntiles = (M + RT - 1) / RT;
+    const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
+    float *scratch = h.red + grp * (2 * NS * WPR);
+    volatile int *abort_flag = &h.abort;
+    int issued = 0;
+
+    auto tile_of = [&](int64_t j) {
+        const int64_t tile = blockIdx.x + (grp + j * RPP) * (int64_t)gridDim.x;
+        return tile < ntiles ? tile : (int64_t)-1;
+    };
+    auto issue = [&](int64_t j) {
+        const int64_t tile = tile_of(j);
+        if (tile < 0) return;
+        const int s = grp * SG + (int)(j % SG);
+        const int64_t r0 = tile * RT;
+        const int rows = (int)(M - r0 < RT ? M - r0 : RT);
+        unsigned char *dst = stages + (size_t)s * p.tc.stride;
+        int64_t wa, wb;
+        stat_window(r0, rows, M, &wa, &wb);
+        const uint32_t tx = (uint32_t)(rows * xrb) * (p.dres ? 2u : 1u) + (uint32_t)(rows * yrb) +
+                            (uint32_t)(wb - wa) * 4u * (LN ? 2u : 1u);
+        mbar_arrive_expect_tx(&h.full[s], tx);
+        ex_copy_rows(dst, p.x, p.ldx, xes, r0, rows, xrb, &h.full[s]);
+        ex_copy_rows(dst + xsec, p.dy, p.lddy, yes, r0, rows, yrb, &h.full[s]);
+        if (p.dres) ex_copy_rows(dst + xsec + ysec, p.dres, p.lddres, xes, r0, rows, xrb, &h.full[s]);
+        if (wb > wa) {
+            float *sd = reinterpret_cast<float *>(dst + xsec + ysec + rsec);
+            bulk_g2s(sd, p.rstd + wa, (uint32_t)(wb - wa) * 4u, &h.full[s]);
+            if constexpr (LN) bulk_g2s(sd + exr_stat_floats(RT), p.mean + wa, (uint32_t)(wb - wa) * 4u, &h.full[s]);
+        }
+        ++issued;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RPP * SG; ++s) mbar_init(&h.full[s], 1);
+        mbar_init(&h.pbar, 1);
+        h.abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        load_params(&h.pbar, gsm, nullptr, p.gamma, nullptr, (uint32_t)((size_t)p.N * esize(p.pdt)));
+    if (t == 0)
+        for (int j = 0; j < SG; ++j) issue(j);
+    mbar_wait_bounded(&h.pbar, 0, abort_flag, p.tc.fault);
+
+    const float n = (float)p.N;
+    const bool has_g = p.gamma != nullptr;
+    float accg[VPT][8], accb[LN ? VPT : 1][8];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            accg[k][e] = 0.f;
+            if constexpr (LN) accb[k][e] = 0.f;
+        }
+    int parity = 0;
+    // Trip count uniform over the CTA (the epilogue's barriers); groups past
+    // their last tile leave the loop early.
+    const int64_t my_tiles = blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    for (int64_t j = 0; j < (my_tiles + RPP - 1) / RPP; ++j) {
+        const int64_t tile = tile_of(j);
+        if (tile < 0) break;  // uniform per group (named barriers only below)
+        const int s = grp * SG + (int)(j % SG);
+        mbar_wait_bounded(&h.full[s], (uint32_t)((j / SG) & 1), abort_flag, p.tc.fault);
+        const int64_t r0 = tile * RT;
+        const int rows = (int)(M - r0 < RT ? M - r0 : RT);
+        int64_t wa, wb;
+        stat_window(r0, rows, M, &wa, &wb);
+        const unsigned char *tb = stages + (size_t)s * p.tc.stride;
+        const float *st = reinterpret_cast<const float *>(tb + xsec + ysec + rsec) - wa;
+        for (int r = 0; r < rows; ++r) {  // every thread of the group works on the same row
+            const int64_t row = r0 + r;
+            const unsigned char *xs = tb + (size_t)r * xrb;
+            const unsigned char *ds = tb + xsec + (size_t)r * yrb;
+            const bool in_win = row < wb;
+            const float rstd = in_win ? st[row] : __ldg(p.rstd + row);
+            const float mean = LN ? (in_win ? st[exr_stat_floats(RT) + row] : __ldg(p.mean + row)) : 0.f;
+            float sum[NS];
+#pragma unroll
+            for (int q = 0; q < NS; ++q) sum[q] = 0.f;
+            float hx[HOLD ? VPT : 1][8], hg[HOLD ? VPT : 1][8], hd[HOLD ? VPT : 1][8];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int64_t c = (int64_t)k * TPR + t;
+                float x8[8], d8[8], g8[8];
+                if (c < nc) {
+                    lds8(xs, c, p.xdt, x8);
+                    lds8(ds, c, p.ydt, d8);
+                    par8(gsm, has_g, c, p.pdt, 1.f, g8);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x8[e] = d8[e] = g8[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float xc = x8[e] - mean;
+                    const float gg = d8[e] * g8[e];
+                    if constexpr (HOLD) {
+                        hx[k][e] = xc;
+                        hg[k][e] = gg;
+                        hd[k][e] = d8[e];
+                    }
+                    sum[0] += gg * xc;
+                    if constexpr (LN) sum[NS - 1] += gg;
+                }
+            }
+            group_allreduce<TPR, NS>(sum, scratch, parity, 1 + grp);
+            if (r == 0 && j >= 1 && t == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(j - 1 + SG);
+            }
+            // dx = rstd g - rstd c1 - (rstd c2) xhat (+ dres), c2 = rstd sum g (x - mean) / n
+            const float c2 = rstd * sum[0] / n;
+            const float rc1 = LN ? rstd * (sum[NS - 1] / n) : 0.f;
+            const float rc2 = rstd * c2;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int64_t c = (int64_t)k * TPR + t;
+                if (c >= nc) continue;
+                float xc[8], gg[8], dv[8], o[8];
+                if constexpr (HOLD) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        xc[e] = hx[k][e];
+                        gg[e] = hg[k][e];
+                        dv[e] = hd[k][e];
+                    }
+                } else {
+                    float x8[8], g8[8];
+                    lds8(xs, c, p.xdt, x8);
+                    lds8(ds, c, p.ydt, dv);
+                    par8(gsm, has_g, c, p.pdt, 1.f, g8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        xc[e] = x8[e] - mean;
+                        gg[e] = dv[e] * g8[e];
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float xh = xc[e] * rstd;
+                    o[e] = fmaf(-rc2, xh, fmaf(rstd, gg[e], -rc1));
+                    accg[k][e] += dv[e] * xh;
+                    if constexpr (LN) accb[k][e] += dv[e];
+                }
+                if (p.dres) {
+                    float r8[8];
+                    lds8(tb + xsec + ysec + (size_t)r * xrb, c, p.xdt, r8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] += r8[e];
+                }
+                st8(row_ptr(p.dx, row, p.lddx, p.xdt), 8 * c, p.xdt, o);
+            }
+        }
+    }
+    if (t == 0 && *abort_flag) exr_drain(h, grp, SG, issued);
+
+    // Epilogue: this CTA's partial row.  With several row groups (same
+    // columns), every group writes its partials to the idle ring, then each
+    // thread adds, for its columns, the groups' values in group order.
+    float *wsg = p.ws + (int64_t)blockIdx.x * p.N;
+    float *wsb = p.ws + ((int64_t)gridDim.x + blockIdx.x) * p.N;
+    if constexpr (RPP > 1) {
+        constexpr int CAP = TPR * VPT * 8;
+        float *comb = reinterpret_cast<float *>(stages);  // [NS][RPP][CAP]
+        __syncthreads();  // every group is done with the ring
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int c = (k * TPR + t) * 8 + e;
+                comb[grp * CAP + c] = accg[k][e];
+                if constexpr (LN) comb[(RPP + grp) * CAP + c] = accb[k][e];
+            }
+        __syncthreads();
+        const int64_t ncol = p.N < CAP ? p.N : CAP;
+        for (int c = threadIdx.x; c < ncol; c += NT) {
+            float sg = 0.f, sb = 0.f;
+#pragma unroll
+            for (int gi = 0; gi < RPP; ++gi) {
+                sg += comb[gi * CAP + c];
+                if constexpr (LN) sb += comb[(RPP + gi) * CAP + c];
+            }
+            wsg[c] = sg;
+            if constexpr (LN) wsb[c] = sb;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int64_t c = (int64_t)k * TPR + t;
+            if (c >= nc) continue;
+            float4 *g4 = reinterpret_cast<float4 *>(wsg + 8 * c);
+            float4 *b4 = reinterpret_cast<float4 *>(wsb + 8 * c);
+            g4[0] = make_float4(accg[k][0], accg[k][1], accg[k][2], accg[k][3]);
+            g4[1] = make_float4(accg[k][4], accg[k][5], accg[k][6], accg[k][7]);
+            if constexpr (LN) {
+                b4[0] = make_float4(accb[k][0], accb[k][1], accb[k][2], accb[k][3]);
+                b4[1] = make_float4(accb[k][4], accb[k][5], accb[k][6], accb[k][7]);
+            }
         }
     }
 }

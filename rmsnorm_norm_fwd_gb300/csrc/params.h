@@ -11,6 +11,7 @@ constexpr int kElemCTA = 256;  // threads per CTA of the element-wise kernels
 constexpr int kColCTA = 512;   // threads per CTA of the column-reduce kernel
 constexpr int kTmaHeaderBytes = 2048;  // TMA kernels: barriers, abort flag, reduction scratch
 constexpr int kTmaMaxStages = 8;       // TMA kernels: deepest shared-memory ring
+constexpr int kExRingMaxStages = 16;   // general-form ring kernels: deepest ring (2 per row group)
 constexpr int kSkPartBytes = 16 * 128 * 4;  // single-kernel column reduce: band sums in shared memory
 
 // Pipeline geometry of the TMA-staged kernels, chosen by the host per call.
@@ -51,6 +52,22 @@ struct BwdParams {
 
 // General form (strided rows, a storage type per tensor, fused residual
 // add).  Strides (ld*) are in elements; dtypes are gbnorm_dtype_t codes.
+// Shared-memory layout of the general-form ring kernels (host and device
+// agree on it): after the header, gamma (and beta) in their storage type
+// (dt 0: fp32, else 16-bit), then the stages; a stage holds one section per
+// row tensor of its tile of rt rows (x, then the residual rows; or x, dy,
+// dres), each 128-byte aligned.
+__host__ __device__ inline size_t ex_al128(size_t b) { return (b + 127) & ~(size_t)127; }
+__host__ __device__ inline size_t exr_param_bytes(int64_t N, int pdt, bool two) {
+    return ex_al128((size_t)N * (pdt == 0 ? 4 : 2)) * (two ? 2 : 1);
+}
+__host__ __device__ inline size_t exr_section(int rt, int64_t N, int dt) {
+    return ex_al128((size_t)rt * (size_t)N * (dt == 0 ? 4 : 2));
+}
+// Floats reserved per saved statistic per backward stage: the widest
+// 16-byte-aligned window of rt rows.
+__host__ __device__ constexpr int exr_stat_floats(int rt) { return (rt + 7) & ~3; }
+
 struct ExFwdParams {
     const void *x;      // [M, ldx] xdt
     const void *res;    // [M, ldr] xdt, or null (no residual add)
@@ -64,6 +81,7 @@ struct ExFwdParams {
     int64_t M, N;
     float eps;
     int xdt, pdt, ydt;
+    TileCfg tc;  // ring kernels: rows per tile, stages, stage stride, fault word
 };
 
 struct ExBwdParams {
@@ -78,6 +96,7 @@ struct ExBwdParams {
     int64_t lddy, ldx, lddres, lddx;
     int64_t M, N;
     int xdt, pdt, ydt;
+    TileCfg tc;  // ring kernels: rows per tile, stages, stage stride, fault word
 };
 
 enum VariantKind : int {
@@ -143,6 +162,7 @@ struct ExVariant {
     const char *name;
     const void *kernel;
     int tpr, vpt, cta;  // capacity tpr * vpt * 8 elements
+    int ring = 0;       // rows staged through a bulk-copy ring (else read into registers)
 };
 struct ExTable {
     const ExVariant *v;

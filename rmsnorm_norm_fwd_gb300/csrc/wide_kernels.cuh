@@ -155,12 +155,12 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wide(const FwdParams p) {
 
         // ---- pass 1: statistics (rows from DRAM, kept in L2)
         float cnt[R], mean[R], acc[R];  // acc: sum x^2 (RMS) or M2 (LN)
-        float pa[R][A];
+        float2 pa[R][A];                // RMS partial sums of squares, as pairs
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             cnt[r] = mean[r] = acc[r] = 0.f;
 #pragma unroll
-            for (int a = 0; a < A; ++a) pa[r][a] = 0.f;
+            for (int a = 0; a < A; ++a) pa[r][a] = f2s(0.f);
         }
         for (int64_t b = t; b < nv; b += (int64_t)NT * U) {
             uint4 q[R][U];
@@ -177,41 +177,42 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wide(const FwdParams p) {
 #pragma unroll
                     for (int u = 0; u < U; ++u)
 #pragma unroll
-                        for (int e = 0; e < E; ++e) {
-                            const float f = vget<T>(q[r][u], e);
-                            pa[r][u % A] += f * f;
+                        for (int e = 0; e < E / 2; ++e) {
+                            const float2 f = vpair<T>(q[r][u], e);
+                            pa[r][u % A] = f2fma(f, f, pa[r][u % A]);
                         }
                 } else {
-                    float ps[A], pm[A];
+                    float2 ps[A], pm[A];
                     int nb = 0;
 #pragma unroll
-                    for (int a = 0; a < A; ++a) ps[a] = pm[a] = 0.f;
+                    for (int a = 0; a < A; ++a) ps[a] = pm[a] = f2s(0.f);
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         if (b + (int64_t)u * NT < nv) {
                             nb += E;
 #pragma unroll
-                            for (int e = 0; e < E; ++e) ps[u % A] += vget<T>(q[r][u], e);
+                            for (int e = 0; e < E / 2; ++e) ps[u % A] = f2add(ps[u % A], vpair<T>(q[r][u], e));
                         }
                     }
-                    float s = ps[0];
+                    float s = ps[0].x + ps[0].y;
 #pragma unroll
-                    for (int a = 1; a < A; ++a) s += ps[a];
+                    for (int a = 1; a < A; ++a) s += ps[a].x + ps[a].y;
                     const float fb = (float)nb;
                     const float mb = __fdiv_rn(s, fb);
+                    const float2 nmb = f2s(-mb);
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         if (b + (int64_t)u * NT < nv) {
 #pragma unroll
-                            for (int e = 0; e < E; ++e) {
-                                const float d = vget<T>(q[r][u], e) - mb;
-                                pm[u % A] += d * d;
+                            for (int e = 0; e < E / 2; ++e) {
+                                const float2 d = f2add(vpair<T>(q[r][u], e), nmb);
+                                pm[u % A] = f2fma(d, d, pm[u % A]);
                             }
                         }
                     }
-                    float m2b = pm[0];
+                    float m2b = pm[0].x + pm[0].y;
 #pragma unroll
-                    for (int a = 1; a < A; ++a) m2b += pm[a];
+                    for (int a = 1; a < A; ++a) m2b += pm[a].x + pm[a].y;
                     if (cnt[r] == 0.f) {
                         cnt[r] = fb;
                         mean[r] = mb;
@@ -231,9 +232,9 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wide(const FwdParams p) {
         if constexpr (!LN) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                acc[r] = pa[r][0];
+                acc[r] = pa[r][0].x + pa[r][0].y;
 #pragma unroll
-                for (int a = 1; a < A; ++a) acc[r] += pa[r][a];
+                for (int a = 1; a < A; ++a) acc[r] += pa[r][a].x + pa[r][a].y;
             }
         }
 
@@ -321,13 +322,14 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wide(const FwdParams p) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (!ok[r]) continue;
-                    float o[E];
+                    float2 o[E / 2];
+                    const float2 nm = f2s(-mean[r]), rs = f2s(rstd[r]);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        o[e] = ((vget<T>(q[r][u], e) - mean[r]) * rstd[r]) * vget<T>(g[u], e);
-                        if constexpr (LN) o[e] += vget<T>(bb[u], e);
+                    for (int e = 0; e < E / 2; ++e) {
+                        o[e] = f2mul(f2mul(f2add(vpair<T>(q[r][u], e), nm), rs), vpair<T>(g[u], e));
+                        if constexpr (LN) o[e] = f2add(o[e], vpair<T>(bb[u], e));
                     }
-                    st_l2hint(static_cast<uint4 *>(p.y) + (base + r) * nv + v, vpack<T>(o), drop);
+                    st_l2hint(static_cast<uint4 *>(p.y) + (base + r) * nv + v, vpack2<T>(o), drop);
                 }
             }
         }
@@ -707,13 +709,14 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     if constexpr (CL > 1) cluster_sync_all();
     else __syncthreads();
 
-    float accg[K][E], accb[LN ? K : 1][E];
+    // dgamma (and dbeta) sums of this thread's columns, as pairs of elements
+    float2 accg[K][E / 2], accb[LN ? K : 1][E / 2];
 #pragma unroll
     for (int k = 0; k < K; ++k)
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            accg[k][e] = 0.f;
-            if constexpr (LN) accb[k][e] = 0.f;
+        for (int e = 0; e < E / 2; ++e) {
+            accg[k][e] = f2s(0.f);
+            if constexpr (LN) accb[k][e] = f2s(0.f);
         }
 
     const int64_t nrows = cid < M ? (M - cid + ncl - 1) / ncl : 0;
@@ -726,12 +729,13 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
             prefetch_row(row_dy(k), (size_t)cnt * 16, lane, keep);
         }
     };
-    auto gam = [&](int k, float (&g)[E]) {
+    auto gam = [&](int k, float2 (&g)[E / 2]) {
         const int64_t lv = (int64_t)k * NT + t;
 #pragma unroll
         for (int h = 0; h < H; ++h) {
             const float4 q = gsm[h * KNT + lv];
-            g[4 * h] = q.x, g[4 * h + 1] = q.y, g[4 * h + 2] = q.z, g[4 * h + 3] = q.w;
+            g[2 * h] = make_float2(q.x, q.y);
+            g[2 * h + 1] = make_float2(q.z, q.w);
         }
     };
     int parity = 0;
@@ -795,10 +799,13 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
         const float rstd2 = has2 ? __ldg(p.rstd + row_of(k2)) : 0.f;
         const float mean2 = (LN && has2) ? __ldg(p.mean + row_of(k2)) : 0.f;
         const float rc1 = rstd2 * cst[k2 % 3][0], rc2 = rstd2 * cst[k2 % 3][1];
+        // the row constants as pairs (negations are exact: x + (-m) = x - m)
+        const float2 nm1 = f2s(-mean1), nm2 = f2s(-mean2), r2 = f2s(rstd2), nrc1 = f2s(-rc1), nrc2 = f2s(-rc2);
         const uint4 *x1 = row_x(has1 ? k1 : 0), *d1 = row_dy(has1 ? k1 : 0);
         const uint4 *x2 = row_x(has2 ? k2 : 0), *d2 = row_dy(has2 ? k2 : 0);
         uint4 *dx2 = static_cast<uint4 *>(p.dx) + row_of(has2 ? k2 : 0) * nv + v0;
-        float a2[2] = {0.f, 0.f}, a1[2] = {0.f, 0.f};
+        // pass-1 partials: lane 0 the even elements, lane 1 the odd ones
+        float2 a2 = f2s(0.f), a1 = f2s(0.f);
 #pragma unroll
         for (int kb = 0; kb < K; kb += KB) {
             uint4 px[KB], pd[KB], qx[KB], qd[KB];
@@ -814,32 +821,33 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
 #pragma unroll
             for (int i = 0; i < KB; ++i) {
                 const int64_t lv = (int64_t)(kb + i) * NT + t;
-                float g[E];
+                float2 g[E / 2];
                 gam(kb + i, g);
                 if (has2) {
-                    float o[E];
+                    float2 o[E / 2];
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float xh = (vget<T>(qx[i], e) - mean2) * rstd2;
-                        const float dyv = vget<T>(qd[i], e);
-                        o[e] = fmaf(-rc2, xh, fmaf(rstd2, dyv * g[e], -rc1));
-                        accg[kb + i][e] += dyv * xh;  // zero past the slice (dy = 0)
-                        if constexpr (LN) accb[kb + i][e] += dyv;
+                    for (int e = 0; e < E / 2; ++e) {
+                        const float2 xh = f2mul(f2add(vpair<T>(qx[i], e), nm2), r2);
+                        const float2 dyv = vpair<T>(qd[i], e);
+                        // dx = rstd g - rstd c1 - (rstd c2) xhat
+                        o[e] = f2fma(nrc2, xh, f2fma(r2, f2mul(dyv, g[e]), nrc1));
+                        accg[kb + i][e] = f2fma(dyv, xh, accg[kb + i][e]);  // zero past the slice (dy = 0)
+                        if constexpr (LN) accb[kb + i][e] = f2add(accb[kb + i][e], dyv);
                     }
-                    if (lv < cnt) st_l2hint(dx2 + lv, vpack<T>(o), drop);
+                    if (lv < cnt) st_l2hint(dx2 + lv, vpack2<T>(o), drop);
                 }
                 if (has1) {
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float gg = vget<T>(pd[i], e) * g[e];  // zero past the slice
-                        a2[e & 1] += gg * (vget<T>(px[i], e) - mean1);
-                        if constexpr (LN) a1[e & 1] += gg;
+                    for (int e = 0; e < E / 2; ++e) {
+                        const float2 gg = f2mul(vpair<T>(pd[i], e), g[e]);  // zero past the slice
+                        a2 = f2fma(gg, f2add(vpair<T>(px[i], e), nm1), a2);
+                        if constexpr (LN) a1 = f2add(a1, gg);
                     }
                 }
             }
         }
-        v[0] = (a2[0] + a2[1]) * rstd1;  // sum g xhat = rstd sum g (x - mean)
-        if constexpr (LN) v[NVAL - 1] = a1[0] + a1[1];
+        v[0] = (a2.x + a2.y) * rstd1;  // sum g xhat = rstd sum g (x - mean)
+        if constexpr (LN) v[NVAL - 1] = a1.x + a1.y;
     };
 
     float v[NVAL];
@@ -887,10 +895,10 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
 #pragma unroll
         for (int h = 0; h < H; ++h) {
             reinterpret_cast<float4 *>(wsg + lv * E)[h] =
-                make_float4(accg[k][4 * h], accg[k][4 * h + 1], accg[k][4 * h + 2], accg[k][4 * h + 3]);
+                make_float4(accg[k][2 * h].x, accg[k][2 * h].y, accg[k][2 * h + 1].x, accg[k][2 * h + 1].y);
             if constexpr (LN)
                 reinterpret_cast<float4 *>(wsb + lv * E)[h] =
-                    make_float4(accb[k][4 * h], accb[k][4 * h + 1], accb[k][4 * h + 2], accb[k][4 * h + 3]);
+                    make_float4(accb[k][2 * h].x, accb[k][2 * h].y, accb[k][2 * h + 1].x, accb[k][2 * h + 1].y);
         }
     }
 }

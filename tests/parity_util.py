@@ -103,7 +103,7 @@ def row_threads(variant: str):
     )
     if variant.startswith("sk"):  # single-kernel backward: the staged kernel's geometry
         variant = variant[2:]
-    m = re.fullmatch(r"ex[fb](\d+)x(\d+)b(\d+)", variant)  # general form: 8-element chunks
+    m = re.fullmatch(r"exr?[fb](\d+)x(\d+)b(\d+)", variant)  # general form: 8-element chunks
     if m:
         return int(m.group(1)), 1, False
     for pat, f in pats:
@@ -114,25 +114,6 @@ def row_threads(variant: str):
     if variant in ("elem", "exe"):
         return 256, 1, True
     raise ValueError(f"unknown variant {variant!r}")
-
-
-# General-form row geometries (TPR, VPT, CTA) per direction, capacity
-# TPR * VPT * 8, in the order the library tries them (the first that holds the
-# row serves it).
-EX_GEOMS = {"fwd": ((32, 1, 256), (32, 2, 256), (64, 2, 256), (128, 2, 256), (128, 4, 256), (256, 4, 256),
-                    (512, 4, 512)),
-            "bwd": ((32, 1, 256), (64, 1, 256), (128, 1, 256), (256, 1, 256), (512, 1, 512), (512, 2, 512),
-                    (512, 4, 512))}
-
-
-def ex_variant(N: int, vec: bool, direction: str = "fwd") -> str:
-    """Name of the general-form kernel that serves rows of N (vec: every row
-    allows 16-byte vectors) in `direction`."""
-    if vec and N % 8 == 0:
-        for tpr, vpt, cta in EX_GEOMS[direction]:
-            if tpr * vpt * 8 >= N:
-                return f"ex{direction[0]}{tpr}x{vpt}b{cta}"
-    return "exe"
 
 
 def sum_depth(N: int, variant: str, dtype: str) -> int:

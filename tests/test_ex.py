@@ -2,12 +2,14 @@
 fp64 oracle: a storage type per tensor (rows, parameters, output), rows with
 their own strides, and the fused residual add, forward and backward, on the
 vector path and the element-wise path (GPU)."""
+import re
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from parity_util import compare, ex_variant
+from parity_util import compare
 from rmsnorm_norm_fwd_gb300.inputs import DTYPES, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -35,7 +37,7 @@ def _vec(*ts):
                for t in ts)
 
 
-def run_ex(op, inp, pad=0, y_dtype=None, residual=None, dres=None, store_h=True):
+def run_ex(op, inp, pad=0, y_dtype=None, residual=None, dres=None, store_h=True, check_path=True):
     """Forward and backward through the general form; returns (host outputs,
     variants).  With a residual, inp.x is x and the backward differentiates at
     the stored h; without one, x itself."""
@@ -46,6 +48,7 @@ def run_ex(op, inp, pad=0, y_dtype=None, residual=None, dres=None, store_h=True)
     gam, bet = inp.gamma.cuda(), inp.beta.cuda() if ln else None
     y = _strided(torch.empty(inp.x.shape, dtype=DTYPES[y_dtype or inp.dtype]), pad + 8)
     y, h, mean, rstd = g.norm_fwd_ex(ln, x, gam, bet, inp.eps, residual=r, store_h=store_h, y=y)
+    vf = g.ex_last_variant(0)
     dy = _strided(inp.dy, pad)
     xb = h if h is not None else x
     if residual is not None and h is None:  # h not stored: the oracle's, for the backward
@@ -53,15 +56,19 @@ def run_ex(op, inp, pad=0, y_dtype=None, residual=None, dres=None, store_h=True)
     dr = _strided(dres, pad) if dres is not None else None
     dx = _strided(torch.empty(inp.x.shape, dtype=inp.x.dtype), pad + 16)
     dx, dg, db = g.norm_bwd_ex(ln, dy, xb, gam, mean, rstd, dres=dr, dx=dx)
+    vb = g.ex_last_variant(1)
     torch.cuda.synchronize()
-    N = inp.x.shape[1]
     out = {"y": y.cpu(), "rstd": rstd.cpu(), "dx": dx.cpu(), "dgamma": dg.cpu()}
     if ln:
         out.update(mean=mean.cpu(), dbeta=db.cpu())
     if h is not None:
         out["h"] = h.cpu()
-    vf = ex_variant(N, _vec(x, r, h, y) and gam.data_ptr() % 16 == 0)
-    vb = ex_variant(N, _vec(dy, xb, dr, dx), "bwd")
+    assert vf and vb
+    # the vector kernels hold rows of up to 16384 elements
+    N = inp.x.shape[1]
+    vec_f = _vec(x, r, h, y) and gam.data_ptr() % 16 == 0 and N % 8 == 0 and N <= 16384
+    vec_b = _vec(dy, xb, dr, dx) and N % 8 == 0 and N <= 16384
+    assert not check_path or ((vf != "exe") == vec_f and (vb != "exe") == vec_b), (vf, vb)
     return out, (vf, vb)
 
 
@@ -91,8 +98,6 @@ def test_strided_rows(op, dtype, N, pad):
     M = 129 if N <= 4096 else 9
     inp = make_inputs(M, N, dtype=dtype, dist="llm" if N >= 4096 else op, op=op)
     out, variants = run_ex(op, inp, pad=pad)
-    if (pad * inp.x.element_size()) % 16 == 0 and N % 8 == 0:
-        assert variants[0] != "exe" or N > 16384
     compare(op, inp, out, variants=variants).assert_ok()
 
 
@@ -153,16 +158,21 @@ def test_optional_parameters_and_empty(op):
     inp.beta = torch.zeros_like(inp.beta)
     x, dy = inp.x.cuda(), inp.dy.cuda()
     y, _, mean, rstd = g.norm_fwd_ex(ln, x, None, None, inp.eps)
+    vf = g.ex_last_variant(0)
     dx, dg, db = g.norm_bwd_ex(ln, dy, x, None, mean, rstd)
+    vb = g.ex_last_variant(1)
     torch.cuda.synchronize()
     out = {"y": y.cpu(), "rstd": rstd.cpu(), "dx": dx.cpu(), "dgamma": dg.cpu()}
     if ln:
         out.update(mean=mean.cpu(), dbeta=db.cpu())
-    compare(op, inp, out, variants=(ex_variant(N, True), ex_variant(N, True, "bwd"))).assert_ok()
+    assert vf.startswith("exrf") and vb.startswith("exrb"), (vf, vb)
+    compare(op, inp, out, variants=(vf, vb)).assert_ok()
     e = torch.empty(0, N, device="cuda", dtype=torch.bfloat16)
     dge = torch.full((N,), 5.0, device="cuda")
     _, _, me, re_ = g.norm_fwd_ex(ln, e, None, None, inp.eps)
+    assert g.ex_last_variant(0) == ""
     g.norm_bwd_ex(ln, e, e, None, me, re_, dgamma=dge)
+    assert g.ex_last_variant(1) == ""
     torch.cuda.synchronize()
     assert torch.all(dge == 0)
 
@@ -178,3 +188,91 @@ def test_ex_deterministic():
     torch.cuda.synchronize()
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+# Every general-form kernel (ring, register, element-wise), forced, on row
+# lengths inside its capacity: several tiles per CTA and a ragged last tile
+# (M prime), mixed types, strided rows, a residual add and dres.
+def _force_cases():
+    import rmsnorm_norm_fwd_gb300 as g
+    cases = []
+    for op in ("rms", "ln"):
+        for d, dn in ((0, "fwd"), (1, "bwd")):
+            for name in g.ex_variants(op == "ln", d):
+                m = re.fullmatch(r"exr?[fb](\d+)x(\d+)b(\d+)", name)
+                cap = int(m.group(1)) * int(m.group(2)) * 8 if m else 4096
+                cases.append((op, dn, name, cap))
+    return cases
+
+
+def _cases_or_empty():
+    try:
+        return _force_cases()
+    except Exception:  # library not built: collected as one skipped case
+        return [("rms", "fwd", "unbuilt", 0)]
+
+
+def _ring_fits(ln, d, name, M, N, xdt, ydt, pdt, extra):
+    """Whether the library's ring layout for `name` fits this call (the rule
+    the planner applies: about 16 KB of rows per stage, two stages per row
+    group at least, in the opt-in shared memory after the header and the
+    parameters)."""
+    es = {"fp32": 4, "bf16": 2, "fp16": 2}
+    m = re.fullmatch(r"exr[fb](\d+)x(\d+)b(\d+)", name)
+    tpr, vpt, nt = (int(v) for v in m.groups())
+    rpp = nt // tpr
+    al = lambda b: (b + 127) // 128 * 128  # noqa: E731
+    optin = torch.cuda.get_device_properties(0).shared_memory_per_block_optin
+    budget = optin - 2048 - al(N * es[pdt]) * (2 if d == 0 and ln else 1)
+
+    def stride(rt):
+        st = al(rt * N * es[xdt]) * (2 if extra else 1)
+        if d == 1:
+            st += al(rt * N * es[ydt]) + al(((rt + 7) & ~3) * 4 * (2 if ln else 1))
+        return st
+    per_row = N * es[xdt] * (2 if extra else 1) + (N * es[ydt] if d == 1 else 0)
+    rt = max(1, min(64, 16384 // per_row, M))
+    while rt > 1 and 2 * rpp * stride(rt) > budget:
+        rt //= 2
+    if 2 * rpp * stride(rt) > budget:
+        return False
+    stages = min(16, budget // stride(rt))
+    stages -= stages % rpp
+    ring = stages * stride(rt)
+    if d == 1 and rpp > 1:
+        ring = max(ring, nt * vpt * 8 * 4 * (2 if ln else 1))
+    return ring <= budget
+
+
+@pytest.mark.parametrize("op,direction,name,cap", _cases_or_empty(),
+                         ids=lambda v: str(v))
+@pytest.mark.parametrize("types", [("bf16", "fp32", "bf16", True), ("fp32", "bf16", "fp16", False)],
+                         ids=["bf16-fp32-extras", "fp32-bf16"])
+def test_forced_variant(op, direction, name, cap, types):
+    """Every general-form kernel, forced, at a row length inside its capacity,
+    several tiles per CTA with a ragged last tile, against the oracle; a ring
+    kernel whose layout cannot fit the call gives way to the usual choice."""
+    import rmsnorm_norm_fwd_gb300 as g
+    if name == "unbuilt":
+        pytest.skip("library not built")
+    ln = op == "ln"
+    d = 0 if direction == "fwd" else 1
+    xdt, pdt, ydt, extras = types
+    N = cap if cap <= 4096 else cap - 8 * 37  # fills the capacity, or leaves part of it empty
+    N = max(8, min(N, 16384))
+    M = 389 if N <= 4096 else 41
+    dist = "llm" if N >= 4096 else op
+    inp = make_inputs(M, N, dtype=xdt, dist=dist, op=op, param_dtype=pdt, dy_dtype=ydt)
+    res = make_inputs(M, N, dtype=xdt, dist="rms", op=op, seed=97).x if extras else None
+    dres = make_inputs(M, N, dtype=xdt, dist="rms", op=op, seed=96).dy if extras else None
+    g.ex_force_variant(ln, d, name)
+    try:
+        out, variants = run_ex(op, inp, pad=8, y_dtype=ydt, residual=res, dres=dres, check_path=False)
+    finally:
+        g.ex_force_variant(ln, d, None)
+    served = name == "exe" or not name.startswith("exr") or _ring_fits(ln, d, name, M, N, xdt, ydt, pdt, extras)
+    assert (variants[d] == name) == served, (variants, served)
+    inp_h = make_inputs(M, N, dtype=xdt, dist=dist, op=op, param_dtype=pdt, dy_dtype=ydt)
+    if extras:
+        inp_h.x = oracle.residual_add(inp.x, res, xdt)
+    compare(op, inp_h, out, variants=variants, y_dtype=ydt, dres=dres).assert_ok()

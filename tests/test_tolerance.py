@@ -5,6 +5,8 @@ rows of a full-size check include every row of the accumulation-stress recipe
 scaled by 100."""
 import numpy as np
 import pytest
+import re
+
 import torch
 
 import oracle
@@ -102,16 +104,18 @@ def test_sample_includes_scaled_rows():
     assert len(scaled) == 30 and scaled <= set(rows.tolist())
 
 
-def test_general_form_geometries_match_the_library():
-    """parity_util's lists of general-form geometries (which the tests use to
-    name the kernel that ran) are the ones compiled into the library."""
-    import os
-    import re
-    from parity_util import EX_GEOMS
-    src = open(os.path.join(os.path.dirname(os.path.dirname(__file__)), "rmsnorm_norm_fwd_gb300", "csrc",
-                            "inst_ex.cu")).read()
-    for macro, d in (("GBN_EXF_GEOMS", "fwd"), ("GBN_EXB_GEOMS", "bwd")):
-        block = src[src.index(f"#define {macro}(X)"):]
-        block = block[:block.index("\n\n")]
-        geoms = tuple(tuple(int(v) for v in m) for m in re.findall(r"X\((\d+), (\d+), (\d+), \d+\)", block))
-        assert geoms == EX_GEOMS[d], d
+def test_general_form_names_parse():
+    """Every general-form kernel the library holds has a name row_threads reads
+    (the tests derive each call's tolerance from the name of the kernel that
+    ran, as gbnorm_ex_last_variant reports it)."""
+    import rmsnorm_norm_fwd_gb300 as g
+    from parity_util import row_threads
+    for ln in (False, True):
+        for d in (0, 1):
+            names = g.ex_variants(ln, d)
+            assert names[-1] == "exe" and len(names) == len(set(names)) > 1
+            for name in names:
+                tpr, cl, elem = row_threads(name)
+                assert cl == 1 and elem == (name == "exe")
+                m = re.fullmatch(r"exr?[fb](\d+)x(\d+)b(\d+)", name)
+                assert elem or (m and int(m.group(1)) == tpr and int(m.group(3)) % tpr == 0)
