@@ -265,6 +265,31 @@ bool wider_geometry(const Variant &v, const CallShape &c, int dev, size_t *dyn_s
     return true;
 }
 
+// Shared-memory ring of a wcs variant (cluster slices resident in shared
+// memory): gamma (and beta, forward LayerNorm) slices in their storage type,
+// then S stages of one row's slice of x (and dy), S between 2 and 8 as room
+// allows.  False if a CTA of the cluster would get no columns, a slice
+// exceeds the per-thread capacity, or two stages do not fit.
+bool wcs_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, size_t *dyn_smem) {
+    const int64_t nv = c.N / v.elems_per_vec;
+    const int64_t slice = (nv + v.cl - 1) / v.cl;
+    if (slice > (int64_t)v.tpr * v.vpt || (int64_t)(v.cl - 1) * slice >= nv) return false;
+    const size_t sb = ex_al128((size_t)slice * 16u);
+    const size_t params = sb * ((c.dir == 0 && c.is_ln) ? 2u : 1u);
+    const size_t stage = sb * (c.dir == 1 ? 2u : 1u);
+    // room for the kernel's static shared memory (barriers, reductions, slots)
+    const size_t avail = (size_t)g_dev[dev].smem_optin - 4096;
+    if (avail < params + 2 * stage) return false;
+    int stages = (int)((avail - params) / stage);
+    if (stages > 8) stages = 8;
+    tc->rows = 1;
+    tc->stages = stages;
+    tc->stride = (uint32_t)stage;
+    tc->fault = g_dev[dev].fault;
+    *dyn_smem = params + (size_t)stages * stage;
+    return true;
+}
+
 // Shared memory of a wide-row variant: none for the forward; for the
 // backward each CTA's column slice of dgamma (and dbeta) sums in fp32.  False
 // if a CTA of the cluster would get no columns or the sums do not fit.
@@ -310,6 +335,11 @@ bool can_serve(const Variant &v, const CallShape &c, int dev) {
     if (v.kind == kWideR) {
         size_t dyn;
         return wider_geometry(v, c, dev, &dyn);
+    }
+    if (v.kind == kWcs) {
+        TileCfg tc;
+        size_t dyn;
+        return wcs_geometry(v, c, dev, &tc, &dyn);
     }
     if (v.kind == kRowsS) {
         size_t dyn;
@@ -399,13 +429,13 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
     const Variant &v = kTables[c.is_ln][c.dir][c.dtype]->v[idx];
     // Kinds whose shared memory (and so occupancy) depends on the shape.
     const bool per_shape = v.staged_rows() || v.kind == kRowsS || v.kind == kWtma || v.kind == kWtmaC ||
-                           v.kind == kWideR || (v.kind == kWide && dyn_smem > 0);
+                           v.kind == kWideR || v.kind == kWcs || (v.kind == kWide && dyn_smem > 0);
     if (o > 0 && !per_shape) {
         *out = o;
         return GBNORM_OK;
     }
     if (v.staged_rows() || v.kind == kTmaCl || v.kind == kRowsS || v.kind == kWtma || v.kind == kWtmaC ||
-        v.kind == kWideR || (v.kind == kWide && dyn_smem > 0)) {
+        v.kind == kWideR || v.kind == kWcs || (v.kind == kWide && dyn_smem > 0)) {
         std::atomic<uint64_t> &cache = g_occ_tma[dev][c.is_ln][c.dir][c.dtype][idx];
         const uint64_t hit = cache.load(std::memory_order_relaxed);
         if (hit != 0 && (hit >> 16) == (uint64_t)dyn_smem) {
@@ -488,6 +518,7 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
     if (v.kind == kWtma && !wtma_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kWtmaC && !wtmac_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kWideR && !wider_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
+    if (v.kind == kWcs && !wcs_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     int occ = 0;
     int st = occupancy(c, idx, dev, pl->dyn_smem, &occ);
     if (st != GBNORM_OK) return st;

@@ -500,6 +500,40 @@ __device__ __forceinline__ void par8(const unsigned char *row, bool present, int
     }
 }
 
+// The same chunk as four pairs (elements 2i, 2i + 1) for the two-lane fp32
+// operations.
+__device__ __forceinline__ void lds8p(const unsigned char *row, int64_t c, int dt, float2 (&f)[4]) {
+    if (dt == kF32) {
+        const uint4 a = lds128(row + 32 * c), b = lds128(row + 32 * c + 16);
+        f[0] = vpair<float>(a, 0);
+        f[1] = vpair<float>(a, 1);
+        f[2] = vpair<float>(b, 0);
+        f[3] = vpair<float>(b, 1);
+    } else {
+        const uint4 a = lds128(row + 16 * c);
+        if (dt == kBF16) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f[i] = vpair<__nv_bfloat16>(a, i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f[i] = vpair<__half>(a, i);
+        }
+    }
+}
+__device__ __forceinline__ void par8p(const unsigned char *row, bool present, int64_t c, int dt, float one,
+                                      float2 (&f)[4]) {
+    if (present) {
+        lds8p(row, c, dt, f);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f[i] = f2s(one);
+    }
+}
+__device__ __forceinline__ void st8p(void *row, int64_t off, int dt, const float2 (&f)[4]) {
+    const float o[8] = {f[0].x, f[0].y, f[1].x, f[1].y, f[2].x, f[2].y, f[3].x, f[3].y};
+    st8(row, off, dt, o);
+}
+
 // Rows [r0, r0 + rows) of a row tensor (row stride ld elements, row_bytes =
 // N * element size) into dst, packed at row_bytes: one copy when the rows are
 // dense, else one per row.  Every source row starts on a 16-byte boundary
@@ -592,42 +626,48 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
         for (int r = 0; r < rows; ++r) {  // every thread of the group works on the same row
             const int64_t row = r0 + r;
             const unsigned char *xs = tb + (size_t)r * xrb;
-            float xf[VPT][8];
+            float2 xf[VPT][4];
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int64_t c = (int64_t)k * TPR + t;
                 if (c < nc) {
-                    lds8(xs, c, p.xdt, xf[k]);
+                    lds8p(xs, c, p.xdt, xf[k]);
                     if (p.res) {
                         // h = x + r in fp32, rounded once to the storage type
-                        float r8[8];
-                        lds8(xs + xsec, c, p.xdt, r8);
+                        float2 r8[4];
+                        lds8p(xs + xsec, c, p.xdt, r8);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) xf[k][e] = round_to(xf[k][e] + r8[e], p.xdt);
-                        if (p.h) st8(row_ptr(p.h, row, p.ldh, p.xdt), 8 * c, p.xdt, xf[k]);
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 hs = f2add(xf[k][e], r8[e]);
+                            xf[k][e] = make_float2(round_to(hs.x, p.xdt), round_to(hs.y, p.xdt));
+                        }
+                        if (p.h) st8p(row_ptr(p.h, row, p.ldh, p.xdt), 8 * c, p.xdt, xf[k]);
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) xf[k][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) xf[k][e] = f2s(0.f);
                 }
             }
-            float acc = 0.f;
+            float2 a2 = f2s(0.f);
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc += LN ? xf[k][e] : xf[k][e] * xf[k][e];
+                for (int e = 0; e < 4; ++e) a2 = LN ? f2add(a2, xf[k][e]) : f2fma(xf[k][e], xf[k][e], a2);
+            float acc = a2.x + a2.y;
             float mean = 0.f;
             if (LN && full) {
                 constexpr float kC = (float)(VPT * 8);
                 mean = acc * (1.f / kC);
-                float m2 = 0.f;
+                const float2 nm = f2s(-mean);
+                float2 q2 = f2s(0.f);
 #pragma unroll
                 for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float d = xf[k][e] - mean;
-                        m2 += d * d;
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 d = f2add(xf[k][e], nm);
+                        q2 = f2fma(d, d, q2);
                     }
+                float m2 = q2.x + q2.y;
                 group_meanvar_equal<TPR>(mean, m2, kC, scratch, parity, 1 + grp);
                 acc = m2;
             } else {
@@ -636,16 +676,18 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
                 acc = a[0];
                 if constexpr (LN) {
                     mean = acc / n;
-                    a[0] = 0.f;
+                    const float2 nm = f2s(-mean);
+                    float2 q2 = f2s(0.f);
 #pragma unroll
                     for (int k = 0; k < VPT; ++k) {
                         if ((int64_t)k * TPR + t >= nc) continue;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float d = xf[k][e] - mean;
-                            a[0] += d * d;
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 d = f2add(xf[k][e], nm);
+                            q2 = f2fma(d, d, q2);
                         }
                     }
+                    a[0] = q2.x + q2.y;
                     group_allreduce<TPR, 1>(a, scratch, parity, 1 + grp);
                     acc = a[0];
                 }
@@ -661,21 +703,22 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
                 if (p.rstd) p.rstd[row] = rstd;
                 if (LN && p.mean) p.mean[row] = mean;
             }
+            const float2 nm = f2s(-mean), rs = f2s(rstd);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int64_t c = (int64_t)k * TPR + t;
                 if (c >= nc) continue;
-                float g[8], o[8];
-                par8(gsm, has_g, c, p.pdt, 1.f, g);
+                float2 g[4], o[4];
+                par8p(gsm, has_g, c, p.pdt, 1.f, g);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = ((xf[k][e] - mean) * rstd) * g[e];
+                for (int e = 0; e < 4; ++e) o[e] = f2mul(f2mul(f2add(xf[k][e], nm), rs), g[e]);
                 if constexpr (LN) {
-                    float b[8];
-                    par8(bsm, has_b, c, p.pdt, 0.f, b);
+                    float2 b[4];
+                    par8p(bsm, has_b, c, p.pdt, 0.f, b);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] += b[e];
+                    for (int e = 0; e < 4; ++e) o[e] = f2add(o[e], b[e]);
                 }
-                st8(row_ptr(p.y, row, p.ldy, p.ydt), 8 * c, p.ydt, o);
+                st8p(row_ptr(p.y, row, p.ldy, p.ydt), 8 * c, p.ydt, o);
             }
         }
     }
@@ -752,13 +795,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
 
     const float n = (float)p.N;
     const bool has_g = p.gamma != nullptr;
-    float accg[VPT][8], accb[LN ? VPT : 1][8];
+    // dgamma (and dbeta) sums of this thread's columns, as pairs
+    float2 accg[VPT][4], accb[LN ? VPT : 1][4];
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            accg[k][e] = 0.f;
-            if constexpr (LN) accb[k][e] = 0.f;
+        for (int e = 0; e < 4; ++e) {
+            accg[k][e] = f2s(0.f);
+            if constexpr (LN) accb[k][e] = f2s(0.f);
         }
     int parity = 0;
     // Trip count uniform over the CTA (the epilogue's barriers); groups past
@@ -782,35 +826,37 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
             const bool in_win = row < wb;
             const float rstd = in_win ? st[row] : __ldg(p.rstd + row);
             const float mean = LN ? (in_win ? st[exr_stat_floats(RT) + row] : __ldg(p.mean + row)) : 0.f;
-            float sum[NS];
-#pragma unroll
-            for (int q = 0; q < NS; ++q) sum[q] = 0.f;
-            float hx[HOLD ? VPT : 1][8], hg[HOLD ? VPT : 1][8], hd[HOLD ? VPT : 1][8];
+            const float2 nm = f2s(-mean);
+            float2 s2 = f2s(0.f), s1 = f2s(0.f);
+            float2 hx[HOLD ? VPT : 1][4], hg[HOLD ? VPT : 1][4], hd[HOLD ? VPT : 1][4];
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int64_t c = (int64_t)k * TPR + t;
-                float x8[8], d8[8], g8[8];
+                float2 x8[4], d8[4], g8[4];
                 if (c < nc) {
-                    lds8(xs, c, p.xdt, x8);
-                    lds8(ds, c, p.ydt, d8);
-                    par8(gsm, has_g, c, p.pdt, 1.f, g8);
+                    lds8p(xs, c, p.xdt, x8);
+                    lds8p(ds, c, p.ydt, d8);
+                    par8p(gsm, has_g, c, p.pdt, 1.f, g8);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x8[e] = d8[e] = g8[e] = 0.f;
+                    for (int e = 0; e < 4; ++e) x8[e] = d8[e] = g8[e] = f2s(0.f);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float xc = x8[e] - mean;
-                    const float gg = d8[e] * g8[e];
+                for (int e = 0; e < 4; ++e) {
+                    const float2 xc = f2add(x8[e], nm);
+                    const float2 gg = f2mul(d8[e], g8[e]);
                     if constexpr (HOLD) {
                         hx[k][e] = xc;
                         hg[k][e] = gg;
                         hd[k][e] = d8[e];
                     }
-                    sum[0] += gg * xc;
-                    if constexpr (LN) sum[NS - 1] += gg;
+                    s2 = f2fma(gg, xc, s2);
+                    if constexpr (LN) s1 = f2add(s1, gg);
                 }
             }
+            float sum[NS];
+            sum[0] = s2.x + s2.y;
+            if constexpr (LN) sum[NS - 1] = s1.x + s1.y;
             group_allreduce<TPR, NS>(sum, scratch, parity, 1 + grp);
             if (r == 0 && j >= 1 && t == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -820,43 +866,44 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
             const float c2 = rstd * sum[0] / n;
             const float rc1 = LN ? rstd * (sum[NS - 1] / n) : 0.f;
             const float rc2 = rstd * c2;
+            const float2 r2 = f2s(rstd), nrc1 = f2s(-rc1), nrc2 = f2s(-rc2);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int64_t c = (int64_t)k * TPR + t;
                 if (c >= nc) continue;
-                float xc[8], gg[8], dv[8], o[8];
+                float2 xc[4], gg[4], dv[4], o[4];
                 if constexpr (HOLD) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < 4; ++e) {
                         xc[e] = hx[k][e];
                         gg[e] = hg[k][e];
                         dv[e] = hd[k][e];
                     }
                 } else {
-                    float x8[8], g8[8];
-                    lds8(xs, c, p.xdt, x8);
-                    lds8(ds, c, p.ydt, dv);
-                    par8(gsm, has_g, c, p.pdt, 1.f, g8);
+                    float2 x8[4], g8[4];
+                    lds8p(xs, c, p.xdt, x8);
+                    lds8p(ds, c, p.ydt, dv);
+                    par8p(gsm, has_g, c, p.pdt, 1.f, g8);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        xc[e] = x8[e] - mean;
-                        gg[e] = dv[e] * g8[e];
+                    for (int e = 0; e < 4; ++e) {
+                        xc[e] = f2add(x8[e], nm);
+                        gg[e] = f2mul(dv[e], g8[e]);
                     }
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float xh = xc[e] * rstd;
-                    o[e] = fmaf(-rc2, xh, fmaf(rstd, gg[e], -rc1));
-                    accg[k][e] += dv[e] * xh;
-                    if constexpr (LN) accb[k][e] += dv[e];
+                for (int e = 0; e < 4; ++e) {
+                    const float2 xh = f2mul(xc[e], r2);
+                    o[e] = f2fma(nrc2, xh, f2fma(r2, gg[e], nrc1));
+                    accg[k][e] = f2fma(dv[e], xh, accg[k][e]);
+                    if constexpr (LN) accb[k][e] = f2add(accb[k][e], dv[e]);
                 }
                 if (p.dres) {
-                    float r8[8];
-                    lds8(tb + xsec + ysec + (size_t)r * xrb, c, p.xdt, r8);
+                    float2 r8[4];
+                    lds8p(tb + xsec + ysec + (size_t)r * xrb, c, p.xdt, r8);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] += r8[e];
+                    for (int e = 0; e < 4; ++e) o[e] = f2add(o[e], r8[e]);
                 }
-                st8(row_ptr(p.dx, row, p.lddx, p.xdt), 8 * c, p.xdt, o);
+                st8p(row_ptr(p.dx, row, p.lddx, p.xdt), 8 * c, p.xdt, o);
             }
         }
     }
@@ -874,10 +921,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = (k * TPR + t) * 8 + e;
-                comb[grp * CAP + c] = accg[k][e];
-                if constexpr (LN) comb[(RPP + grp) * CAP + c] = accb[k][e];
+            for (int e = 0; e < 4; ++e) {
+                const int c = (k * TPR + t) * 8 + 2 * e;
+                comb[grp * CAP + c] = accg[k][e].x;
+                comb[grp * CAP + c + 1] = accg[k][e].y;
+                if constexpr (LN) {
+                    comb[(RPP + grp) * CAP + c] = accb[k][e].x;
+                    comb[(RPP + grp) * CAP + c + 1] = accb[k][e].y;
+                }
             }
         __syncthreads();
         const int64_t ncol = p.N < CAP ? p.N : CAP;
@@ -898,11 +949,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
             if (c >= nc) continue;
             float4 *g4 = reinterpret_cast<float4 *>(wsg + 8 * c);
             float4 *b4 = reinterpret_cast<float4 *>(wsb + 8 * c);
-            g4[0] = make_float4(accg[k][0], accg[k][1], accg[k][2], accg[k][3]);
-            g4[1] = make_float4(accg[k][4], accg[k][5], accg[k][6], accg[k][7]);
+            g4[0] = make_float4(accg[k][0].x, accg[k][0].y, accg[k][1].x, accg[k][1].y);
+            g4[1] = make_float4(accg[k][2].x, accg[k][2].y, accg[k][3].x, accg[k][3].y);
             if constexpr (LN) {
-                b4[0] = make_float4(accb[k][0], accb[k][1], accb[k][2], accb[k][3]);
-                b4[1] = make_float4(accb[k][4], accb[k][5], accb[k][6], accb[k][7]);
+                b4[0] = make_float4(accb[k][0].x, accb[k][0].y, accb[k][1].x, accb[k][1].y);
+                b4[1] = make_float4(accb[k][2].x, accb[k][2].y, accb[k][3].x, accb[k][3].y);
             }
         }
     }

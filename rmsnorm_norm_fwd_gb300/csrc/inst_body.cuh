@@ -6,6 +6,7 @@
 #include "tma_cluster_kernels.cuh"
 #include "wide_kernels.cuh"
 #include "wtma_kernels.cuh"
+#include "wcs_kernels.cuh"
 #include "variants.inc"
 
 namespace gbn {
@@ -49,7 +50,13 @@ namespace gbn {
             ((CW) + 1) * 32, VecTraits<GBN_T>::E, 1, 0},
 #define GBN_WT_RMS(CW, U) GBN_WTMA(false, CW, U)
 #define GBN_WT_LN(CW, U) GBN_WTMA(true, CW, U)
+#define GBN_FWCS(LN, NT, VPT, CL)                                                              \
+    Variant{GBN_WCS_VNAME(NT, VPT, CL), (const void *)&fwd_wcs<GBN_T, LN, NT, VPT, CL>, kWcs, NT, VPT, 1, \
+            CL, NT, VecTraits<GBN_T>::E, 1, 0},
+#define GBN_FWCS_RMS(NT, VPT, CL) GBN_FWCS(false, NT, VPT, CL)
+#define GBN_FWCS_LN(NT, VPT, CL) GBN_FWCS(true, NT, VPT, CL)
 static const Variant rms_variants[] = {
+    GBN_WCS_GEOMS(GBN_FWCS_RMS)
     GBN_WTMA_FWD_GEOMS(GBN_WT_RMS)
     GBN_TMP_FWD_GEOMS(GBN_FP_RMS)
     GBN_TMA_FWD_GEOMS(GBN_T_RMS)
@@ -59,6 +66,7 @@ static const Variant rms_variants[] = {
     GBN_FWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
+    GBN_WCS_GEOMS(GBN_FWCS_LN)
     GBN_WTMA_FWD_GEOMS(GBN_WT_LN)
     GBN_TMP_FWD_GEOMS(GBN_FP_LN)
     GBN_TMA_FWD_GEOMS(GBN_T_LN)
@@ -90,6 +98,9 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_WTMA
 #undef GBN_WT_RMS
 #undef GBN_WT_LN
+#undef GBN_FWCS
+#undef GBN_FWCS_RMS
+#undef GBN_FWCS_LN
 #endif
 
 #ifdef GBN_BWD
@@ -140,7 +151,13 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
             kWideR, NT, K, 1, CL, NT, VecTraits<GBN_T>::E, MINB, 0},
 #define GBN_WR_RMS(NT, K, CL, PF, MINB, F) GBN_WIDER(false, NT, K, CL, PF, MINB, F)
 #define GBN_WR_LN(NT, K, CL, PF, MINB, F) GBN_WIDER(true, NT, K, CL, PF, MINB, F)
+#define GBN_BWCS(LN, NT, VPT, CL)                                                              \
+    Variant{GBN_WCS_VNAME(NT, VPT, CL), (const void *)&bwd_wcs<GBN_T, LN, NT, VPT, CL>, kWcs, NT, VPT, 1, \
+            CL, NT, VecTraits<GBN_T>::E, 1, 0},
+#define GBN_BWCS_RMS(NT, VPT, CL) GBN_BWCS(false, NT, VPT, CL)
+#define GBN_BWCS_LN(NT, VPT, CL) GBN_BWCS(true, NT, VPT, CL)
 static const Variant rms_variants[] = {
+    GBN_WCS_GEOMS(GBN_BWCS_RMS)
     GBN_WIDER_BWD_GEOMS(GBN_WR_RMS)
     GBN_BWTMA_BWD_GEOMS(GBN_BWT_RMS)
     GBN_TMA_BWD_GEOMS(GBN_T_RMS)
@@ -152,6 +169,7 @@ static const Variant rms_variants[] = {
     GBN_BWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&bwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
+    GBN_WCS_GEOMS(GBN_BWCS_LN)
     GBN_WIDER_BWD_GEOMS(GBN_WR_LN)
     GBN_BWTMA_BWD_GEOMS(GBN_BWT_LN)
     GBN_TMA_BWD_GEOMS(GBN_T_LN)
@@ -176,6 +194,9 @@ const VariantTable GBN_CAT(kBwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_WIDER
 #undef GBN_WR_RMS
 #undef GBN_WR_LN
+#undef GBN_BWCS
+#undef GBN_BWCS_RMS
+#undef GBN_BWCS_LN
 #undef GBN_SKTMA
 #undef GBN_SKT_RMS
 #undef GBN_SKT_LN

@@ -110,6 +110,7 @@ enum VariantKind : int {
     kWtma = 7,  // one CTA per row, the row streamed twice through a bulk-copy ring (forward)
     kWtmaC = 8, // column slices of a cluster streamed twice through a bulk-copy ring (backward)
     kWideR = 9, // as kWide (backward), the dgamma/dbeta sums in registers, gamma in shared memory
+    kWcs = 10,  // cluster column slices of each row resident in shared memory (bulk-copy ring)
 };
 
 // One compiled kernel and the geometry the host needs to launch it.

@@ -62,6 +62,10 @@ def _geom(name):
     if m:
         cl, k = (int(v) for v in m.groups())
         return ("bwtma", 512, k, cl)
+    m = re.fullmatch(r"wcs(\d+)v(\d+)c(\d+)", name)
+    if m:
+        nt, vpt, cl = (int(v) for v in m.groups())
+        return ("wcs", nt, vpt, cl)
     m = re.fullmatch(r"bwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)", name)
     if m:
         nt, k, cl, _, _, _ = (int(v) for v in m.groups())
@@ -125,6 +129,12 @@ def test_forced_variant(op, direction, dtype, variant):
         nt, k, cl = geo[1], geo[2], geo[3]
         cap = cl * k * nt * E
         shapes = [(9, cap), (9, cap - E), (7, cap // 2 + 3 * E), (5, cl * 3 * E), (3, (cl - 1) * E)]
+    elif geo[0] == "wcs":
+        # cluster slices resident in shared memory: full slices, one vector
+        # short, a ragged last slice, three vectors per CTA
+        nt, vpt, cl = geo[1], geo[2], geo[3]
+        cap = cl * vpt * nt * E
+        shapes = [(9, cap), (9, cap - E), (7, cap // 2 + 3 * E), (5, cl * 3 * E)]
     elif geo[0] == "wide":
         # any row length (per CTA of the cluster): two full load batches per
         # thread, one vector short of that, a slice where only part of the CTA
@@ -158,7 +168,7 @@ def test_forced_variant(op, direction, dtype, variant):
             while full > geo[3] * E and g.variant_name(op == "ln", 1, 9, full, dtype) != variant:
                 full //= 2
             shapes = [(9, full), (9, full - E)] + shapes[2:]
-        if geo is not None and geo[0] not in ("wide", "bwtma") and geo[5]:
+        if geo is not None and geo[0] not in ("wide", "bwtma", "wcs") and geo[5]:
             # A staged variant may hold fewer elements than its register
             # capacity when gamma/beta and two stages must fit in shared
             # memory: take the widest row it serves, at least a quarter of it.
@@ -490,6 +500,30 @@ def test_wide_ring_wraps(op, variant, limit):
     finally:
         g.set_grid_limit(0)
         g.force_variant(op == "ln", 0, "bf16", None)
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("direction", [0, 1])
+@pytest.mark.parametrize("variant,N", [("wcs512v4c8", 131072), ("wcs512v2c16", 131072 - 24),
+                                       ("wcs512v4c4", 65536 - 8 * 5), ("wcs512v4c8", 3000)])
+@pytest.mark.parametrize("limit", [1, 3])
+def test_wcs_ring_wraps(op, direction, variant, N, limit):
+    """The cluster kernels with row slices resident in shared memory, under a
+    grid cap (in clusters): each cluster walks many rows, so the ring stages
+    (refilled as each row's pass 2 ends), the pass order (pass 1 one row
+    ahead) and the four exchange slots go through many phases."""
+    import rmsnorm_norm_fwd_gb300 as g
+    cl = int(re.search(r"c(\d+)$", variant).group(1))
+    M = 29
+    try:
+        g.force_variant(op == "ln", direction, "bf16", variant)
+        g.set_grid_limit(limit * cl)
+        assert g.variant_name(op == "ln", direction, M, N, "bf16") == variant
+        rep, _, _ = run_case(op, "bf16", M, N)
+        rep.assert_ok()
+    finally:
+        g.set_grid_limit(0)
+        g.force_variant(op == "ln", direction, "bf16", None)
 
 
 @pytest.mark.parametrize("op", ["rms", "ln"])
