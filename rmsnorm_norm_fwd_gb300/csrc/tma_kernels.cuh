@@ -424,18 +424,16 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
     const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
     float *scratch = h.red + grp * (2 * NS * WPR);
     // gamma of vector v of this thread's columns, as E floats.
-    auto gamma_of = [&](int v, float (&g)[E]) {
+    auto gamma_of = [&](int v, float2 (&g)[E / 2]) {
 #pragma unroll
         for (int hh = 0; hh < H; ++hh) {
             const float4 q = gpar[hh * nv + v];
-            g[4 * hh] = q.x;
-            g[4 * hh + 1] = q.y;
-            g[4 * hh + 2] = q.z;
-            g[4 * hh + 3] = q.w;
+            g[2 * hh] = make_float2(q.x, q.y);
+            g[2 * hh + 1] = make_float2(q.z, q.w);
         }
     };
     // HOLD: this thread's gamma, kept in registers (its columns never change).
-    float gf[HOLD ? VPT : 1][E];
+    float2 gf[HOLD ? VPT : 1][E / 2];
     if constexpr (HOLD) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -444,18 +442,19 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
                 gamma_of(v, gf[k]);
             } else {
 #pragma unroll
-                for (int e = 0; e < E; ++e) gf[k][e] = 0.f;
+                for (int e = 0; e < E / 2; ++e) gf[k][e] = f2s(0.f);
             }
         }
     }
     const float n = (float)p.N;
-    float accg[VPT][E], accb[LN ? VPT : 1][E];
+    // dgamma (and dbeta) partials of this thread's columns, as pairs
+    float2 accg[VPT][E / 2], accb[LN ? VPT : 1][E / 2];
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            accg[k][e] = 0.f;
-            if constexpr (LN) accb[k][e] = 0.f;
+        for (int e = 0; e < E / 2; ++e) {
+            accg[k][e] = f2s(0.f);
+            if constexpr (LN) accb[k][e] = f2s(0.f);
         }
     volatile int *abort_flag = &h.abort;
     int parity = 0, it = 0;
@@ -486,10 +485,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
             // sum g xhat = rstd * sum g (x - mean).  With at most 24 elements
             // per thread (HOLD) x - mean, g and the raw dy stay in registers for
             // pass 2; otherwise pass 2 re-reads the staged row.
-            float sum[NS];
-#pragma unroll
-            for (int i = 0; i < NS; ++i) sum[i] = 0.f;
-            float hx[HOLD ? VPT : 1][E], hg[HOLD ? VPT : 1][E];
+            const float2 nm = f2s(-mean);
+            float2 s2 = f2s(0.f), s1 = f2s(0.f);
+            float2 hx[HOLD ? VPT : 1][E / 2], hg[HOLD ? VPT : 1][E / 2];
             uint4 hd[HOLD ? VPT : 1];
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
@@ -497,29 +495,32 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
                 const bool ok = rok && v < nv;
                 const uint4 q = ok ? lds128(xs + v) : make_uint4(0, 0, 0, 0);
                 const uint4 d = ok ? lds128(ds + v) : make_uint4(0, 0, 0, 0);
-                float gk[E];
+                float2 gk[E / 2];
                 if constexpr (HOLD) {
                     hd[k] = d;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) gk[e] = gf[HOLD ? k : 0][e];
+                    for (int e = 0; e < E / 2; ++e) gk[e] = gf[HOLD ? k : 0][e];
                 } else if (ok) {
                     gamma_of(v, gk);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < E; ++e) gk[e] = 0.f;
+                    for (int e = 0; e < E / 2; ++e) gk[e] = f2s(0.f);
                 }
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float xc = vget<T>(q, e) - mean;
-                    const float gg = vget<T>(d, e) * gk[e];
+                for (int e = 0; e < E / 2; ++e) {
+                    const float2 xc = f2add(vpair<T>(q, e), nm);
+                    const float2 gg = f2mul(vpair<T>(d, e), gk[e]);
                     if constexpr (HOLD) {
                         hx[k][e] = xc;
                         hg[k][e] = gg;
                     }
-                    sum[0] += gg * xc;
-                    if constexpr (LN) sum[NS - 1] += gg;
+                    s2 = f2fma(gg, xc, s2);
+                    if constexpr (LN) s1 = f2add(s1, gg);
                 }
             }
+            float sum[NS];
+            sum[0] = s2.x + s2.y;
+            if constexpr (LN) sum[NS - 1] = s1.x + s1.y;
             group_allreduce<TPR, NS>(sum, scratch, parity, 1 + grp);
             if (!rok) continue;  // uniform per row group: no collective below
             // dx = rstd (g - c1 - xhat c2) = rstd g - rstd c1 - (rstd c2) xhat,
@@ -527,35 +528,35 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
             const float c2 = rstd * sum[0] / n;
             const float rc1 = LN ? rstd * (sum[NS - 1] / n) : 0.f;
             const float rc2 = rstd * c2;
+            const float2 r2 = f2s(rstd), nrc1 = f2s(-rc1), nrc2 = f2s(-rc2);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * TPR + t;
                 if (v >= nv) continue;
-                float o[E];
+                float2 o[E / 2];
                 if constexpr (HOLD) {
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float dyv = vget<T>(hd[k], e);
-                        const float xh = hx[k][e] * rstd;
-                        o[e] = fmaf(-rc2, xh, fmaf(rstd, hg[k][e], -rc1));
-                        accg[k][e] += dyv * xh;
-                        if constexpr (LN) accb[k][e] += dyv;
+                    for (int e = 0; e < E / 2; ++e) {
+                        const float2 dyv = vpair<T>(hd[k], e);
+                        const float2 xh = f2mul(hx[k][e], r2);
+                        o[e] = f2fma(nrc2, xh, f2fma(r2, hg[k][e], nrc1));
+                        accg[k][e] = f2fma(dyv, xh, accg[k][e]);
+                        if constexpr (LN) accb[k][e] = f2add(accb[k][e], dyv);
                     }
                 } else {
                     const uint4 q = lds128(xs + v), d = lds128(ds + v);
-                    float gk[E];
+                    float2 gk[E / 2];
                     gamma_of(v, gk);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float xh = (vget<T>(q, e) - mean) * rstd;
-                        const float dyv = vget<T>(d, e);
-                        const float gg = dyv * gk[e];
-                        o[e] = fmaf(-rc2, xh, fmaf(rstd, gg, -rc1));
-                        accg[k][e] += dyv * xh;
-                        if constexpr (LN) accb[k][e] += dyv;
+                    for (int e = 0; e < E / 2; ++e) {
+                        const float2 xh = f2mul(f2add(vpair<T>(q, e), nm), r2);
+                        const float2 dyv = vpair<T>(d, e);
+                        o[e] = f2fma(nrc2, xh, f2fma(r2, f2mul(dyv, gk[e]), nrc1));
+                        accg[k][e] = f2fma(dyv, xh, accg[k][e]);
+                        if constexpr (LN) accb[k][e] = f2add(accb[k][e], dyv);
                     }
                 }
-                st_vec(p.dx, row * nv + v, vpack<T>(o));
+                st_vec(p.dx, row * nv + v, vpack2<T>(o));
             }
         }
         __syncwarp();
@@ -575,10 +576,14 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const int c = (k * TPR + t) * E + e;
-                comb[grp * CAP + c] = accg[k][e];
-                if constexpr (LN) comb[(RPP + grp) * CAP + c] = accb[k][e];
+            for (int e = 0; e < E / 2; ++e) {
+                const int c = (k * TPR + t) * E + 2 * e;
+                comb[grp * CAP + c] = accg[k][e].x;
+                comb[grp * CAP + c + 1] = accg[k][e].y;
+                if constexpr (LN) {
+                    comb[(RPP + grp) * CAP + c] = accb[k][e].x;
+                    comb[(RPP + grp) * CAP + c + 1] = accb[k][e].y;
+                }
             }
         named_sync(kTmaBarAll, NT);
         const int64_t ncol = nv * E < CAP ? nv * E : CAP;
@@ -598,9 +603,13 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) bwd_tma(const BwdParams p) {
             const int64_t v = (int64_t)k * TPR + t;
             if (v >= nv) continue;
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                wsg[v * E + e] = accg[k][e];
-                if constexpr (LN) wsb[v * E + e] = accb[k][e];
+            for (int e = 0; e < E / 2; ++e) {
+                wsg[v * E + 2 * e] = accg[k][e].x;
+                wsg[v * E + 2 * e + 1] = accg[k][e].y;
+                if constexpr (LN) {
+                    wsb[v * E + 2 * e] = accb[k][e].x;
+                    wsb[v * E + 2 * e + 1] = accb[k][e].y;
+                }
             }
         }
     }
@@ -690,31 +699,34 @@ __global__ void __launch_bounds__(NT, 1) fwd_tmp(const FwdParams p) {
         for (int r = 0; r < rows; ++r) {  // every thread of the group works on the same row
             const uint4 *xs = reinterpret_cast<const uint4 *>(tb + (size_t)r * row_bytes);
             const int64_t row = r0 + r;
-            float xf[VPT][E];
+            float2 xf[VPT][E / 2];  // the row's elements of this thread, as pairs
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * TPR + t;
                 const uint4 q = v < nv ? lds128(xs + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int e = 0; e < E; ++e) xf[k][e] = vget<T>(q, e);
+                for (int e = 0; e < E / 2; ++e) xf[k][e] = vpair<T>(q, e);
             }
-            float acc = 0.f;
+            float2 a2 = f2s(0.f);
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc += LN ? xf[k][e] : xf[k][e] * xf[k][e];
+                for (int e = 0; e < E / 2; ++e) a2 = LN ? f2add(a2, xf[k][e]) : f2fma(xf[k][e], xf[k][e], a2);
+            float acc = a2.x + a2.y;
             float mean = 0.f;
             if (LN && full) {
                 constexpr float kC = (float)(VPT * E);
                 mean = acc * (1.f / kC);
-                float m2 = 0.f;
+                const float2 nm = f2s(-mean);
+                float2 q2 = f2s(0.f);
 #pragma unroll
                 for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float d = xf[k][e] - mean;
-                        m2 += d * d;
+                    for (int e = 0; e < E / 2; ++e) {
+                        const float2 d = f2add(xf[k][e], nm);
+                        q2 = f2fma(d, d, q2);
                     }
+                float m2 = q2.x + q2.y;
                 group_meanvar_equal<TPR>(mean, m2, kC, scratch, parity, 1 + grp);
                 acc = m2;
             } else {
@@ -723,16 +735,18 @@ __global__ void __launch_bounds__(NT, 1) fwd_tmp(const FwdParams p) {
                 acc = a[0];
                 if constexpr (LN) {
                     mean = acc / n;
-                    a[0] = 0.f;
+                    const float2 nm = f2s(-mean);
+                    float2 q2 = f2s(0.f);
 #pragma unroll
                     for (int k = 0; k < VPT; ++k) {
                         if (k * TPR + t >= nv) continue;
 #pragma unroll
-                        for (int e = 0; e < E; ++e) {
-                            const float d = xf[k][e] - mean;
-                            a[0] += d * d;
+                        for (int e = 0; e < E / 2; ++e) {
+                            const float2 d = f2add(xf[k][e], nm);
+                            q2 = f2fma(d, d, q2);
                         }
                     }
+                    a[0] = q2.x + q2.y;
                     group_allreduce<TPR, 1>(a, scratch, parity, 1 + grp);
                     acc = a[0];
                 }
@@ -749,27 +763,24 @@ __global__ void __launch_bounds__(NT, 1) fwd_tmp(const FwdParams p) {
                 if (p.rstd) p.rstd[row] = rstd;
                 if (LN && p.mean) p.mean[row] = mean;
             }
+            const float2 nm = f2s(-mean), rs = f2s(rstd);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * TPR + t;
                 if (v >= nv) continue;
-                float o[E];
+                float2 o[E / 2];
 #pragma unroll
                 for (int hh = 0; hh < H; ++hh) {
                     const float4 g = gpar[hh * nv + v];
-                    o[4 * hh] = ((xf[k][4 * hh] - mean) * rstd) * g.x;
-                    o[4 * hh + 1] = ((xf[k][4 * hh + 1] - mean) * rstd) * g.y;
-                    o[4 * hh + 2] = ((xf[k][4 * hh + 2] - mean) * rstd) * g.z;
-                    o[4 * hh + 3] = ((xf[k][4 * hh + 3] - mean) * rstd) * g.w;
+                    o[2 * hh] = f2mul(f2mul(f2add(xf[k][2 * hh], nm), rs), make_float2(g.x, g.y));
+                    o[2 * hh + 1] = f2mul(f2mul(f2add(xf[k][2 * hh + 1], nm), rs), make_float2(g.z, g.w));
                     if constexpr (LN) {
                         const float4 b = bpar[hh * nv + v];
-                        o[4 * hh] += b.x;
-                        o[4 * hh + 1] += b.y;
-                        o[4 * hh + 2] += b.z;
-                        o[4 * hh + 3] += b.w;
+                        o[2 * hh] = f2add(o[2 * hh], make_float2(b.x, b.y));
+                        o[2 * hh + 1] = f2add(o[2 * hh + 1], make_float2(b.z, b.w));
                     }
                 }
-                st_vec(p.y, row * nv + v, vpack<T>(o));
+                st_vec(p.y, row * nv + v, vpack2<T>(o));
             }
         }
     }
@@ -861,17 +872,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
                                            vget<T>(g, 4 * hh + 3));
     }
     __syncthreads();
-    auto gamma_of = [&](int v, float (&g)[E]) {
+    // gamma of vector v of this thread's columns, as E / 2 pairs
+    auto gamma_of = [&](int v, float2 (&g)[E / 2]) {
 #pragma unroll
         for (int hh = 0; hh < H; ++hh) {
             const float4 q = gpar[hh * nv + v];
-            g[4 * hh] = q.x;
-            g[4 * hh + 1] = q.y;
-            g[4 * hh + 2] = q.z;
-            g[4 * hh + 3] = q.w;
+            g[2 * hh] = make_float2(q.x, q.y);
+            g[2 * hh + 1] = make_float2(q.z, q.w);
         }
     };
-    float gf[HOLD ? VPT : 1][E];
+    float2 gf[HOLD ? VPT : 1][E / 2];
     if constexpr (HOLD) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -880,18 +890,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
                 gamma_of(v, gf[k]);
             } else {
 #pragma unroll
-                for (int e = 0; e < E; ++e) gf[k][e] = 0.f;
+                for (int e = 0; e < E / 2; ++e) gf[k][e] = f2s(0.f);
             }
         }
     }
     const float n = (float)p.N;
-    float accg[VPT][E], accb[LN ? VPT : 1][E];
+    float2 accg[VPT][E / 2], accb[LN ? VPT : 1][E / 2];
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            accg[k][e] = 0.f;
-            if constexpr (LN) accb[k][e] = 0.f;
+        for (int e = 0; e < E / 2; ++e) {
+            accg[k][e] = f2s(0.f);
+            if constexpr (LN) accb[k][e] = f2s(0.f);
         }
     int parity = 0;
     // Trip count uniform over the CTA (the epilogue's barriers); groups past
@@ -915,10 +925,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
             const bool in_win = row < wb;
             const float rstd = in_win ? st[row] : __ldg(p.rstd + row);
             const float mean = LN ? (in_win ? st[stat_stride(RT) + row] : __ldg(p.mean + row)) : 0.f;
-            float sum[NS];
-#pragma unroll
-            for (int q = 0; q < NS; ++q) sum[q] = 0.f;
-            float hx[HOLD ? VPT : 1][E], hg[HOLD ? VPT : 1][E];
+            const float2 nm = f2s(-mean);
+            float2 s2 = f2s(0.f), s1 = f2s(0.f);
+            float2 hx[HOLD ? VPT : 1][E / 2], hg[HOLD ? VPT : 1][E / 2];
             uint4 hd[HOLD ? VPT : 1];
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
@@ -926,29 +935,32 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
                 const bool ok = v < nv;
                 const uint4 q = ok ? lds128(xs + v) : make_uint4(0, 0, 0, 0);
                 const uint4 d = ok ? lds128(ds + v) : make_uint4(0, 0, 0, 0);
-                float gk[E];
+                float2 gk[E / 2];
                 if constexpr (HOLD) {
                     hd[k] = d;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) gk[e] = gf[HOLD ? k : 0][e];
+                    for (int e = 0; e < E / 2; ++e) gk[e] = gf[HOLD ? k : 0][e];
                 } else if (ok) {
                     gamma_of(v, gk);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < E; ++e) gk[e] = 0.f;
+                    for (int e = 0; e < E / 2; ++e) gk[e] = f2s(0.f);
                 }
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float xc = vget<T>(q, e) - mean;
-                    const float gg = vget<T>(d, e) * gk[e];
+                for (int e = 0; e < E / 2; ++e) {
+                    const float2 xc = f2add(vpair<T>(q, e), nm);
+                    const float2 gg = f2mul(vpair<T>(d, e), gk[e]);
                     if constexpr (HOLD) {
                         hx[k][e] = xc;
                         hg[k][e] = gg;
                     }
-                    sum[0] += gg * xc;
-                    if constexpr (LN) sum[NS - 1] += gg;
+                    s2 = f2fma(gg, xc, s2);
+                    if constexpr (LN) s1 = f2add(s1, gg);
                 }
             }
+            float sum[NS];
+            sum[0] = s2.x + s2.y;
+            if constexpr (LN) sum[NS - 1] = s1.x + s1.y;
             group_allreduce<TPR, NS>(sum, scratch, parity, 1 + grp);
             if (r == 0 && j >= 1 && t == 0) {
                 // Every thread of the group is past its last read of the
@@ -960,34 +972,35 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
             const float c2 = rstd * sum[0] / n;
             const float rc1 = LN ? rstd * (sum[NS - 1] / n) : 0.f;
             const float rc2 = rstd * c2;
+            const float2 r2 = f2s(rstd), nrc1 = f2s(-rc1), nrc2 = f2s(-rc2);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * TPR + t;
                 if (v >= nv) continue;
-                float o[E];
+                float2 o[E / 2];
                 if constexpr (HOLD) {
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float dyv = vget<T>(hd[k], e);
-                        const float xh = hx[k][e] * rstd;
-                        o[e] = fmaf(-rc2, xh, fmaf(rstd, hg[k][e], -rc1));
-                        accg[k][e] += dyv * xh;
-                        if constexpr (LN) accb[k][e] += dyv;
+                    for (int e = 0; e < E / 2; ++e) {
+                        const float2 dyv = vpair<T>(hd[k], e);
+                        const float2 xh = f2mul(hx[k][e], r2);
+                        o[e] = f2fma(nrc2, xh, f2fma(r2, hg[k][e], nrc1));
+                        accg[k][e] = f2fma(dyv, xh, accg[k][e]);
+                        if constexpr (LN) accb[k][e] = f2add(accb[k][e], dyv);
                     }
                 } else {
                     const uint4 q = lds128(xs + v), d = lds128(ds + v);
-                    float gk[E];
+                    float2 gk[E / 2];
                     gamma_of(v, gk);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float xh = (vget<T>(q, e) - mean) * rstd;
-                        const float dyv = vget<T>(d, e);
-                        o[e] = fmaf(-rc2, xh, fmaf(rstd, dyv * gk[e], -rc1));
-                        accg[k][e] += dyv * xh;
-                        if constexpr (LN) accb[k][e] += dyv;
+                    for (int e = 0; e < E / 2; ++e) {
+                        const float2 xh = f2mul(f2add(vpair<T>(q, e), nm), r2);
+                        const float2 dyv = vpair<T>(d, e);
+                        o[e] = f2fma(nrc2, xh, f2fma(r2, f2mul(dyv, gk[e]), nrc1));
+                        accg[k][e] = f2fma(dyv, xh, accg[k][e]);
+                        if constexpr (LN) accb[k][e] = f2add(accb[k][e], dyv);
                     }
                 }
-                st_vec(p.dx, row * nv + v, vpack<T>(o));
+                st_vec(p.dx, row * nv + v, vpack2<T>(o));
             }
         }
     }
@@ -1012,10 +1025,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const int c = (k * TPR + t) * E + e;
-                comb[grp * CAP + c] = accg[k][e];
-                if constexpr (LN) comb[(RPP + grp) * CAP + c] = accb[k][e];
+            for (int e = 0; e < E / 2; ++e) {
+                const int c = (k * TPR + t) * E + 2 * e;
+                comb[grp * CAP + c] = accg[k][e].x;
+                comb[grp * CAP + c + 1] = accg[k][e].y;
+                if constexpr (LN) {
+                    comb[(RPP + grp) * CAP + c] = accb[k][e].x;
+                    comb[(RPP + grp) * CAP + c + 1] = accb[k][e].y;
+                }
             }
         __syncthreads();
         const int64_t ncol = nv * E < CAP ? nv * E : CAP;
@@ -1038,10 +1055,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_tmp(const BwdParams p) {
             float4 *b4 = reinterpret_cast<float4 *>(wsb + v * E);
 #pragma unroll
             for (int hh = 0; hh < H; ++hh) {
-                g4[hh] = make_float4(accg[k][4 * hh], accg[k][4 * hh + 1], accg[k][4 * hh + 2], accg[k][4 * hh + 3]);
+                g4[hh] = make_float4(accg[k][2 * hh].x, accg[k][2 * hh].y, accg[k][2 * hh + 1].x,
+                                     accg[k][2 * hh + 1].y);
                 if constexpr (LN)
-                    b4[hh] = make_float4(accb[k][4 * hh], accb[k][4 * hh + 1], accb[k][4 * hh + 2],
-                                         accb[k][4 * hh + 3]);
+                    b4[hh] = make_float4(accb[k][2 * hh].x, accb[k][2 * hh].y, accb[k][2 * hh + 1].x,
+                                         accb[k][2 * hh + 1].y);
             }
         }
     }

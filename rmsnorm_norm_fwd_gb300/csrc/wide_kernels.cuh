@@ -661,7 +661,11 @@ namespace gbn {
 // FUSE: 1 pass 1 of row j in the same sweep as pass 2 of row j - 2 (both
 // rows' loads in flight together); 0 pass 1 of row k + 1, the exchange of row
 // k, then pass 2 of row k.
-template <typename T, bool LN, int NT, int K, int CL, int PF, int MINB, int FUSE>
+// DB (LayerNorm): 1 the dbeta sums in shared memory (each thread's own fp32
+// plane entries, a read-modify-write per vector) and gamma kept there in its
+// storage type, which frees K * E registers for a larger K or a second CTA
+// per SM; 0 both sums in registers, gamma widened to fp32.
+template <typename T, bool LN, int NT, int K, int CL, int PF, int MINB, int FUSE, int DB = 0>
 __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     pdl_launch_dependents();  // the column reduce waits for this grid's completion
     constexpr int E = VecTraits<T>::E;
@@ -671,7 +675,10 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     constexpr int NS = 4;
     constexpr int KB = FUSE ? (K < 2 ? K : 2) : (K < 4 ? K : 4);  // vectors per tensor per batch
     static_assert(NT % 32 == 0 && NT <= 1024 && CL >= 1 && CL <= 16 && K % KB == 0, "shape");
-    extern __shared__ __align__(16) float4 gsm[];  // gamma of the slice, [H][K * NT] float4
+    static_assert(!DB || LN, "dbeta sums only for LayerNorm");
+    // gamma of the slice: [H][K * NT] float4 (DB: [K * NT] raw vectors), then
+    // (DB) the dbeta sums [H][K * NT] float4
+    extern __shared__ __align__(16) float4 gsm[];
     __shared__ float red[2][NVAL][W];
     __shared__ float slot[NS][CL][NVAL];
     __shared__ __align__(8) uint64_t xch[NS];
@@ -689,14 +696,22 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
     constexpr int KNT = K * NT;
 
+    uint4 *graw = reinterpret_cast<uint4 *>(gsm);
+    float4 *dbs = gsm + KNT;  // DB: this slice's dbeta sums
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const int64_t lv = (int64_t)k * NT + t;
         const uint4 g = lv < cnt ? param_vec<T>(p.gamma, v0 + lv, true) : make_uint4(0, 0, 0, 0);
+        if constexpr (DB) {
+            graw[lv] = g;
 #pragma unroll
-        for (int h = 0; h < H; ++h)
-            gsm[h * KNT + lv] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
-                                            vget<T>(g, 4 * h + 3));
+            for (int h = 0; h < H; ++h) dbs[h * KNT + lv] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+#pragma unroll
+            for (int h = 0; h < H; ++h)
+                gsm[h * KNT + lv] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
+                                                vget<T>(g, 4 * h + 3));
+        }
     }
     if (t == 0) {
         abort_flag = 0;
@@ -710,13 +725,13 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     else __syncthreads();
 
     // dgamma (and dbeta) sums of this thread's columns, as pairs of elements
-    float2 accg[K][E / 2], accb[LN ? K : 1][E / 2];
+    float2 accg[K][E / 2], accb[(LN && !DB) ? K : 1][E / 2];
 #pragma unroll
     for (int k = 0; k < K; ++k)
 #pragma unroll
         for (int e = 0; e < E / 2; ++e) {
             accg[k][e] = f2s(0.f);
-            if constexpr (LN) accb[k][e] = f2s(0.f);
+            if constexpr (LN && !DB) accb[k][e] = f2s(0.f);
         }
 
     const int64_t nrows = cid < M ? (M - cid + ncl - 1) / ncl : 0;
@@ -731,11 +746,17 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     };
     auto gam = [&](int k, float2 (&g)[E / 2]) {
         const int64_t lv = (int64_t)k * NT + t;
+        if constexpr (DB) {
+            const uint4 q = graw[lv];
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-            const float4 q = gsm[h * KNT + lv];
-            g[2 * h] = make_float2(q.x, q.y);
-            g[2 * h + 1] = make_float2(q.z, q.w);
+            for (int e = 0; e < E / 2; ++e) g[e] = vpair<T>(q, e);
+        } else {
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const float4 q = gsm[h * KNT + lv];
+                g[2 * h] = make_float2(q.x, q.y);
+                g[2 * h + 1] = make_float2(q.z, q.w);
+            }
         }
     };
     int parity = 0;
@@ -832,7 +853,17 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
                         // dx = rstd g - rstd c1 - (rstd c2) xhat
                         o[e] = f2fma(nrc2, xh, f2fma(r2, f2mul(dyv, g[e]), nrc1));
                         accg[kb + i][e] = f2fma(dyv, xh, accg[kb + i][e]);  // zero past the slice (dy = 0)
-                        if constexpr (LN) accb[kb + i][e] = f2add(accb[kb + i][e], dyv);
+                        if constexpr (LN && !DB) accb[kb + i][e] = f2add(accb[kb + i][e], dyv);
+                    }
+                    if constexpr (DB) {
+                        // this thread's own dbeta entries: no other thread touches them
+#pragma unroll
+                        for (int h = 0; h < H; ++h) {
+                            float4 &b4 = dbs[h * KNT + lv];
+                            const float2 lo = f2add(make_float2(b4.x, b4.y), vpair<T>(qd[i], 2 * h));
+                            const float2 hi = f2add(make_float2(b4.z, b4.w), vpair<T>(qd[i], 2 * h + 1));
+                            b4 = make_float4(lo.x, lo.y, hi.x, hi.y);
+                        }
                     }
                     if (lv < cnt) st_l2hint(dx2 + lv, vpack2<T>(o), drop);
                 }
@@ -896,7 +927,9 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
         for (int h = 0; h < H; ++h) {
             reinterpret_cast<float4 *>(wsg + lv * E)[h] =
                 make_float4(accg[k][2 * h].x, accg[k][2 * h].y, accg[k][2 * h + 1].x, accg[k][2 * h + 1].y);
-            if constexpr (LN)
+            if constexpr (LN && DB)
+                reinterpret_cast<float4 *>(wsb + lv * E)[h] = dbs[h * KNT + lv];
+            else if constexpr (LN)
                 reinterpret_cast<float4 *>(wsb + lv * E)[h] =
                     make_float4(accb[k][2 * h].x, accb[k][2 * h].y, accb[k][2 * h + 1].x, accb[k][2 * h + 1].y);
         }
