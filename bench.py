@@ -71,8 +71,8 @@ L2_CLEAN_BYTES = 512 << 20
 # occupancy and launch code that decides how the kernel runs.
 ROOFLINE_SOURCES = ("tma_kernels.cuh", "device_common.cuh", "params.h",
                     ("api.cu", "// ------------------------------------------------------------------ argument checks"))
-NCU_TRAFFIC = {"sources_digest": "03c3dfef26610b70", "variant": "tma128x2w8", "N": 2048,
-               "bytes_per_launch": 537188608 + 231839488}
+NCU_TRAFFIC = {"sources_digest": "73913f5206b7585e", "variant": "sktma128x2w8", "N": 2048,
+               "bytes_per_launch": 537220352 + 231536896}
 
 
 # The other workloads of the path, each timed per shape and direction inside

@@ -731,9 +731,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
     constexpr int NS = LN ? 2 : 1;
     constexpr int RPP = NT / TPR;
     constexpr int WPR = TPR / 32;
-    // pass-1 values kept in registers for pass 2 (as long as the dgamma/dbeta
-    // sums leave room for them)
-    constexpr bool HOLD = LN ? VPT == 1 : VPT <= 2;
+    // pass-1 values kept in registers for pass 2 where the dgamma/dbeta sums
+    // leave room for them (LayerNorm: two chunks only with one row group per
+    // CTA, whose scratch addressing is simplest; otherwise they spill)
+    constexpr bool HOLD = LN ? (VPT == 1 || (VPT == 2 && TPR == NT)) : VPT <= 2;
     static_assert(NT % TPR == 0 && TPR % 32 == 0 && TPR > 32 && 2 * RPP <= kExRingMaxStages, "CTA shape");
     static_assert(RPP * 2 * NS * WPR <= (int)(sizeof(ExRingHeader::red) / 4), "scratch");
     extern __shared__ __align__(128) unsigned char smem[];

@@ -29,13 +29,16 @@ namespace gbn {
 
 // Ring kernels (TPR, VPT, NT): one CTA of NT threads per SM, NT / TPR row
 // groups; capacity TPR * VPT * 8 elements.  Tried before the register
-// kernels.
+// kernels, in this order (512 x 2 after 256 x 4: the same capacity, measured
+// slower, but one row group needs only two stages where two groups' four do
+// not fit).
 #define GBN_EXR_GEOMS(X) \
     X(64, 1, 512)        \
     X(64, 2, 512)        \
     X(128, 2, 512)       \
     X(128, 4, 512)       \
     X(256, 4, 512)       \
+    X(512, 2, 512)       \
     X(512, 4, 512)
 
 #define GBN_EXRF(LN, TPR, VPT, NT) \
