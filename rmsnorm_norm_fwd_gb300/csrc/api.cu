@@ -840,7 +840,7 @@ struct ExCall {
 
 // Slots per (device, is_ln, dir): one per table entry, the last one for the
 // element-wise kernel.
-constexpr int kExSlots = 33;
+constexpr int kExSlots = kExMaxVariants + 1;
 // Per slot: the dynamic shared-memory limit raised, and the last (shared
 // memory, occupancy) pair.
 std::atomic<int> g_ex_smem_set[kMaxDev][2][2][kExSlots];
@@ -925,7 +925,7 @@ bool exr_geometry(const ExVariant &v, const ExCall &c, int dev, TileCfg *tc, siz
 // Plans variant i of the table for this call: false if it cannot serve it.
 int ex_try(const ExCall &c, int i, int dev, ExPlan *pl, bool *ok) {
     *ok = false;
-    const ExTable &t = kExTables[c.is_ln][c.dir];
+    const ExTable &t = ex_table(c.is_ln, c.dir);
     const ExVariant &v = t.v[i];
     if ((int64_t)v.tpr * v.vpt * 8 < c.N) return GBNORM_OK;
     const int64_t limit = g_grid_limit.load(std::memory_order_relaxed);
@@ -933,6 +933,7 @@ int ex_try(const ExCall &c, int i, int dev, ExPlan *pl, bool *ok) {
     int occ = 0;
     if (v.ring) {
         if (c.no_ring || (c.dir == 1 && !c.stats16)) return GBNORM_OK;
+        if (v.xt >= 0 && (v.xt != c.xdt || c.ydt != c.xdt)) return GBNORM_OK;
         TileCfg tc;
         size_t dyn;
         if (!exr_geometry(v, c, dev, &tc, &dyn)) return GBNORM_OK;
@@ -964,7 +965,7 @@ int ex_try(const ExCall &c, int i, int dev, ExPlan *pl, bool *ok) {
 // The first table entry that serves the call (ring kernels come first; a
 // forced entry is tried before all others), else the element-wise kernel.
 int ex_plan(const ExCall &c, int dev, ExPlan *pl) {
-    const ExTable &t = kExTables[c.is_ln][c.dir];
+    const ExTable &t = ex_table(c.is_ln, c.dir);
     const int forced = g_ex_force[c.is_ln][c.dir].load(std::memory_order_relaxed) - 1;
     if (c.vec && c.N % 8 == 0) {
         bool ok = false;
@@ -1262,12 +1263,12 @@ const char *gbnorm_variant_at(int is_layernorm, int dir, int dtype, int index) {
 
 int gbnorm_ex_variant_count(int is_layernorm, int dir) {
     if (dir != 0 && dir != 1) return 0;
-    return kExTables[is_layernorm ? 1 : 0][dir].count + 1;
+    return ex_table(is_layernorm ? 1 : 0, dir).count + 1;
 }
 
 const char *gbnorm_ex_variant_at(int is_layernorm, int dir, int index) {
     if (dir != 0 && dir != 1) return nullptr;
-    const ExTable &t = kExTables[is_layernorm ? 1 : 0][dir];
+    const ExTable &t = ex_table(is_layernorm ? 1 : 0, dir);
     if (index == t.count) return "exe";
     return (index >= 0 && index < t.count) ? t.v[index].name : nullptr;
 }
@@ -1279,7 +1280,7 @@ int gbnorm_ex_force_variant(int is_layernorm, int dir, const char *name) {
         g_ex_force[ln][dir].store(0);
         return GBNORM_OK;
     }
-    const ExTable &t = kExTables[ln][dir];
+    const ExTable &t = ex_table(ln, dir);
     for (int i = 0; i <= t.count; ++i) {
         if (std::strcmp(gbnorm_ex_variant_at(ln, dir, i), name) == 0) {
             g_ex_force[ln][dir].store(i + 1);

@@ -558,7 +558,10 @@ __device__ __forceinline__ void exr_drain(ExRingHeader &h, int grp, int SG, int 
                           reinterpret_cast<volatile int *>(&zero), nullptr);
 }
 
-template <bool LN, int TPR, int VPT, int NT>
+// XT: the storage type of x (and of y, dy, h, dres, dx) fixed at compile
+// time (kF32 / kF16 / kBF16), which folds every conversion branch; -1 reads
+// the types from the call (any combination).
+template <bool LN, int TPR, int VPT, int NT, int XT = -1>
 __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
     constexpr int RPP = NT / TPR;
     constexpr int WPR = TPR / 32;
@@ -566,14 +569,15 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
     static_assert(RPP * 2 * 2 * WPR <= (int)(sizeof(ExRingHeader::red) / 4), "scratch");
     extern __shared__ __align__(128) unsigned char smem[];
     ExRingHeader &h = *reinterpret_cast<ExRingHeader *>(smem);
+    const int xdt = XT >= 0 ? XT : p.xdt, ydt = XT >= 0 ? XT : p.ydt;
     const int64_t M = p.M, nc = p.N / 8;
-    const int xes = esize(p.xdt);
+    const int xes = esize(xdt);
     const size_t xrb = (size_t)p.N * xes;
     unsigned char *gsm = smem + kTmaHeaderBytes;  // gamma, then beta
     unsigned char *bsm = gsm + exr_param_bytes(p.N, p.pdt, false);
     unsigned char *stages = smem + kTmaHeaderBytes + exr_param_bytes(p.N, p.pdt, LN);
     const int SG = p.tc.stages / RPP, RT = p.tc.rows;
-    const size_t xsec = exr_section(RT, p.N, p.xdt);
+    const size_t xsec = exr_section(RT, p.N, xdt);
     const int64_t ntiles = (M + RT - 1) / RT;
     const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
     float *scratch = h.red + grp * (2 * 2 * WPR);
@@ -631,17 +635,17 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
             for (int k = 0; k < VPT; ++k) {
                 const int64_t c = (int64_t)k * TPR + t;
                 if (c < nc) {
-                    lds8p(xs, c, p.xdt, xf[k]);
+                    lds8p(xs, c, xdt, xf[k]);
                     if (p.res) {
                         // h = x + r in fp32, rounded once to the storage type
                         float2 r8[4];
-                        lds8p(xs + xsec, c, p.xdt, r8);
+                        lds8p(xs + xsec, c, xdt, r8);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 hs = f2add(xf[k][e], r8[e]);
-                            xf[k][e] = make_float2(round_to(hs.x, p.xdt), round_to(hs.y, p.xdt));
+                            xf[k][e] = make_float2(round_to(hs.x, xdt), round_to(hs.y, xdt));
                         }
-                        if (p.h) st8p(row_ptr(p.h, row, p.ldh, p.xdt), 8 * c, p.xdt, xf[k]);
+                        if (p.h) st8p(row_ptr(p.h, row, p.ldh, xdt), 8 * c, xdt, xf[k]);
                     }
                 } else {
 #pragma unroll
@@ -718,14 +722,14 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) o[e] = f2add(o[e], b[e]);
                 }
-                st8p(row_ptr(p.y, row, p.ldy, p.ydt), 8 * c, p.ydt, o);
+                st8p(row_ptr(p.y, row, p.ldy, ydt), 8 * c, ydt, o);
             }
         }
     }
     if (t == 0 && *abort_flag) exr_drain(h, grp, SG, issued);
 }
 
-template <bool LN, int TPR, int VPT, int NT>
+template <bool LN, int TPR, int VPT, int NT, int XT = -1>
 __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
     pdl_launch_dependents();  // the column reduce waits for this grid's completion
     constexpr int NS = LN ? 2 : 1;
@@ -739,14 +743,15 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
     static_assert(RPP * 2 * NS * WPR <= (int)(sizeof(ExRingHeader::red) / 4), "scratch");
     extern __shared__ __align__(128) unsigned char smem[];
     ExRingHeader &h = *reinterpret_cast<ExRingHeader *>(smem);
+    const int xdt = XT >= 0 ? XT : p.xdt, ydt = XT >= 0 ? XT : p.ydt;
     const int64_t M = p.M, nc = p.N / 8;
-    const int xes = esize(p.xdt), yes = esize(p.ydt);
+    const int xes = esize(xdt), yes = esize(ydt);
     const size_t xrb = (size_t)p.N * xes, yrb = (size_t)p.N * yes;
     unsigned char *gsm = smem + kTmaHeaderBytes;  // gamma in its storage type
     unsigned char *stages = smem + kTmaHeaderBytes + exr_param_bytes(p.N, p.pdt, false);
     const int SG = p.tc.stages / RPP, RT = p.tc.rows;
     // stage: x | dy | dres (if any) | rstd, mean windows
-    const size_t xsec = exr_section(RT, p.N, p.xdt), ysec = exr_section(RT, p.N, p.ydt);
+    const size_t xsec = exr_section(RT, p.N, xdt), ysec = exr_section(RT, p.N, ydt);
     const size_t rsec = p.dres ? xsec : 0;
     const int64_t ntiles = (M + RT - 1) / RT;
     const int t = threadIdx.x % TPR, grp = threadIdx.x / TPR;
@@ -835,8 +840,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
                 const int64_t c = (int64_t)k * TPR + t;
                 float2 x8[4], d8[4], g8[4];
                 if (c < nc) {
-                    lds8p(xs, c, p.xdt, x8);
-                    lds8p(ds, c, p.ydt, d8);
+                    lds8p(xs, c, xdt, x8);
+                    lds8p(ds, c, ydt, d8);
                     par8p(gsm, has_g, c, p.pdt, 1.f, g8);
                 } else {
 #pragma unroll
@@ -882,8 +887,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
                     }
                 } else {
                     float2 x8[4], g8[4];
-                    lds8p(xs, c, p.xdt, x8);
-                    lds8p(ds, c, p.ydt, dv);
+                    lds8p(xs, c, xdt, x8);
+                    lds8p(ds, c, ydt, dv);
                     par8p(gsm, has_g, c, p.pdt, 1.f, g8);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -900,11 +905,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
                 }
                 if (p.dres) {
                     float2 r8[4];
-                    lds8p(tb + xsec + ysec + (size_t)r * xrb, c, p.xdt, r8);
+                    lds8p(tb + xsec + ysec + (size_t)r * xrb, c, xdt, r8);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) o[e] = f2add(o[e], r8[e]);
                 }
-                st8p(row_ptr(p.dx, row, p.lddx, p.xdt), 8 * c, p.xdt, o);
+                st8p(row_ptr(p.dx, row, p.lddx, xdt), 8 * c, xdt, o);
             }
         }
     }

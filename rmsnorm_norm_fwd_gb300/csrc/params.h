@@ -165,12 +165,15 @@ struct ExVariant {
     const void *kernel;
     int tpr, vpt, cta;  // capacity tpr * vpt * 8 elements
     int ring = 0;       // rows staged through a bulk-copy ring (else read into registers)
+    int xt = -1;        // ring: storage type of the rows fixed at compile time (x = y, dy), -1 any
 };
 struct ExTable {
     const ExVariant *v;
     int count;
     const void *elem;
 };
-extern const ExTable kExTables[2][2];
+constexpr int kExMaxVariants = 48;  // entries per table (the planner keeps one slot each, and one for exe)
+extern const ExTable kExFwdTables[2], kExBwdTables[2];  // [is_ln]
+inline const ExTable &ex_table(int is_ln, int dir) { return dir ? kExBwdTables[is_ln] : kExFwdTables[is_ln]; }
 
 }  // namespace gbn

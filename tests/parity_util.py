@@ -104,7 +104,7 @@ def row_threads(variant: str):
     )
     if variant.startswith("sk"):  # single-kernel backward: the staged kernel's geometry
         variant = variant[2:]
-    m = re.fullmatch(r"exr?[fb](\d+)x(\d+)b(\d+)", variant)  # general form: 8-element chunks
+    m = re.fullmatch(r"exr?[fb](\d+)x(\d+)b(\d+)(?:_(?:bf16|fp16|fp32))?", variant)  # general form
     if m:
         return int(m.group(1)), 1, False
     for pat, f in pats:

@@ -199,7 +199,7 @@ def _force_cases():
     for op in ("rms", "ln"):
         for d, dn in ((0, "fwd"), (1, "bwd")):
             for name in g.ex_variants(op == "ln", d):
-                m = re.fullmatch(r"exr?[fb](\d+)x(\d+)b(\d+)", name)
+                m = re.match(r"exr?[fb](\d+)x(\d+)b(\d+)", name)
                 cap = int(m.group(1)) * int(m.group(2)) * 8 if m else 4096
                 cases.append((op, dn, name, cap))
     return cases
@@ -213,13 +213,16 @@ def _cases_or_empty():
 
 
 def _ring_fits(ln, d, name, M, N, xdt, ydt, pdt, extra):
-    """Whether the library's ring layout for `name` fits this call (the rule
-    the planner applies: about 16 KB of rows per stage, two stages per row
-    group at least, in the opt-in shared memory after the header and the
+    """Whether the planner may take ring kernel `name` for this call: a build
+    for one row storage type only when x and y (dy) have it, and a ring
+    layout that fits (about 16 KB of rows per stage, two stages per row group
+    at least, in the opt-in shared memory after the header and the
     parameters)."""
     es = {"fp32": 4, "bf16": 2, "fp16": 2}
-    m = re.fullmatch(r"exr[fb](\d+)x(\d+)b(\d+)", name)
-    tpr, vpt, nt = (int(v) for v in m.groups())
+    m = re.fullmatch(r"exr[fb](\d+)x(\d+)b(\d+)(?:_(bf16|fp16|fp32))?", name)
+    tpr, vpt, nt = (int(v) for v in m.groups()[:3])
+    if m.group(4) and (m.group(4) != xdt or ydt != xdt):
+        return False  # built for one row storage type shared by x and y / dy
     rpp = nt // tpr
     al = lambda b: (b + 127) // 128 * 128  # noqa: E731
     optin = torch.cuda.get_device_properties(0).shared_memory_per_block_optin
@@ -246,8 +249,9 @@ def _ring_fits(ln, d, name, M, N, xdt, ydt, pdt, extra):
 
 @pytest.mark.parametrize("op,direction,name,cap", _cases_or_empty(),
                          ids=lambda v: str(v))
-@pytest.mark.parametrize("types", [("bf16", "fp32", "bf16", True), ("fp32", "bf16", "fp16", False)],
-                         ids=["bf16-fp32-extras", "fp32-bf16"])
+@pytest.mark.parametrize("types", [("bf16", "fp32", "bf16", True), ("fp32", "bf16", "fp16", False),
+                                   ("fp16", "bf16", "fp16", True), ("fp32", "fp32", "fp32", False)],
+                         ids=["bf16-fp32-extras", "fp32-bf16-fp16y", "fp16-bf16-extras", "fp32"])
 def test_forced_variant(op, direction, name, cap, types):
     """Every general-form kernel, forced, at a row length inside its capacity,
     several tiles per CTA with a ragged last tile, against the oracle; a ring

@@ -117,5 +117,5 @@ def test_general_form_names_parse():
             for name in names:
                 tpr, cl, elem = row_threads(name)
                 assert cl == 1 and elem == (name == "exe")
-                m = re.fullmatch(r"exr?[fb](\d+)x(\d+)b(\d+)", name)
+                m = re.fullmatch(r"exr?[fb](\d+)x(\d+)b(\d+)(?:_(?:bf16|fp16|fp32))?", name)
                 assert elem or (m and int(m.group(1)) == tpr and int(m.group(3)) % tpr == 0)
