@@ -293,6 +293,20 @@ bool wcs_geometry(const Variant &v, const CallShape &c, int dev, TileCfg *tc, si
     return true;
 }
 
+// Shared memory of a cluster-slice forward variant: gamma (and beta) of a
+// slice in their storage type.  False if the slice exceeds the per-thread
+// capacity or does not fit.
+bool fwider_geometry(const Variant &v, const CallShape &c, int dev, size_t *dyn_smem) {
+    if (c.dir != 0) return false;
+    const int64_t nv = c.N / v.elems_per_vec;
+    const int64_t slice = (nv + v.cl - 1) / v.cl;
+    if (slice > (int64_t)v.tpr * v.vpt) return false;
+    const size_t bytes = (size_t)v.tpr * v.vpt * 16u * (c.is_ln ? 2u : 1u);
+    if (bytes + 4096 > (size_t)g_dev[dev].smem_optin) return false;
+    *dyn_smem = bytes;
+    return true;
+}
+
 // Shared memory of a wide-row variant: none for the forward; for the
 // backward each CTA's column slice of dgamma (and dbeta) sums in fp32.  False
 // if a CTA of the cluster would get no columns or the sums do not fit.
@@ -343,6 +357,10 @@ bool can_serve(const Variant &v, const CallShape &c, int dev) {
         TileCfg tc;
         size_t dyn;
         return wcs_geometry(v, c, dev, &tc, &dyn);
+    }
+    if (v.kind == kWideF) {
+        size_t dyn;
+        return fwider_geometry(v, c, dev, &dyn);
     }
     if (v.kind == kRowsS) {
         size_t dyn;
@@ -432,13 +450,14 @@ int occupancy(const CallShape &c, int idx, int dev, size_t dyn_smem, int *out) {
     const Variant &v = kTables[c.is_ln][c.dir][c.dtype]->v[idx];
     // Kinds whose shared memory (and so occupancy) depends on the shape.
     const bool per_shape = v.staged_rows() || v.kind == kRowsS || v.kind == kWtma || v.kind == kWtmaC ||
-                           v.kind == kWideR || v.kind == kWcs || (v.kind == kWide && dyn_smem > 0);
+                           v.kind == kWideR || v.kind == kWcs || v.kind == kWideF ||
+                           (v.kind == kWide && dyn_smem > 0);
     if (o > 0 && !per_shape) {
         *out = o;
         return GBNORM_OK;
     }
     if (v.staged_rows() || v.kind == kTmaCl || v.kind == kRowsS || v.kind == kWtma || v.kind == kWtmaC ||
-        v.kind == kWideR || v.kind == kWcs || (v.kind == kWide && dyn_smem > 0)) {
+        v.kind == kWideR || v.kind == kWcs || v.kind == kWideF || (v.kind == kWide && dyn_smem > 0)) {
         std::atomic<uint64_t> &cache = g_occ_tma[dev][c.is_ln][c.dir][c.dtype][idx];
         const uint64_t hit = cache.load(std::memory_order_relaxed);
         if (hit != 0 && (hit >> 16) == (uint64_t)dyn_smem) {
@@ -522,6 +541,7 @@ int make_plan(const CallShape &c, int idx, int dev, Plan *pl) {
     if (v.kind == kWtmaC && !wtmac_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kWideR && !wider_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     if (v.kind == kWcs && !wcs_geometry(v, c, dev, &pl->tc, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
+    if (v.kind == kWideF && !fwider_geometry(v, c, dev, &pl->dyn_smem)) return GBNORM_ERR_UNSUPPORTED;
     int occ = 0;
     int st = occupancy(c, idx, dev, pl->dyn_smem, &occ);
     if (st != GBNORM_OK) return st;
@@ -825,6 +845,7 @@ struct ExPlan {
     int cta;
     TileCfg tc;        // ring kernels
     const char *name;
+    int planes = 0;    // ring kernels: parameters as fp32 planes
 };
 
 // A general-form call as the planner sees it.
@@ -876,16 +897,16 @@ int ex_occupancy(int dev, int is_ln, int dir, int slot, const void *k, int cta, 
 }
 
 // Ring layout of a ring variant for this call: shared memory holds the
-// header, gamma (and beta, forward LayerNorm) in their storage type, then the
-// stages.  A stage is a tile of RT rows: x (then the residual rows), or x, dy
+// header, gamma (and beta, forward LayerNorm) widened to fp32 planes (planes)
+// or in their storage type, then the stages.  A stage is a tile of RT rows: x (then the residual rows), or x, dy
 // (then dres) and the statistics windows.  About 16 KB of rows per stage, at
 // least two stages per row group, at most kExRingMaxStages in all.  False if
 // that does not fit.
-bool exr_geometry(const ExVariant &v, const ExCall &c, int dev, TileCfg *tc, size_t *dyn) {
+bool exr_geometry(const ExVariant &v, const ExCall &c, int dev, bool planes, TileCfg *tc, size_t *dyn) {
     const int rpp = v.cta / v.tpr;
     const int min_stages = 2 * rpp;
     if (min_stages > kExRingMaxStages) return false;
-    const size_t params = exr_param_bytes(c.N, c.pdt, c.dir == 0 && c.is_ln);
+    const size_t params = exr_param_bytes(c.N, c.pdt, c.dir == 0 && c.is_ln, planes);
     const size_t optin = (size_t)g_dev[dev].smem_optin;
     if (optin <= (size_t)kTmaHeaderBytes + params + 1024) return false;
     const size_t budget = optin - kTmaHeaderBytes - params;
@@ -934,16 +955,25 @@ int ex_try(const ExCall &c, int i, int dev, ExPlan *pl, bool *ok) {
     if (v.ring) {
         if (c.no_ring || (c.dir == 1 && !c.stats16)) return GBNORM_OK;
         if (v.xt >= 0 && (v.xt != c.xdt || c.ydt != c.xdt)) return GBNORM_OK;
+        // gamma (beta) widened into fp32 planes (conflict-free 16-byte reads,
+        // nothing to convert) where the ring still fits beside them, except
+        // 16-bit gamma and beta of the LayerNorm forward, which measured
+        // faster read in their storage type (one 16-byte read per 8
+        // elements of each)
         TileCfg tc;
         size_t dyn;
-        if (!exr_geometry(v, c, dev, &tc, &dyn)) return GBNORM_OK;
+        int planes = (c.dir == 0 && c.is_ln && c.pdt != GBNORM_F32) ? 0 : 1;
+        if (!planes || !exr_geometry(v, c, dev, true, &tc, &dyn)) {
+            planes = 0;
+            if (!exr_geometry(v, c, dev, false, &tc, &dyn)) return GBNORM_OK;
+        }
         const int st = ex_occupancy(dev, c.is_ln, c.dir, i, v.kernel, v.cta, dyn, &occ);
         if (st != GBNORM_OK) return st;
         // persistent: at most one CTA per SM
         const int64_t ntiles = (c.M + tc.rows - 1) / tc.rows;
         int64_t cap = sms;
         if (limit > 0 && limit < cap) cap = limit;
-        *pl = ExPlan{v.kernel, ntiles < cap ? ntiles : cap, dyn, v.cta, tc, v.name};
+        *pl = ExPlan{v.kernel, ntiles < cap ? ntiles : cap, dyn, v.cta, tc, v.name, planes};
         *ok = true;
         return GBNORM_OK;
     }
@@ -1033,7 +1063,8 @@ int do_fwd_ex(int is_ln, int64_t M, int64_t N, float eps, const void *x, int64_t
     s = ex_plan(ExCall{is_ln, 0, M, N, xdt, ydt, pdt, res != nullptr, vec, true, false}, dev, &pl);
     if (s != GBNORM_OK) return s;
     g_ex_last[0] = pl.name;
-    ExFwdParams p{x, res, h, gamma, beta, y, mean, rstd, ldx, ldr, ldh, ldy, M, N, eps, xdt, pdt, ydt, pl.tc};
+    ExFwdParams p{x, res, h, gamma, beta, y, mean, rstd, ldx, ldr, ldh, ldy, M, N, eps, xdt, pdt, ydt, pl.tc,
+                  pl.planes};
     return launch_ex(pl, &p, stream);
 }
 
@@ -1102,7 +1133,7 @@ int do_bwd_ex(int is_ln, int64_t M, int64_t N, const void *dy, int64_t lddy, int
         if (s != GBNORM_OK) return s;
         g_ex_last[1] = pl.name;
         ExBwdParams p{dy, x, dres, gamma, mean, rstd, dx, static_cast<float *>(ws), lddy, ldx, lddres, lddx,
-                      M, N, xdt, pdt, ydt, pl.tc};
+                      M, N, xdt, pdt, ydt, pl.tc, pl.planes};
         s = launch_ex(pl, &p, stream);
         if (s != GBNORM_OK) return s;
         P = pl.grid;

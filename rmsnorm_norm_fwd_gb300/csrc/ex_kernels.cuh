@@ -529,6 +529,20 @@ __device__ __forceinline__ void par8p(const unsigned char *row, bool present, in
         for (int i = 0; i < 4; ++i) f[i] = f2s(one);
     }
 }
+// Parameter chunk c as pairs: from fp32 planes (element 0-3 at [c], 4-7 at
+// [nc + c]; conflict-free, nothing to convert) or from the raw row.
+__device__ __forceinline__ void parp(bool planes, const float4 *pl, const unsigned char *raw, bool present,
+                                     int64_t nc, int64_t c, int dt, float one, float2 (&f)[4]) {
+    if (planes) {
+        const float4 a = pl[c], b = pl[nc + c];
+        f[0] = make_float2(a.x, a.y);
+        f[1] = make_float2(a.z, a.w);
+        f[2] = make_float2(b.x, b.y);
+        f[3] = make_float2(b.z, b.w);
+    } else {
+        par8p(raw, present, c, dt, one, f);
+    }
+}
 __device__ __forceinline__ void st8p(void *row, int64_t off, int dt, const float2 (&f)[4]) {
     const float o[8] = {f[0].x, f[0].y, f[1].x, f[1].y, f[2].x, f[2].y, f[3].x, f[3].y};
     st8(row, off, dt, o);
@@ -573,9 +587,11 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
     const int64_t M = p.M, nc = p.N / 8;
     const int xes = esize(xdt);
     const size_t xrb = (size_t)p.N * xes;
+    const bool planes = p.planes != 0;
     unsigned char *gsm = smem + kTmaHeaderBytes;  // gamma, then beta
-    unsigned char *bsm = gsm + exr_param_bytes(p.N, p.pdt, false);
-    unsigned char *stages = smem + kTmaHeaderBytes + exr_param_bytes(p.N, p.pdt, LN);
+    unsigned char *bsm = gsm + exr_param_bytes(p.N, p.pdt, false, planes);
+    unsigned char *stages = smem + kTmaHeaderBytes + exr_param_bytes(p.N, p.pdt, LN, planes);
+    const float4 *gpl = reinterpret_cast<const float4 *>(gsm), *bpl = reinterpret_cast<const float4 *>(bsm);
     const int SG = p.tc.stages / RPP, RT = p.tc.rows;
     const size_t xsec = exr_section(RT, p.N, xdt);
     const int64_t ntiles = (M + RT - 1) / RT;
@@ -608,12 +624,18 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
         fence_mbar_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && !planes)
         load_params(&h.pbar, gsm, bsm, p.gamma, LN ? p.beta : nullptr,
                     (uint32_t)((size_t)p.N * esize(p.pdt)));
     if (t == 0)
         for (int j = 0; j < SG; ++j) issue(j);
-    mbar_wait_bounded(&h.pbar, 0, abort_flag, p.tc.fault);
+    if (planes) {
+        // gamma (beta) planes: [0, 2 nc) then, for LayerNorm, [2 nc, 4 nc)
+        ex_load_params<LN, NT>(reinterpret_cast<float4 *>(gsm), p.gamma, p.beta, p.pdt, nc);
+        __syncthreads();
+    } else {
+        mbar_wait_bounded(&h.pbar, 0, abort_flag, p.tc.fault);
+    }
 
     const float n = (float)p.N;
     const bool full = nc == (int64_t)TPR * VPT;  // every thread holds VPT chunks (uniform)
@@ -713,12 +735,12 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
                 const int64_t c = (int64_t)k * TPR + t;
                 if (c >= nc) continue;
                 float2 g[4], o[4];
-                par8p(gsm, has_g, c, p.pdt, 1.f, g);
+                parp(planes, gpl, gsm, has_g, nc, c, p.pdt, 1.f, g);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) o[e] = f2mul(f2mul(f2add(xf[k][e], nm), rs), g[e]);
                 if constexpr (LN) {
                     float2 b[4];
-                    par8p(bsm, has_b, c, p.pdt, 0.f, b);
+                    parp(planes, gpl + 2 * nc, bsm, has_b, nc, c, p.pdt, 0.f, b);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) o[e] = f2add(o[e], b[e]);
                 }
@@ -747,8 +769,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
     const int64_t M = p.M, nc = p.N / 8;
     const int xes = esize(xdt), yes = esize(ydt);
     const size_t xrb = (size_t)p.N * xes, yrb = (size_t)p.N * yes;
-    unsigned char *gsm = smem + kTmaHeaderBytes;  // gamma in its storage type
-    unsigned char *stages = smem + kTmaHeaderBytes + exr_param_bytes(p.N, p.pdt, false);
+    const bool planes = p.planes != 0;
+    unsigned char *gsm = smem + kTmaHeaderBytes;  // gamma: fp32 planes, or its storage type
+    unsigned char *stages = smem + kTmaHeaderBytes + exr_param_bytes(p.N, p.pdt, false, planes);
+    const float4 *gpl = reinterpret_cast<const float4 *>(gsm);
     const int SG = p.tc.stages / RPP, RT = p.tc.rows;
     // stage: x | dy | dres (if any) | rstd, mean windows
     const size_t xsec = exr_section(RT, p.N, xdt), ysec = exr_section(RT, p.N, ydt);
@@ -793,11 +817,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
         fence_mbar_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && !planes)
         load_params(&h.pbar, gsm, nullptr, p.gamma, nullptr, (uint32_t)((size_t)p.N * esize(p.pdt)));
     if (t == 0)
         for (int j = 0; j < SG; ++j) issue(j);
-    mbar_wait_bounded(&h.pbar, 0, abort_flag, p.tc.fault);
+    if (planes) {
+        ex_load_params<false, NT>(reinterpret_cast<float4 *>(gsm), p.gamma, nullptr, p.pdt, nc);
+        __syncthreads();
+    } else {
+        mbar_wait_bounded(&h.pbar, 0, abort_flag, p.tc.fault);
+    }
 
     const float n = (float)p.N;
     const bool has_g = p.gamma != nullptr;
@@ -842,7 +871,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
                 if (c < nc) {
                     lds8p(xs, c, xdt, x8);
                     lds8p(ds, c, ydt, d8);
-                    par8p(gsm, has_g, c, p.pdt, 1.f, g8);
+                    parp(planes, gpl, gsm, has_g, nc, c, p.pdt, 1.f, g8);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) x8[e] = d8[e] = g8[e] = f2s(0.f);
@@ -889,7 +918,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_exr(const ExBwdParams p) {
                     float2 x8[4], g8[4];
                     lds8p(xs, c, xdt, x8);
                     lds8p(ds, c, ydt, dv);
-                    par8p(gsm, has_g, c, p.pdt, 1.f, g8);
+                    parp(planes, gpl, gsm, has_g, nc, c, p.pdt, 1.f, g8);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         xc[e] = f2add(x8[e], nm);

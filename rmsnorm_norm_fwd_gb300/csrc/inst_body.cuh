@@ -50,12 +50,19 @@ namespace gbn {
             ((CW) + 1) * 32, VecTraits<GBN_T>::E, 1, 0},
 #define GBN_WT_RMS(CW, U) GBN_WTMA(false, CW, U)
 #define GBN_WT_LN(CW, U) GBN_WTMA(true, CW, U)
+#define GBN_FWIDER(LN, NT, K, CL, PF, MINB, F)                                                 \
+    Variant{GBN_FWIDER_VNAME(NT, K, CL, PF, MINB, F),                                          \
+            (const void *)&fwd_wider<GBN_T, LN, NT, K, CL, PF, MINB, F>, kWideF, NT, K, 1, CL, NT, \
+            VecTraits<GBN_T>::E, MINB, 0},
+#define GBN_FWR_RMS(NT, K, CL, PF, MINB, F) GBN_FWIDER(false, NT, K, CL, PF, MINB, F)
+#define GBN_FWR_LN(NT, K, CL, PF, MINB, F) GBN_FWIDER(true, NT, K, CL, PF, MINB, F)
 #define GBN_FWCS(LN, NT, VPT, CL)                                                              \
     Variant{GBN_WCS_VNAME(NT, VPT, CL), (const void *)&fwd_wcs<GBN_T, LN, NT, VPT, CL>, kWcs, NT, VPT, 1, \
             CL, NT, VecTraits<GBN_T>::E, 1, 0},
 #define GBN_FWCS_RMS(NT, VPT, CL) GBN_FWCS(false, NT, VPT, CL)
 #define GBN_FWCS_LN(NT, VPT, CL) GBN_FWCS(true, NT, VPT, CL)
 static const Variant rms_variants[] = {
+    GBN_FWIDER_GEOMS(GBN_FWR_RMS)
     GBN_WCS_GEOMS(GBN_FWCS_RMS)
     GBN_WTMA_FWD_GEOMS(GBN_WT_RMS)
     GBN_TMP_FWD_GEOMS(GBN_FP_RMS)
@@ -66,6 +73,7 @@ static const Variant rms_variants[] = {
     GBN_FWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
+    GBN_FWIDER_GEOMS(GBN_FWR_LN)
     GBN_WCS_GEOMS(GBN_FWCS_LN)
     GBN_WTMA_FWD_GEOMS(GBN_WT_LN)
     GBN_TMP_FWD_GEOMS(GBN_FP_LN)
@@ -99,6 +107,9 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_WT_RMS
 #undef GBN_WT_LN
 #undef GBN_FWCS
+#undef GBN_FWIDER
+#undef GBN_FWR_RMS
+#undef GBN_FWR_LN
 #undef GBN_FWCS_RMS
 #undef GBN_FWCS_LN
 #endif

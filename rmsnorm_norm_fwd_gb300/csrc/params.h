@@ -56,10 +56,11 @@ struct BwdParams {
 // agree on it): after the header, gamma (and beta) in their storage type
 // (dt 0: fp32, else 16-bit), then the stages; a stage holds one section per
 // row tensor of its tile of rt rows (x, then the residual rows; or x, dy,
-// dres), each 128-byte aligned.
+// dres), each 128-byte aligned.  With `planes`, gamma (and beta) are held
+// widened to fp32 whatever their storage type.
 __host__ __device__ inline size_t ex_al128(size_t b) { return (b + 127) & ~(size_t)127; }
-__host__ __device__ inline size_t exr_param_bytes(int64_t N, int pdt, bool two) {
-    return ex_al128((size_t)N * (pdt == 0 ? 4 : 2)) * (two ? 2 : 1);
+__host__ __device__ inline size_t exr_param_bytes(int64_t N, int pdt, bool two, bool planes = false) {
+    return ex_al128((size_t)N * (planes || pdt == 0 ? 4 : 2)) * (two ? 2 : 1);
 }
 __host__ __device__ inline size_t exr_section(int rt, int64_t N, int dt) {
     return ex_al128((size_t)rt * (size_t)N * (dt == 0 ? 4 : 2));
@@ -82,6 +83,7 @@ struct ExFwdParams {
     float eps;
     int xdt, pdt, ydt;
     TileCfg tc;  // ring kernels: rows per tile, stages, stage stride, fault word
+    int planes;  // ring kernels: gamma (beta) widened to fp32 planes in shared memory, else kept raw
 };
 
 struct ExBwdParams {
@@ -97,6 +99,7 @@ struct ExBwdParams {
     int64_t M, N;
     int xdt, pdt, ydt;
     TileCfg tc;  // ring kernels: rows per tile, stages, stage stride, fault word
+    int planes;  // ring kernels: gamma widened to fp32 planes in shared memory, else kept raw
 };
 
 enum VariantKind : int {
@@ -111,6 +114,7 @@ enum VariantKind : int {
     kWtmaC = 8, // column slices of a cluster streamed twice through a bulk-copy ring (backward)
     kWideR = 9, // as kWide (backward), the dgamma/dbeta sums in registers, gamma in shared memory
     kWcs = 10,  // cluster column slices of each row resident in shared memory (bulk-copy ring)
+    kWideF = 11, // forward on kWideR's layout: cluster column slices, gamma/beta slices in shared memory
 };
 
 // One compiled kernel and the geometry the host needs to launch it.
@@ -142,7 +146,9 @@ struct Variant {
     bool staged_rows() const { return kind == kTma || kind == kTmaP; }
     int rows_per_cta_iter() const {
         return (kind == kRows || kind == kRowsS) ? (cta / tpr) * rows
-                                                 : ((kind == kWide || kind == kWideR) && cl == 1) ? rows : 1;
+                                                 : ((kind == kWide || kind == kWideR || kind == kWideF) && cl == 1)
+                                                       ? rows
+                                                       : 1;
     }
 };
 

@@ -937,3 +937,295 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
 }
 
 }  // namespace gbn
+
+namespace gbn {
+
+// ============================================================================ forward, cluster slices
+// Wide-row forward on the layout of bwd_wider: a cluster of CL CTAs shares
+// each row, CTA `rank` always owns the same column slice, so gamma (and
+// beta) of the slice sit in its shared memory for the whole call (in their
+// storage type) and pass 2 re-reads only x from L2 -- fwd_wide re-reads x,
+// gamma and beta per row, three L2 loads per vector.  Per row: pass 1
+// streams the slice from DRAM (L2 evict_last) for this thread's statistics
+// (RMS: the sum of squares; LN: count, mean and M2 per batch of KB vectors,
+// merged with the update of Chan, Golub and LeVeque), the CTA combines them
+// (warps in order) and sends them to every CTA of the cluster through
+// distributed shared memory (four slots); the row's exchange is collected
+// (CL partials in rank order: identical bits in every CTA) a whole sweep
+// later, then pass 2 writes y from the slice re-read from L2 (evict_first).
+// Thread t owns vectors t + k * NT (k < K) of the slice.
+// FUSE: 0 pass 1 of row k + 1, the exchange of row k, then pass 2 of row k;
+// 1 pass 1 of row j in the same sweep as pass 2 of row j - 2 (both rows'
+// loads in flight together, KB = 4 vectors of each per batch).
+template <typename T, bool LN, int NT, int K, int CL, int PF, int MINB, int FUSE = 0>
+__global__ void __launch_bounds__(NT, MINB) fwd_wider(const FwdParams p) {
+    constexpr int E = VecTraits<T>::E;
+    constexpr int W = NT / 32;
+    constexpr int NVAL = LN ? 3 : 1;  // exchanged: (count, mean, M2) or the sum of squares
+    constexpr int NS = 4;
+    // vectors per batch: the whole of a thread's slice up to 8, 4 when fused
+    constexpr int KB = FUSE ? (K < 4 ? K : 4) : (K < 8 ? K : 8);
+    static_assert(NT % 32 == 0 && NT <= 1024 && CL >= 1 && CL <= 16 && K % KB == 0, "shape");
+    extern __shared__ __align__(16) uint4 psm[];  // gamma of the slice [K * NT], then beta
+    __shared__ float red[2][3][W];
+    __shared__ float slot[NS][CL][NVAL];
+    __shared__ __align__(8) uint64_t xch[NS];
+    __shared__ int abort_flag;
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int rank = CL > 1 ? (int)cluster_ctarank() : 0;
+    const int64_t cid = CL > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
+    const int64_t ncl = CL > 1 ? (int64_t)cluster_count_x() : (int64_t)gridDim.x;
+    const int64_t M = p.M, nv = p.N / E;
+    const int64_t slice = (nv + CL - 1) / CL;
+    const int64_t v0 = rank * slice;
+    const int64_t cnt = nv - v0 < slice ? (nv - v0 > 0 ? nv - v0 : 0) : slice;
+    const float n = (float)p.N;
+    const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
+    constexpr int KNT = K * NT;
+
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int64_t lv = (int64_t)k * NT + t;
+        psm[lv] = lv < cnt ? param_vec<T>(p.gamma, v0 + lv, true) : make_uint4(0, 0, 0, 0);
+        if constexpr (LN) psm[KNT + lv] = lv < cnt ? param_vec<T>(p.beta, v0 + lv, false) : make_uint4(0, 0, 0, 0);
+    }
+    if (t == 0) {
+        abort_flag = 0;
+        if (CL > 1) {
+            for (int j = 0; j < NS; ++j) mbar_init(&xch[j], CL);
+            fence_mbar_init();
+        }
+    }
+    // every CTA's barriers exist before any peer arrives on them
+    if constexpr (CL > 1) cluster_sync_all();
+    else __syncthreads();
+
+    const int64_t nrows = cid < M ? (M - cid + ncl - 1) / ncl : 0;
+    auto row_of = [&](int64_t k) { return cid + k * ncl; };
+    auto row_x = [&](int64_t k) { return static_cast<const uint4 *>(p.x) + row_of(k) * nv + v0; };
+    auto prefetch = [&](int64_t k) {
+        if (warp == 0 && k < nrows && cnt > 0) prefetch_row(row_x(k), (size_t)cnt * 16, lane, keep);
+    };
+    int parity = 0;
+    float cst[3][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // (mean, rstd) of row k at [k % 3]
+
+    // The CTA's statistics of row k from this thread's (identical bits in
+    // every thread), sent to the cluster (or, alone, turned into mean, rstd).
+    // v: RMS {sum x^2}; LN {count, mean, M2}.
+    auto finish1 = [&](int64_t k, float (&v)[NVAL]) {
+        if constexpr (!LN) {
+            float acc = v[0];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0) red[parity][0][warp] = acc;
+            __syncthreads();
+            acc = 0.f;
+#pragma unroll 4
+            for (int w = 0; w < W; ++w) acc += red[parity][0][w];
+            v[0] = acc;
+        } else {
+            warp_combine(v[0], v[1], v[2]);
+            if (lane == 0) {
+                red[parity][0][warp] = v[0];
+                red[parity][1][warp] = v[1];
+                red[parity][2][warp] = v[2];
+            }
+            __syncthreads();
+            // the same group combine over the warps, in warp order
+            float tn = 0.f, ts = 0.f;
+#pragma unroll 4
+            for (int w = 0; w < W; ++w) {
+                tn += red[parity][0][w];
+                ts += red[parity][0][w] * red[parity][1][w];
+            }
+            const float mu = tn > 0.f ? ts / tn : 0.f;
+            float a2 = 0.f;
+#pragma unroll 4
+            for (int w = 0; w < W; ++w) {
+                const float d = red[parity][1][w] - mu;
+                a2 += red[parity][2][w] + red[parity][0][w] * (d * d);
+            }
+            v[0] = tn;
+            v[1] = mu;
+            v[2] = a2;
+        }
+        parity ^= 1;
+        if constexpr (CL > 1) {
+            if (t < CL) {
+                const int sp = (int)(k % NS);
+                const uint32_t dst = map_to_rank(smem_u32(&slot[sp][rank][0]), (uint32_t)t);
+#pragma unroll
+                for (int i = 0; i < NVAL; ++i) st_cluster_f32(dst + 4u * i, v[i]);
+                mbar_arrive_remote(map_to_rank(smem_u32(&xch[sp]), (uint32_t)t));
+            }
+        } else {
+            cst[k % 3][0] = LN ? v[1] : 0.f;
+            cst[k % 3][1] = rsqrtf((LN ? v[2] : v[0]) / n + p.eps);
+        }
+    };
+    // The exchange of row k: CL partials combined in rank order.
+    auto recv = [&](int64_t k) {
+        if constexpr (CL > 1) {
+            const int sp = (int)(k % NS);
+            mbar_wait_cluster_bounded(&xch[sp], (uint32_t)((k / NS) & 1), &abort_flag, p.tc.fault);
+            if constexpr (!LN) {
+                float s = 0.f;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) s += slot[sp][c][0];
+                cst[k % 3][0] = 0.f;
+                cst[k % 3][1] = rsqrtf(s / n + p.eps);
+            } else {
+                float tn = 0.f, ts = 0.f;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    tn += slot[sp][c][0];
+                    ts += slot[sp][c][0] * slot[sp][c][1];
+                }
+                const float mu = ts / tn;
+                float a2 = 0.f;
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    const float d = slot[sp][c][1] - mu;
+                    a2 += slot[sp][c][2] + slot[sp][c][0] * (d * d);
+                }
+                cst[k % 3][0] = mu;
+                cst[k % 3][1] = rsqrtf(a2 / n + p.eps);
+            }
+        }
+    };
+    // One sweep over the slice: pass 1 of row k1 (if has1: this thread's
+    // statistics into v) and pass 2 of row k2 (if has2: y), their loads in
+    // the same batches.  Branches uniform over the CTA.
+    auto sweep = [&](bool has1, int64_t k1, bool has2, int64_t k2, float (&v)[NVAL]) {
+        const uint4 *x1 = row_x(has1 ? k1 : 0), *x2 = row_x(has2 ? k2 : 0);
+        const float mean2 = cst[(has2 ? k2 : 0) % 3][0], rstd2 = cst[(has2 ? k2 : 0) % 3][1];
+        const float2 nm = f2s(-mean2), rs = f2s(rstd2);
+        if (has2 && rank == 0 && t == 0) {
+            const int64_t row = row_of(k2);
+            if (p.rstd) p.rstd[row] = rstd2;
+            if (LN && p.mean) p.mean[row] = mean2;
+        }
+        uint4 *yr = static_cast<uint4 *>(p.y) + row_of(has2 ? k2 : 0) * nv + v0;
+        float2 a = f2s(0.f);                 // RMS: sum of squares
+        float cn = 0.f, mean = 0.f, m2 = 0.f;  // LN: running count, mean, M2
+#pragma unroll
+        for (int kb = 0; kb < K; kb += KB) {
+            uint4 q1[KB], q2[KB];
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                const int64_t lv = (int64_t)(kb + i) * NT + t;
+                const bool ok = lv < cnt;
+                q1[i] = (has1 && ok) ? ld_l2hint(x1 + lv, keep) : make_uint4(0, 0, 0, 0);
+                q2[i] = (has2 && ok) ? ld_l2hint(x2 + lv, drop) : make_uint4(0, 0, 0, 0);
+            }
+            if (has2) {
+#pragma unroll
+                for (int i = 0; i < KB; ++i) {
+                    const int64_t lv = (int64_t)(kb + i) * NT + t;
+                    if (lv >= cnt) continue;
+                    const uint4 g = psm[lv];
+                    uint4 b = make_uint4(0, 0, 0, 0);
+                    if constexpr (LN) b = psm[KNT + lv];
+                    float2 o[E / 2];
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e) {
+                        o[e] = f2mul(f2mul(f2add(vpair<T>(q2[i], e), nm), rs), vpair<T>(g, e));
+                        if constexpr (LN) o[e] = f2add(o[e], vpair<T>(b, e));
+                    }
+                    st_l2hint(yr + lv, vpack2<T>(o), drop);
+                }
+            }
+            if (has1) {
+                if constexpr (!LN) {
+#pragma unroll
+                    for (int i = 0; i < KB; ++i)
+#pragma unroll
+                        for (int e = 0; e < E / 2; ++e) {
+                            const float2 f = vpair<T>(q1[i], e);
+                            a = f2fma(f, f, a);
+                        }
+                } else {
+                    int nb = 0;
+                    float2 s2 = f2s(0.f);
+#pragma unroll
+                    for (int i = 0; i < KB; ++i) {
+                        if ((int64_t)(kb + i) * NT + t < cnt) nb += E;
+#pragma unroll
+                        for (int e = 0; e < E / 2; ++e) s2 = f2add(s2, vpair<T>(q1[i], e));
+                    }
+                    if (nb > 0) {
+                        const float fb = (float)nb;
+                        const float mb = __fdiv_rn(s2.x + s2.y, fb);
+                        const float2 nmb = f2s(-mb);
+                        float2 d2 = f2s(0.f);
+#pragma unroll
+                        for (int i = 0; i < KB; ++i) {
+                            if ((int64_t)(kb + i) * NT + t >= cnt) continue;
+#pragma unroll
+                            for (int e = 0; e < E / 2; ++e) {
+                                const float2 d = f2add(vpair<T>(q1[i], e), nmb);
+                                d2 = f2fma(d, d, d2);
+                            }
+                        }
+                        const float m2b = d2.x + d2.y;
+                        if (cn == 0.f) {
+                            cn = fb;
+                            mean = mb;
+                            m2 = m2b;
+                        } else {
+                            // running += batch
+                            const float tot = cn + fb;
+                            const float d = mb - mean;
+                            const float rr = __fdiv_rn(fb, tot);
+                            mean += d * rr;
+                            m2 += m2b + d * d * cn * rr;
+                            cn = tot;
+                        }
+                    }
+                }
+            }
+        }
+        if constexpr (!LN) {
+            v[0] = a.x + a.y;
+        } else {
+            v[0] = cn;
+            v[1] = mean;
+            v[2] = m2;
+        }
+    };
+
+    float v[NVAL];
+    if constexpr (FUSE) {
+        // step j: pass 1 of row j with pass 2 of row j - 2, then row j's
+        // statistics go out and row j - 1's come in (a whole sweep after
+        // they were sent)
+        for (int64_t j = 0; j < nrows + 2; ++j) {
+            const bool has1 = j < nrows, has2 = j >= 2;
+            if (PF >= 1) prefetch(j + 1);
+            sweep(has1, j, has2, j - 2, v);
+            if (has1) finish1(j, v);
+            if (j >= 1 && j - 1 < nrows) recv(j - 1);
+        }
+    } else {
+        // pass 1 of row k + 1, then row k's exchange, then pass 2 of row k
+        if (PF >= 1) prefetch(0);
+        if (nrows > 0) {
+            sweep(true, 0, false, 0, v);
+            finish1(0, v);
+        }
+        for (int64_t kr = 0; kr < nrows; ++kr) {
+            if (kr + 1 < nrows) {
+                if (PF >= 1) prefetch(kr + 1);
+                sweep(true, kr + 1, false, 0, v);
+                finish1(kr + 1, v);
+            }
+            recv(kr);
+            sweep(false, 0, true, kr, v);
+        }
+    }
+    // no CTA leaves while a peer could still write into its shared memory
+    if constexpr (CL > 1) cluster_sync_all();
+}
+
+}  // namespace gbn

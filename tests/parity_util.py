@@ -101,6 +101,7 @@ def row_threads(variant: str):
         (r"bwtma(\d+)x(\d+)", lambda g: (512, g[0])),               # wide backward, bulk-copy ring
         (r"bwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)d?", lambda g: (g[0], g[2])),  # wide bwd, register sums
         (r"wcs(\d+)v(\d+)c(\d+)", lambda g: (g[0], g[2])),           # cluster slices in shared memory
+        (r"fwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)", lambda g: (g[0], g[2])),  # wide fwd, cluster slices
     )
     if variant.startswith("sk"):  # single-kernel backward: the staged kernel's geometry
         variant = variant[2:]

@@ -70,6 +70,10 @@ def _geom(name):
     if m:
         nt, k, cl, _, _, _ = (int(v) for v in m.groups())
         return ("bwtma", nt, k, cl)
+    m = re.fullmatch(r"fwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)", name)
+    if m:
+        nt, k, cl, _, _, _ = (int(v) for v in m.groups())
+        return ("bwtma", nt, k, cl)
     m = re.fullmatch(r"wtma(\d+)x(\d+)", name)
     if m:
         cw, u = (int(v) for v in m.groups())
@@ -524,6 +528,30 @@ def test_wcs_ring_wraps(op, direction, variant, N, limit):
     finally:
         g.set_grid_limit(0)
         g.force_variant(op == "ln", direction, "bf16", None)
+
+
+@pytest.mark.parametrize("op", ["rms", "ln"])
+@pytest.mark.parametrize("variant,N", [("fwr256k8c8p1m2f0", 131072), ("fwr256k8c4p0m2f0", 65536 - 24),
+                                       ("fwr512k4c2p0m1f0", 32768 - 8), ("fwr256k8c1p0m2f0", 16384),
+                                       ("fwr256k4c16p0m2f0", 131072 - 8 * 9), ("fwr256k8c8p0m2f1", 131072),
+                                       ("fwr256k8c4p0m2f1", 65536 - 8 * 3)])
+@pytest.mark.parametrize("limit", [1, 3])
+def test_wide_forward_cluster_rows(op, variant, N, limit):
+    """The cluster-slice wide forward under a grid cap (in clusters): each
+    cluster walks many rows, so the four exchange slots and the pass order
+    (pass 1 one row ahead of pass 2) go through many phases."""
+    import rmsnorm_norm_fwd_gb300 as g
+    cl = int(re.search(r"c(\d+)p", variant).group(1))
+    M = 23
+    try:
+        g.force_variant(op == "ln", 0, "bf16", variant)
+        g.set_grid_limit(limit * cl)
+        assert g.variant_name(op == "ln", 0, M, N, "bf16") == variant
+        rep, _, _ = run_case(op, "bf16", M, N)
+        rep.assert_ok()
+    finally:
+        g.set_grid_limit(0)
+        g.force_variant(op == "ln", 0, "bf16", None)
 
 
 @pytest.mark.parametrize("op", ["rms", "ln"])
