@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
     for (int64_t base = (int64_t)blockIdx.x * RPC; base < p.M; base += (int64_t)gridDim.x * RPC) {
         const int64_t row = base + grp;
         const bool rok = row < p.M;
-        float xf[VPT][E];
+        float2 xf[VPT][E / 2];  // the row's elements of this thread, as pairs
         {
             uint4 q[VPT];
 #pragma unroll
@@ -233,29 +233,31 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                for (int e = 0; e < E; ++e) xf[k][e] = vget<T>(q[k], e);
+                for (int e = 0; e < E / 2; ++e) xf[k][e] = vpair<T>(q[k], e);
         }
-        // four independent accumulation chains per thread (latency)
-        float sa[4] = {0.f, 0.f, 0.f, 0.f};
+        // four independent accumulation chains per thread (two pairs)
+        float2 sa[2] = {f2s(0.f), f2s(0.f)};
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < E; ++e) sa[e & 3] += LN ? xf[k][e] : xf[k][e] * xf[k][e];
-        const float s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
+            for (int e = 0; e < E / 2; ++e)
+                sa[e & 1] = LN ? f2add(sa[e & 1], xf[k][e]) : f2fma(xf[k][e], xf[k][e], sa[e & 1]);
+        const float s = (sa[0].x + sa[1].x) + (sa[0].y + sa[1].y);
         float mean = 0.f, rstd;
         if (LN && full) {
             // equal per-thread counts: local mean and M2, one combine (fwd_rows)
             constexpr float kC = (float)(VPT * E);
             float mm[1] = {s * (1.f / kC)}, m2[1];
-            float qa[4] = {0.f, 0.f, 0.f, 0.f};
+            const float2 nmm = f2s(-mm[0]);
+            float2 qa[2] = {f2s(0.f), f2s(0.f)};
 #pragma unroll
             for (int k = 0; k < VPT; ++k)
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float d = xf[k][e] - mm[0];
-                    qa[e & 3] += d * d;
+                for (int e = 0; e < E / 2; ++e) {
+                    const float2 d = f2add(xf[k][e], nmm);
+                    qa[e & 1] = f2fma(d, d, qa[e & 1]);
                 }
-            m2[0] = (qa[0] + qa[1]) + (qa[2] + qa[3]);
+            m2[0] = (qa[0].x + qa[1].x) + (qa[0].y + qa[1].y);
             row_meanvar_equal<TPR, RPC, 1>(mm, m2, kC, red2, parity);
             mean = mm[0];
             rstd = rsqrtf(m2[0] / n + p.eps);
@@ -264,16 +266,18 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
             row_allreduce<TPR, RPC, 1, 1>(a, red1, parity);
             if constexpr (LN) {
                 mean = a[0] / n;
-                a[0] = 0.f;
+                const float2 nm = f2s(-mean);
+                float2 q2 = f2s(0.f);
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
                     if (!vok[k]) continue;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float d = xf[k][e] - mean;
-                        a[0] += d * d;
+                    for (int e = 0; e < E / 2; ++e) {
+                        const float2 d = f2add(xf[k][e], nm);
+                        q2 = f2fma(d, d, q2);
                     }
                 }
+                a[0] = q2.x + q2.y;
                 row_allreduce<TPR, RPC, 1, 1>(a, red1, parity);
             }
             rstd = rsqrtf(a[0] / n + p.eps);
@@ -283,27 +287,23 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
             if (LN && p.mean) p.mean[row] = mean;
         }
         // y = ((x - mean) * rstd) * gamma (+ beta)
+        const float2 nm = f2s(-mean), rs = f2s(rstd);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             if (!(rok && vok[k])) continue;
-            float o[E];
+            float2 o[E / 2];
 #pragma unroll
             for (int h = 0; h < H; ++h) {
                 const float4 g = pars[h * nv + vid[k]];
-                float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-                if constexpr (LN) b = pars[(H + h) * nv + vid[k]];
-                o[4 * h] = ((xf[k][4 * h] - mean) * rstd) * g.x;
-                o[4 * h + 1] = ((xf[k][4 * h + 1] - mean) * rstd) * g.y;
-                o[4 * h + 2] = ((xf[k][4 * h + 2] - mean) * rstd) * g.z;
-                o[4 * h + 3] = ((xf[k][4 * h + 3] - mean) * rstd) * g.w;
+                o[2 * h] = f2mul(f2mul(f2add(xf[k][2 * h], nm), rs), make_float2(g.x, g.y));
+                o[2 * h + 1] = f2mul(f2mul(f2add(xf[k][2 * h + 1], nm), rs), make_float2(g.z, g.w));
                 if constexpr (LN) {
-                    o[4 * h] += b.x;
-                    o[4 * h + 1] += b.y;
-                    o[4 * h + 2] += b.z;
-                    o[4 * h + 3] += b.w;
+                    const float4 b = pars[(H + h) * nv + vid[k]];
+                    o[2 * h] = f2add(o[2 * h], make_float2(b.x, b.y));
+                    o[2 * h + 1] = f2add(o[2 * h + 1], make_float2(b.z, b.w));
                 }
             }
-            st_vec(p.y, row * nv + vid[k], vpack<T>(o));
+            st_vec(p.y, row * nv + vid[k], vpack2<T>(o));
         }
     }
 }
