@@ -324,9 +324,11 @@ bool wide_geometry(const Variant &v, const CallShape &c, int dev, size_t *dyn_sm
 }
 
 // Shared memory of a row-resident variant with gamma (and beta) staged as
-// fp32: [N] floats each; false if it does not fit.
+// fp32 ([N] floats each) or, raw, in their storage type ([N / E] 16-byte
+// vectors each); false if it does not fit.
 bool rows_s_geometry(const Variant &v, const CallShape &c, int dev, size_t *dyn_smem) {
-    const size_t bytes = (size_t)c.N * 4u * (c.is_ln ? 2u : 1u);
+    const size_t per = v.raw ? (size_t)(c.N / v.elems_per_vec) * 16u : (size_t)c.N * 4u;
+    const size_t bytes = per * (c.is_ln ? 2u : 1u);
     if (bytes + 4096 > (size_t)g_dev[dev].smem_optin) return false;
     *dyn_smem = bytes;
     return true;

@@ -40,6 +40,12 @@ namespace gbn {
             kRowsS, TPR, VPT, 1, 1, CTA, VecTraits<GBN_T>::E, MINB, 0},
 #define GBN_S_RMS(TPR, VPT, CTA, MINB) GBN_ROWS_S(false, TPR, VPT, CTA, MINB)
 #define GBN_S_LN(TPR, VPT, CTA, MINB) GBN_ROWS_S(true, TPR, VPT, CTA, MINB)
+#define GBN_ROWS_SR(LN, TPR, VPT, CTA, MINB)                                                   \
+    Variant{GBN_FWD_SR_VNAME(TPR, VPT, CTA, MINB),                                             \
+            (const void *)&fwd_rows_s<GBN_T, LN, TPR, VPT, CTA, MINB, true>, kRowsS, TPR, VPT, 1, 1, CTA, \
+            VecTraits<GBN_T>::E, MINB, 0, 0, 0, 1},
+#define GBN_SR_RMS(TPR, VPT, CTA, MINB) GBN_ROWS_SR(false, TPR, VPT, CTA, MINB)
+#define GBN_SR_LN(TPR, VPT, CTA, MINB) GBN_ROWS_SR(true, TPR, VPT, CTA, MINB)
 #define GBN_FTMP(LN, TPR, VPT, NT)                                                             \
     Variant{GBN_TMP_VNAME(TPR, VPT, NT), (const void *)&fwd_tmp<GBN_T, LN, TPR, VPT, NT>, kTmaP, TPR, \
             VPT, 0, 1, NT, VecTraits<GBN_T>::E, 1, 32768},
@@ -70,6 +76,7 @@ static const Variant rms_variants[] = {
     GBN_TMAC_FWD_GEOMS(GBN_C_RMS)
     GBN_WIDE_FWD_GEOMS(GBN_W_RMS)
     GBN_FWD_S_GEOMS(GBN_S_RMS)
+    GBN_FWD_SR_GEOMS(GBN_SR_RMS)
     GBN_FWD_GEOMS(GBN_X_RMS)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, false>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 static const Variant ln_variants[] = {
@@ -81,6 +88,7 @@ static const Variant ln_variants[] = {
     GBN_TMAC_FWD_GEOMS(GBN_C_LN)
     GBN_WIDE_FWD_GEOMS(GBN_W_LN)
     GBN_FWD_S_GEOMS(GBN_S_LN)
+    GBN_FWD_SR_GEOMS(GBN_SR_LN)
     GBN_FWD_GEOMS(GBN_X_LN)
     Variant{"elem", (const void *)&fwd_elem<GBN_T, true>, kElem, kElemCTA, 0, 1, 1, kElemCTA, 1, 0, 0}};
 const VariantTable GBN_CAT(kFwdRms_, GBN_SFX) = {rms_variants, (int)(sizeof(rms_variants) / sizeof(Variant))};
@@ -98,6 +106,9 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_W_RMS
 #undef GBN_W_LN
 #undef GBN_ROWS_S
+#undef GBN_ROWS_SR
+#undef GBN_SR_RMS
+#undef GBN_SR_LN
 #undef GBN_S_RMS
 #undef GBN_S_LN
 #undef GBN_FTMP

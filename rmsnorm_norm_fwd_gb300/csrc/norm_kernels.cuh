@@ -180,7 +180,10 @@ __global__ void __launch_bounds__(CTA) fwd_rows(const FwdParams p) {
 // converted once to fp32 registers.  Fewer registers per thread (more warps
 // per SM) and about half the instructions per element of fwd_rows for
 // LayerNorm: x is converted once, gamma and beta not at all per row.
-template <typename T, bool LN, int TPR, int VPT, int CTA, int MINB>
+// RAW: gamma and beta staged in their storage type ([nv] 16-byte vectors
+// each) and converted per use: a quarter of the fp32 planes' shared memory
+// for 16-bit types, so more CTAs fit on an SM.
+template <typename T, bool LN, int TPR, int VPT, int CTA, int MINB, bool RAW = false>
 __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
     static_assert(CTA % TPR == 0 && TPR % 32 == 0, "bad row-group shape");
     constexpr int E = VecTraits<T>::E;
@@ -189,6 +192,7 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
     // gamma as [H][nv] float4 (plane-major: a warp's 16-byte reads are
     // consecutive, no bank conflicts), then beta likewise
     extern __shared__ __align__(16) float4 pars[];
+    uint4 *const parr = reinterpret_cast<uint4 *>(pars);  // RAW: gamma [nv], then beta [nv]
     __shared__ RowReduceSmem<TPR, RPC, 1, 2> red2;
     __shared__ RowReduceSmem<TPR, RPC, 1, 1> red1;
 
@@ -202,6 +206,11 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
         const uint4 g = param_vec<T>(p.gamma, v, true);
         uint4 b = make_uint4(0, 0, 0, 0);
         if constexpr (LN) b = param_vec<T>(p.beta, v, false);
+        if constexpr (RAW) {
+            parr[v] = g;
+            if constexpr (LN) parr[nv + v] = b;
+            continue;
+        }
 #pragma unroll
         for (int h = 0; h < H; ++h) {
             pars[h * nv + v] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
@@ -292,6 +301,18 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
         for (int k = 0; k < VPT; ++k) {
             if (!(rok && vok[k])) continue;
             float2 o[E / 2];
+            if constexpr (RAW) {
+                const uint4 g = parr[vid[k]];
+                uint4 b = make_uint4(0, 0, 0, 0);
+                if constexpr (LN) b = parr[nv + vid[k]];
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) {
+                    o[e] = f2mul(f2mul(f2add(xf[k][e], nm), rs), vpair<T>(g, e));
+                    if constexpr (LN) o[e] = f2add(o[e], vpair<T>(b, e));
+                }
+                st_vec(p.y, row * nv + vid[k], vpack2<T>(o));
+                continue;
+            }
 #pragma unroll
             for (int h = 0; h < H; ++h) {
                 const float4 g = pars[h * nv + vid[k]];

@@ -132,6 +132,7 @@ struct Variant {
     int stage_target;    // kTma: bytes of one stage the host aims for
     int fused = 0;       // 1: the kernel also sums the partial rows (cooperative launch, no column reduce)
     int db = 0;          // kWideR: 1 the dbeta sums (and gamma, in its storage type) in shared memory
+    int raw = 0;         // kRowsS: 1 gamma (and beta) staged in their storage type, not as fp32
 
     // Longest row (elements) this variant can hold.
     int64_t max_n() const {

@@ -80,10 +80,11 @@ __device__ __forceinline__ void prefetch_row(const void *row, size_t row_bytes, 
 // warp: three butterfly sums, every lane ends with identical bits (each
 // butterfly step adds two operands in either order).  An empty union gives
 // (0, 0, 0).
+template <int G = 32>
 __device__ __forceinline__ void warp_combine(float &n, float &mean, float &m2) {
     float tn = n, ts = n * mean;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
+    for (int o = 1; o < G; o <<= 1) {
         tn += __shfl_xor_sync(0xffffffffu, tn, o);
         ts += __shfl_xor_sync(0xffffffffu, ts, o);
     }
@@ -91,7 +92,7 @@ __device__ __forceinline__ void warp_combine(float &n, float &mean, float &m2) {
     const float d = mean - mu;
     float tm = m2 + n * (d * d);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) tm += __shfl_xor_sync(0xffffffffu, tm, o);
+    for (int o = 1; o < G; o <<= 1) tm += __shfl_xor_sync(0xffffffffu, tm, o);
     n = tn;
     mean = mu;
     m2 = tm;
@@ -676,6 +677,7 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     constexpr int KB = FUSE ? (K < 2 ? K : 2) : (K < 4 ? K : 4);  // vectors per tensor per batch
     static_assert(NT % 32 == 0 && NT <= 1024 && CL >= 1 && CL <= 16 && K % KB == 0, "shape");
     static_assert(!DB || LN, "dbeta sums only for LayerNorm");
+    static_assert((W & (W - 1)) == 0 && (CL & (CL - 1)) == 0, "warps per CTA, CTAs per row: powers of two");
     // gamma of the slice: [H][K * NT] float4 (DB: [K * NT] raw vectors), then
     // (DB) the dbeta sums [H][K * NT] float4
     extern __shared__ __align__(16) float4 gsm[];
@@ -774,11 +776,13 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
             for (int i = 0; i < NVAL; ++i) red[parity][i][warp] = v[i];
         }
         __syncthreads();
+        // every warp runs the same butterfly over the warps' sums (lane l
+        // takes warp l % W's): identical bits in every thread
 #pragma unroll
         for (int i = 0; i < NVAL; ++i) {
-            float s = 0.f;
-#pragma unroll 4
-            for (int w = 0; w < W; ++w) s += red[parity][i][w];
+            float s = red[parity][i][lane & (W - 1)];
+#pragma unroll
+            for (int o = 1; o < W; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
             v[i] = s;
         }
         parity ^= 1;
@@ -799,12 +803,14 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
         if constexpr (CL > 1) {
             const int sp = (int)(kr % NS);
             mbar_wait_cluster_bounded(&xch[sp], (uint32_t)((kr / NS) & 1), &abort_flag, p.tc.fault);
+            // a butterfly over the CL partials (lane l takes rank l % CL's):
+            // identical bits in every thread of every CTA
             float s[NVAL];
 #pragma unroll
             for (int i = 0; i < NVAL; ++i) {
-                s[i] = 0.f;
+                s[i] = slot[sp][lane & (CL - 1)][i];
 #pragma unroll
-                for (int c = 0; c < CL; ++c) s[i] += slot[sp][c][i];
+                for (int o = 1; o < CL; o <<= 1) s[i] += __shfl_xor_sync(0xffffffffu, s[i], o);
             }
             cst[kr % 3][0] = LN ? s[NVAL - 1] / n : 0.f;
             cst[kr % 3][1] = s[0] / n;
@@ -813,8 +819,9 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     // One sweep over the slice: pass 1 of row k1 (if has1: this thread's
     // partials into v) and pass 2 of row k2 (if has2: dx and the sums), their
     // loads in the same batches so that both rows' latencies overlap.  The
-    // branches are uniform over the CTA.
-    auto sweep = [&](bool has1, int64_t k1, bool has2, int64_t k2, float (&v)[NVAL]) {
+    // branches are uniform over the CTA.  fullc: every thread holds all K
+    // vectors of its share (a literal in each inlined copy of the body).
+    auto sweep = [&](bool has1, int64_t k1, bool has2, int64_t k2, float (&v)[NVAL], bool fullc) {
         const float rstd1 = has1 ? __ldg(p.rstd + row_of(k1)) : 0.f;
         const float mean1 = (LN && has1) ? __ldg(p.mean + row_of(k1)) : 0.f;
         const float rstd2 = has2 ? __ldg(p.rstd + row_of(k2)) : 0.f;
@@ -833,7 +840,7 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
 #pragma unroll
             for (int i = 0; i < KB; ++i) {
                 const int64_t lv = (int64_t)(kb + i) * NT + t;
-                const bool ok = lv < cnt;
+                const bool ok = fullc || lv < cnt;
                 px[i] = (has1 && ok) ? ld_l2hint(x1 + lv, keep) : make_uint4(0, 0, 0, 0);
                 pd[i] = (has1 && ok) ? ld_l2hint(d1 + lv, keep) : make_uint4(0, 0, 0, 0);
                 qx[i] = (has2 && ok) ? ld_l2hint(x2 + lv, drop) : make_uint4(0, 0, 0, 0);
@@ -865,7 +872,7 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
                             b4 = make_float4(lo.x, lo.y, hi.x, hi.y);
                         }
                     }
-                    if (lv < cnt) st_l2hint(dx2 + lv, vpack2<T>(o), drop);
+                    if (fullc || lv < cnt) st_l2hint(dx2 + lv, vpack2<T>(o), drop);
                 }
                 if (has1) {
 #pragma unroll
@@ -881,38 +888,44 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
         if constexpr (LN) v[NVAL - 1] = a1.x + a1.y;
     };
 
-    float v[NVAL];
-    if constexpr (FUSE) {
-        // step j: pass 1 of row j with pass 2 of row j - 2, then row j's
-        // partials go out and row j - 1's come in (a whole sweep after they
-        // were sent)
-        if (PF == 2) prefetch(0);
-        for (int64_t j = 0; j < nrows + 2; ++j) {
-            const bool has1 = j < nrows, has2 = j >= 2;
-            if (PF >= 1) prefetch(j + (PF == 2 ? 1 : 0));
-            sweep(has1, j, has2, j - 2, v);
-            if (has1) finish1(j, v);
-            if (j >= 1 && j - 1 < nrows) recv(j - 1);
-        }
-    } else {
-        // pass 1 of row k + 1, then row k's exchange, then pass 2 of row k
-        if (PF == 2) prefetch(0);
-        if (nrows > 0) {
-            if (PF == 1) prefetch(0);
-            sweep(true, 0, false, 0, v);
-            finish1(0, v);
-        }
-        for (int64_t kr = 0; kr < nrows; ++kr) {
-            if (kr + 1 < nrows) {
-                if (PF == 1) prefetch(kr + 1);
-                if (PF == 2) prefetch(kr + 2);
-                sweep(true, kr + 1, false, 0, v);
-                finish1(kr + 1, v);
+    // the body once per case, so that with every vector of the share present
+    // the bound checks drop out of the compiled loops
+    auto run = [&](bool fullc) {
+        float v[NVAL];
+        if constexpr (FUSE) {
+            // step j: pass 1 of row j with pass 2 of row j - 2, then row j's
+            // partials go out and row j - 1's come in (a whole sweep after they
+            // were sent)
+            if (PF == 2) prefetch(0);
+            for (int64_t j = 0; j < nrows + 2; ++j) {
+                const bool has1 = j < nrows, has2 = j >= 2;
+                if (PF >= 1) prefetch(j + (PF == 2 ? 1 : 0));
+                sweep(has1, j, has2, j - 2, v, fullc);
+                if (has1) finish1(j, v);
+                if (j >= 1 && j - 1 < nrows) recv(j - 1);
             }
-            recv(kr);
-            sweep(false, 0, true, kr, v);
+        } else {
+            // pass 1 of row k + 1, then row k's exchange, then pass 2 of row k
+            if (PF == 2) prefetch(0);
+            if (nrows > 0) {
+                if (PF == 1) prefetch(0);
+                sweep(true, 0, false, 0, v, fullc);
+                finish1(0, v);
+            }
+            for (int64_t kr = 0; kr < nrows; ++kr) {
+                if (kr + 1 < nrows) {
+                    if (PF == 1) prefetch(kr + 1);
+                    if (PF == 2) prefetch(kr + 2);
+                    sweep(true, kr + 1, false, 0, v, fullc);
+                    finish1(kr + 1, v);
+                }
+                recv(kr);
+                sweep(false, 0, true, kr, v, fullc);
+            }
         }
-    }
+    };
+    if (cnt == (int64_t)KNT) run(true);
+    else run(false);
     // no CTA leaves while a peer could still write into its shared memory
     if constexpr (CL > 1) cluster_sync_all();
 
@@ -949,14 +962,18 @@ namespace gbn {
 // streams the slice from DRAM (L2 evict_last) for this thread's statistics
 // (RMS: the sum of squares; LN: count, mean and M2 per batch of KB vectors,
 // merged with the update of Chan, Golub and LeVeque), the CTA combines them
-// (warps in order) and sends them to every CTA of the cluster through
-// distributed shared memory (four slots); the row's exchange is collected
-// (CL partials in rank order: identical bits in every CTA) a whole sweep
-// later, then pass 2 writes y from the slice re-read from L2 (evict_first).
+// (every warp runs the same butterfly over the warps' partials) and sends
+// them to every CTA of the cluster through distributed shared memory (four
+// slots); the row's exchange is collected (a butterfly over the CL partials
+// in rank positions: identical bits in every CTA) a whole sweep later, then
+// pass 2 writes y from the slice re-read from L2 (evict_first).
 // Thread t owns vectors t + k * NT (k < K) of the slice.
 // FUSE: 0 pass 1 of row k + 1, the exchange of row k, then pass 2 of row k;
 // 1 pass 1 of row j in the same sweep as pass 2 of row j - 2 (both rows'
-// loads in flight together, KB = 4 vectors of each per batch).
+// loads in flight together, KB = 4 vectors of each per batch); 2 one pass:
+// the slice stays in registers from its DRAM read to its y (no L2 re-read),
+// two rows per thread, the next row's loads issued before this row's
+// statistics.
 template <typename T, bool LN, int NT, int K, int CL, int PF, int MINB, int FUSE = 0>
 __global__ void __launch_bounds__(NT, MINB) fwd_wider(const FwdParams p) {
     constexpr int E = VecTraits<T>::E;
@@ -964,8 +981,10 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wider(const FwdParams p) {
     constexpr int NVAL = LN ? 3 : 1;  // exchanged: (count, mean, M2) or the sum of squares
     constexpr int NS = 4;
     // vectors per batch: the whole of a thread's slice up to 8, 4 when fused
-    constexpr int KB = FUSE ? (K < 4 ? K : 4) : (K < 8 ? K : 8);
+    constexpr int KB = FUSE == 1 ? (K < 4 ? K : 4) : (K < 8 ? K : 8);
     static_assert(NT % 32 == 0 && NT <= 1024 && CL >= 1 && CL <= 16 && K % KB == 0, "shape");
+    static_assert(((KB * E) & (KB * E - 1)) == 0, "a whole batch holds a power-of-two count");
+    static_assert((W & (W - 1)) == 0 && (CL & (CL - 1)) == 0, "warps per CTA, CTAs per row: powers of two");
     extern __shared__ __align__(16) uint4 psm[];  // gamma of the slice [K * NT], then beta
     __shared__ float red[2][3][W];
     __shared__ float slot[NS][CL][NVAL];
@@ -1014,15 +1033,19 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wider(const FwdParams p) {
     // every thread), sent to the cluster (or, alone, turned into mean, rstd).
     // v: RMS {sum x^2}; LN {count, mean, M2}.
     auto finish1 = [&](int64_t k, float (&v)[NVAL]) {
+        // The warps' partials are combined by every warp at once: lane l
+        // takes warp l % W's, then a butterfly over W lanes (identical bits
+        // in every lane of every warp).
+        const int wl = lane & (W - 1);
         if constexpr (!LN) {
             float acc = v[0];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
             if (lane == 0) red[parity][0][warp] = acc;
             __syncthreads();
-            acc = 0.f;
-#pragma unroll 4
-            for (int w = 0; w < W; ++w) acc += red[parity][0][w];
+            acc = red[parity][0][wl];
+#pragma unroll
+            for (int o = 1; o < W; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
             v[0] = acc;
         } else {
             warp_combine(v[0], v[1], v[2]);
@@ -1032,23 +1055,10 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wider(const FwdParams p) {
                 red[parity][2][warp] = v[2];
             }
             __syncthreads();
-            // the same group combine over the warps, in warp order
-            float tn = 0.f, ts = 0.f;
-#pragma unroll 4
-            for (int w = 0; w < W; ++w) {
-                tn += red[parity][0][w];
-                ts += red[parity][0][w] * red[parity][1][w];
-            }
-            const float mu = tn > 0.f ? ts / tn : 0.f;
-            float a2 = 0.f;
-#pragma unroll 4
-            for (int w = 0; w < W; ++w) {
-                const float d = red[parity][1][w] - mu;
-                a2 += red[parity][2][w] + red[parity][0][w] * (d * d);
-            }
-            v[0] = tn;
-            v[1] = mu;
-            v[2] = a2;
+            v[0] = red[parity][0][wl];
+            v[1] = red[parity][1][wl];
+            v[2] = red[parity][2][wl];
+            warp_combine<W>(v[0], v[1], v[2]);
         }
         parity ^= 1;
         if constexpr (CL > 1) {
@@ -1069,43 +1079,138 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wider(const FwdParams p) {
         if constexpr (CL > 1) {
             const int sp = (int)(k % NS);
             mbar_wait_cluster_bounded(&xch[sp], (uint32_t)((k / NS) & 1), &abort_flag, p.tc.fault);
+            // lane l takes rank l % CL's partial, then a butterfly over CL
+            // lanes: identical bits in every thread of every CTA
+            const int cl = lane & (CL - 1);
             if constexpr (!LN) {
-                float s = 0.f;
+                float s = slot[sp][cl][0];
 #pragma unroll
-                for (int c = 0; c < CL; ++c) s += slot[sp][c][0];
+                for (int o = 1; o < CL; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                 cst[k % 3][0] = 0.f;
                 cst[k % 3][1] = rsqrtf(s / n + p.eps);
             } else {
-                float tn = 0.f, ts = 0.f;
-#pragma unroll
-                for (int c = 0; c < CL; ++c) {
-                    tn += slot[sp][c][0];
-                    ts += slot[sp][c][0] * slot[sp][c][1];
-                }
-                const float mu = ts / tn;
-                float a2 = 0.f;
-#pragma unroll
-                for (int c = 0; c < CL; ++c) {
-                    const float d = slot[sp][c][1] - mu;
-                    a2 += slot[sp][c][2] + slot[sp][c][0] * (d * d);
-                }
+                float tn = slot[sp][cl][0], mu = slot[sp][cl][1], a2 = slot[sp][cl][2];
+                warp_combine<CL>(tn, mu, a2);
                 cst[k % 3][0] = mu;
                 cst[k % 3][1] = rsqrtf(a2 / n + p.eps);
             }
         }
     };
-    // One sweep over the slice: pass 1 of row k1 (if has1: this thread's
-    // statistics into v) and pass 2 of row k2 (if has2: y), their loads in
-    // the same batches.  Branches uniform over the CTA.
-    auto sweep = [&](bool has1, int64_t k1, bool has2, int64_t k2, float (&v)[NVAL]) {
-        const uint4 *x1 = row_x(has1 ? k1 : 0), *x2 = row_x(has2 ? k2 : 0);
-        const float mean2 = cst[(has2 ? k2 : 0) % 3][0], rstd2 = cst[(has2 ? k2 : 0) % 3][1];
-        const float2 nm = f2s(-mean2), rs = f2s(rstd2);
-        if (has2 && rank == 0 && t == 0) {
-            const int64_t row = row_of(k2);
+    // One accumulation chain per pair position of a vector (E / 2 chains),
+    // summed pairwise at the end of the batch.
+    auto chains = [&](float2 (&c)[E / 2]) {
+#pragma unroll
+        for (int w = 1; w < E / 2; w <<= 1)
+#pragma unroll
+            for (int e = 0; e + w < E / 2; e += 2 * w) c[e] = f2add(c[e], c[e + w]);
+        return c[0];
+    };
+    // This thread's statistics of KB vectors q (vectors kb .. kb + KB - 1 of
+    // its share) folded into the running RMS sum of squares a, or the LN
+    // running count, mean and M2.  fullc: every thread holds all K vectors
+    // of its share (no per-vector bound checks; a literal in each inlined
+    // copy of the body below).
+    auto stat_batch = [&](const uint4 (&q)[KB], int kb, float2 &a, float &cn, float &mean, float &m2, bool fullc) {
+        const bool FULL = fullc;
+        if constexpr (!LN) {
+            float2 c[E / 2];
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) c[e] = f2s(0.f);
+#pragma unroll
+            for (int i = 0; i < KB; ++i)
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) {
+                    const float2 f = vpair<T>(q[i], e);
+                    c[e] = f2fma(f, f, c[e]);
+                }
+            a = f2add(a, chains(c));
+        } else {
+            int nb = 0;
+            float2 c[E / 2];
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) c[e] = f2s(0.f);
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                if (FULL || (int64_t)(kb + i) * NT + t < cnt) nb += E;
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) c[e] = f2add(c[e], vpair<T>(q[i], e));
+            }
+            if (nb > 0) {
+                const float fb = (float)nb;
+                const float2 s2 = chains(c);
+                // a whole batch holds a power-of-two count: the product by its
+                // reciprocal is the correctly rounded quotient
+                const float mb = nb == KB * E ? (s2.x + s2.y) * (1.f / (float)(KB * E)) : __fdiv_rn(s2.x + s2.y, fb);
+                const float2 nmb = f2s(-mb);
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) c[e] = f2s(0.f);
+#pragma unroll
+                for (int i = 0; i < KB; ++i) {
+                    if (!FULL && (int64_t)(kb + i) * NT + t >= cnt) continue;
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e) {
+                        const float2 d = f2add(vpair<T>(q[i], e), nmb);
+                        c[e] = f2fma(d, d, c[e]);
+                    }
+                }
+                const float2 d2 = chains(c);
+                const float m2b = d2.x + d2.y;
+                if (cn == 0.f) {
+                    cn = fb;
+                    mean = mb;
+                    m2 = m2b;
+                } else {
+                    // running += batch
+                    const float tot = cn + fb;
+                    const float d = mb - mean;
+                    const float rr = __fdiv_rn(fb, tot);
+                    mean += d * rr;
+                    m2 += m2b + d * d * cn * rr;
+                    cn = tot;
+                }
+            }
+        }
+    };
+    auto stat_out = [&](const float2 &a, float cn, float mean, float m2, float (&v)[NVAL]) {
+        if constexpr (!LN) {
+            v[0] = a.x + a.y;
+        } else {
+            v[0] = cn;
+            v[1] = mean;
+            v[2] = m2;
+        }
+    };
+    // The row's (mean and) rstd, stored by one thread of rank 0.
+    auto put_stats = [&](int64_t k, float mean2, float rstd2) {
+        if (rank == 0 && t == 0) {
+            const int64_t row = row_of(k);
             if (p.rstd) p.rstd[row] = rstd2;
             if (LN && p.mean) p.mean[row] = mean2;
         }
+    };
+    // y of vector lv of the slice from its x (q).
+    auto out_vec = [&](const uint4 &q, int64_t lv, uint4 *yr, float2 nm, float2 rs) {
+        const uint4 g = psm[lv];
+        uint4 b = make_uint4(0, 0, 0, 0);
+        if constexpr (LN) b = psm[KNT + lv];
+        float2 o[E / 2];
+#pragma unroll
+        for (int e = 0; e < E / 2; ++e) {
+            const float2 xh = f2mul(f2add(vpair<T>(q, e), nm), rs);
+            // LN: xhat * gamma + beta in one rounding
+            o[e] = LN ? f2fma(xh, vpair<T>(g, e), vpair<T>(b, e)) : f2mul(xh, vpair<T>(g, e));
+        }
+        st_l2hint(yr + lv, vpack2<T>(o), drop);
+    };
+    // One sweep over the slice: pass 1 of row k1 (if has1: this thread's
+    // statistics into v) and pass 2 of row k2 (if has2: y), their loads in
+    // the same batches.  Branches uniform over the CTA.
+    auto sweep = [&](bool has1, int64_t k1, bool has2, int64_t k2, float (&v)[NVAL], bool fullc) {
+        const bool FULL = fullc;
+        const uint4 *x1 = row_x(has1 ? k1 : 0), *x2 = row_x(has2 ? k2 : 0);
+        const float mean2 = cst[(has2 ? k2 : 0) % 3][0], rstd2 = cst[(has2 ? k2 : 0) % 3][1];
+        const float2 nm = f2s(-mean2), rs = f2s(rstd2);
+        if (has2) put_stats(k2, mean2, rstd2);
         uint4 *yr = static_cast<uint4 *>(p.y) + row_of(has2 ? k2 : 0) * nv + v0;
         float2 a = f2s(0.f);                 // RMS: sum of squares
         float cn = 0.f, mean = 0.f, m2 = 0.f;  // LN: running count, mean, M2
@@ -1115,7 +1220,7 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wider(const FwdParams p) {
 #pragma unroll
             for (int i = 0; i < KB; ++i) {
                 const int64_t lv = (int64_t)(kb + i) * NT + t;
-                const bool ok = lv < cnt;
+                const bool ok = FULL || lv < cnt;
                 q1[i] = (has1 && ok) ? ld_l2hint(x1 + lv, keep) : make_uint4(0, 0, 0, 0);
                 q2[i] = (has2 && ok) ? ld_l2hint(x2 + lv, drop) : make_uint4(0, 0, 0, 0);
             }
@@ -1123,107 +1228,105 @@ __global__ void __launch_bounds__(NT, MINB) fwd_wider(const FwdParams p) {
 #pragma unroll
                 for (int i = 0; i < KB; ++i) {
                     const int64_t lv = (int64_t)(kb + i) * NT + t;
-                    if (lv >= cnt) continue;
-                    const uint4 g = psm[lv];
-                    uint4 b = make_uint4(0, 0, 0, 0);
-                    if constexpr (LN) b = psm[KNT + lv];
-                    float2 o[E / 2];
-#pragma unroll
-                    for (int e = 0; e < E / 2; ++e) {
-                        o[e] = f2mul(f2mul(f2add(vpair<T>(q2[i], e), nm), rs), vpair<T>(g, e));
-                        if constexpr (LN) o[e] = f2add(o[e], vpair<T>(b, e));
-                    }
-                    st_l2hint(yr + lv, vpack2<T>(o), drop);
+                    if (FULL || lv < cnt) out_vec(q2[i], lv, yr, nm, rs);
                 }
             }
-            if (has1) {
-                if constexpr (!LN) {
-#pragma unroll
-                    for (int i = 0; i < KB; ++i)
-#pragma unroll
-                        for (int e = 0; e < E / 2; ++e) {
-                            const float2 f = vpair<T>(q1[i], e);
-                            a = f2fma(f, f, a);
-                        }
-                } else {
-                    int nb = 0;
-                    float2 s2 = f2s(0.f);
-#pragma unroll
-                    for (int i = 0; i < KB; ++i) {
-                        if ((int64_t)(kb + i) * NT + t < cnt) nb += E;
-#pragma unroll
-                        for (int e = 0; e < E / 2; ++e) s2 = f2add(s2, vpair<T>(q1[i], e));
-                    }
-                    if (nb > 0) {
-                        const float fb = (float)nb;
-                        const float mb = __fdiv_rn(s2.x + s2.y, fb);
-                        const float2 nmb = f2s(-mb);
-                        float2 d2 = f2s(0.f);
-#pragma unroll
-                        for (int i = 0; i < KB; ++i) {
-                            if ((int64_t)(kb + i) * NT + t >= cnt) continue;
-#pragma unroll
-                            for (int e = 0; e < E / 2; ++e) {
-                                const float2 d = f2add(vpair<T>(q1[i], e), nmb);
-                                d2 = f2fma(d, d, d2);
-                            }
-                        }
-                        const float m2b = d2.x + d2.y;
-                        if (cn == 0.f) {
-                            cn = fb;
-                            mean = mb;
-                            m2 = m2b;
-                        } else {
-                            // running += batch
-                            const float tot = cn + fb;
-                            const float d = mb - mean;
-                            const float rr = __fdiv_rn(fb, tot);
-                            mean += d * rr;
-                            m2 += m2b + d * d * cn * rr;
-                            cn = tot;
-                        }
-                    }
-                }
-            }
+            if (has1) stat_batch(q1, kb, a, cn, mean, m2, fullc);
         }
-        if constexpr (!LN) {
-            v[0] = a.x + a.y;
-        } else {
-            v[0] = cn;
-            v[1] = mean;
-            v[2] = m2;
+        stat_out(a, cn, mean, m2, v);
+    };
+    // Register-resident rows (FUSE 2): the slice of row k, read once from
+    // DRAM, stays in this thread's registers (q) until its y is written.
+    auto load_r = [&](int64_t k, uint4 (&q)[K], bool fullc) {
+        const bool FULL = fullc;
+        const bool has = k < nrows;
+        const uint4 *xr = row_x(has ? k : 0);
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const int64_t lv = (int64_t)i * NT + t;
+            q[i] = (has && (FULL || lv < cnt)) ? ld_l2hint(xr + lv, drop) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto stats_r = [&](const uint4 (&q)[K], float (&v)[NVAL], bool fullc) {
+        float2 a = f2s(0.f);
+        float cn = 0.f, mean = 0.f, m2 = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < K; kb += KB) {
+            uint4 qb[KB];
+#pragma unroll
+            for (int i = 0; i < KB; ++i) qb[i] = q[kb + i];
+            stat_batch(qb, kb, a, cn, mean, m2, fullc);
+        }
+        stat_out(a, cn, mean, m2, v);
+    };
+    auto write_r = [&](int64_t k, const uint4 (&q)[K], bool fullc) {
+        const bool FULL = fullc;
+        const float mean2 = cst[k % 3][0], rstd2 = cst[k % 3][1];
+        put_stats(k, mean2, rstd2);
+        uint4 *yr = static_cast<uint4 *>(p.y) + row_of(k) * nv + v0;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const int64_t lv = (int64_t)i * NT + t;
+            if (FULL || lv < cnt) out_vec(q[i], lv, yr, f2s(-mean2), f2s(rstd2));
         }
     };
 
-    float v[NVAL];
-    if constexpr (FUSE) {
-        // step j: pass 1 of row j with pass 2 of row j - 2, then row j's
-        // statistics go out and row j - 1's come in (a whole sweep after
-        // they were sent)
-        for (int64_t j = 0; j < nrows + 2; ++j) {
-            const bool has1 = j < nrows, has2 = j >= 2;
-            if (PF >= 1) prefetch(j + 1);
-            sweep(has1, j, has2, j - 2, v);
-            if (has1) finish1(j, v);
-            if (j >= 1 && j - 1 < nrows) recv(j - 1);
-        }
-    } else {
-        // pass 1 of row k + 1, then row k's exchange, then pass 2 of row k
-        if (PF >= 1) prefetch(0);
-        if (nrows > 0) {
-            sweep(true, 0, false, 0, v);
-            finish1(0, v);
-        }
-        for (int64_t kr = 0; kr < nrows; ++kr) {
-            if (kr + 1 < nrows) {
-                if (PF >= 1) prefetch(kr + 1);
-                sweep(true, kr + 1, false, 0, v);
-                finish1(kr + 1, v);
+    // Every thread holds all K vectors of its share (uniform over the CTA):
+    // the body is inlined once per case, so with fullc true the bound checks
+    // drop out of the compiled loops.
+    auto run = [&](bool fullc) {
+        float v[NVAL];
+        if constexpr (FUSE == 2) {
+            // row k + 1's loads go out before row k's statistics, so they are in
+            // flight through row k's reduction, exchange and y
+            uint4 qa[K], qb[K];
+            load_r(0, qa, fullc);
+            for (int64_t k = 0; k < nrows; k += 2) {
+                load_r(k + 1, qb, fullc);
+                stats_r(qa, v, fullc);
+                finish1(k, v);
+                recv(k);
+                write_r(k, qa, fullc);
+                if (k + 1 < nrows) {
+                    load_r(k + 2, qa, fullc);
+                    stats_r(qb, v, fullc);
+                    finish1(k + 1, v);
+                    recv(k + 1);
+                    write_r(k + 1, qb, fullc);
+                }
             }
-            recv(kr);
-            sweep(false, 0, true, kr, v);
+        } else if constexpr (FUSE) {
+
+            // step j: pass 1 of row j with pass 2 of row j - 2, then row j's
+            // statistics go out and row j - 1's come in (a whole sweep after
+            // they were sent)
+            for (int64_t j = 0; j < nrows + 2; ++j) {
+                const bool has1 = j < nrows, has2 = j >= 2;
+                if (PF >= 1) prefetch(j + 1);
+                sweep(has1, j, has2, j - 2, v, fullc);
+                if (has1) finish1(j, v);
+                if (j >= 1 && j - 1 < nrows) recv(j - 1);
+            }
+        } else {
+            // pass 1 of row k + 1, then row k's exchange, then pass 2 of row k
+            if (PF >= 1) prefetch(0);
+            if (nrows > 0) {
+                sweep(true, 0, false, 0, v, fullc);
+                finish1(0, v);
+            }
+            for (int64_t kr = 0; kr < nrows; ++kr) {
+                if (kr + 1 < nrows) {
+                    if (PF >= 1) prefetch(kr + 1);
+                    sweep(true, kr + 1, false, 0, v, fullc);
+                    finish1(kr + 1, v);
+                }
+                recv(kr);
+                sweep(false, 0, true, kr, v, fullc);
+            }
         }
-    }
+    };
+    if (cnt == (int64_t)KNT) run(true);
+    else run(false);
     // no CTA leaves while a peer could still write into its shared memory
     if constexpr (CL > 1) cluster_sync_all();
 }

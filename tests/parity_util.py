@@ -91,7 +91,7 @@ def row_threads(variant: str):
     compiled variant, from its name."""
     pats = (
         (r"(\d+)x(\d+)r(\d+)c(\d+)b(\d+)", lambda g: (g[0], g[3])),   # register rows (cluster)
-        (r"s(\d+)x(\d+)b(\d+)m(\d+)", lambda g: (g[0], 1)),           # register rows, params in smem
+        (r"s(\d+)x(\d+)b(\d+)m(\d+)r?", lambda g: (g[0], 1)),         # register rows, params in smem
         (r"tmp(\d+)x(\d+)b(\d+)", lambda g: (g[0], 1)),               # staged rows, no producer
         (r"tma(\d+)x(\d+)w(\d+)", lambda g: (g[0], 1)),               # staged rows, producer warp
         (r"tmac(\d+)x(\d+)s(\d+)", lambda g: (256, g[0])),            # staged cluster rows

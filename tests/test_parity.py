@@ -38,7 +38,7 @@ def _geom(name):
     m = re.fullmatch(r"(\d+)x(\d+)r(\d+)c(\d+)b(\d+)", name)
     if m:
         return tuple(int(v) for v in m.groups()) + (False,)
-    m = re.fullmatch(r"s(\d+)x(\d+)b(\d+)m(\d+)", name)
+    m = re.fullmatch(r"s(\d+)x(\d+)b(\d+)m(\d+)r?", name)
     if m:
         tpr, vpt, cta, _ = (int(v) for v in m.groups())
         return (tpr, vpt, 1, 1, cta, False)
@@ -534,12 +534,17 @@ def test_wcs_ring_wraps(op, direction, variant, N, limit):
 @pytest.mark.parametrize("variant,N", [("fwr256k8c8p1m2f0", 131072), ("fwr256k8c4p0m2f0", 65536 - 24),
                                        ("fwr512k4c2p0m1f0", 32768 - 8), ("fwr256k8c1p0m2f0", 16384),
                                        ("fwr256k4c16p0m2f0", 131072 - 8 * 9), ("fwr256k8c8p0m2f1", 131072),
-                                       ("fwr256k8c4p0m2f1", 65536 - 8 * 3)])
+                                       ("fwr256k8c4p0m2f1", 65536 - 8 * 3), ("fwr256k8c8p0m2f2", 131072),
+                                       ("fwr256k8c4p0m2f2", 65536 - 24), ("fwr512k8c1p0m1f2", 32768 - 8 * 9),
+                                       ("fwr256k8c1p0m2f2", 16384 - 8), ("fwr256k4c1p0m4f2", 8192),
+                                       ("fwr256k8c2p0m2f2", 32768 - 8)])
 @pytest.mark.parametrize("limit", [1, 3])
 def test_wide_forward_cluster_rows(op, variant, N, limit):
     """The cluster-slice wide forward under a grid cap (in clusters): each
     cluster walks many rows, so the four exchange slots and the pass order
-    (pass 1 one row ahead of pass 2) go through many phases."""
+    (pass 1 one row ahead of pass 2; in the one-pass form the two register
+    buffers, with an odd row count ending on the first) go through many
+    phases."""
     import rmsnorm_norm_fwd_gb300 as g
     cl = int(re.search(r"c(\d+)p", variant).group(1))
     M = 23
