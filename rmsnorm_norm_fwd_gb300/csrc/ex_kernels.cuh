@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(NT, 1) fwd_exr(const ExFwdParams p) {
     unsigned char *gsm = smem + kTmaHeaderBytes;  // gamma, then beta
     unsigned char *bsm = gsm + exr_param_bytes(p.N, p.pdt, false, planes);
     unsigned char *stages = smem + kTmaHeaderBytes + exr_param_bytes(p.N, p.pdt, LN, planes);
-    const float4 *gpl = reinterpret_cast<const float4 *>(gsm), *bpl = reinterpret_cast<const float4 *>(bsm);
+    const float4 *gpl = reinterpret_cast<const float4 *>(gsm);  // planes: gamma, then beta at + 2 * nc
     const int SG = p.tc.stages / RPP, RT = p.tc.rows;
     const size_t xsec = exr_section(RT, p.N, xdt);
     const int64_t ntiles = (M + RT - 1) / RT;

@@ -209,15 +209,15 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
         if constexpr (RAW) {
             parr[v] = g;
             if constexpr (LN) parr[nv + v] = b;
-            continue;
-        }
+        } else {
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-            pars[h * nv + v] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
-                                           vget<T>(g, 4 * h + 3));
-            if constexpr (LN)
-                pars[(H + h) * nv + v] = make_float4(vget<T>(b, 4 * h), vget<T>(b, 4 * h + 1),
-                                                     vget<T>(b, 4 * h + 2), vget<T>(b, 4 * h + 3));
+            for (int h = 0; h < H; ++h) {
+                pars[h * nv + v] = make_float4(vget<T>(g, 4 * h), vget<T>(g, 4 * h + 1), vget<T>(g, 4 * h + 2),
+                                               vget<T>(g, 4 * h + 3));
+                if constexpr (LN)
+                    pars[(H + h) * nv + v] = make_float4(vget<T>(b, 4 * h), vget<T>(b, 4 * h + 1),
+                                                         vget<T>(b, 4 * h + 2), vget<T>(b, 4 * h + 3));
+            }
         }
     }
     __syncthreads();
@@ -310,18 +310,17 @@ __global__ void __launch_bounds__(CTA, MINB) fwd_rows_s(const FwdParams p) {
                     o[e] = f2mul(f2mul(f2add(xf[k][e], nm), rs), vpair<T>(g, e));
                     if constexpr (LN) o[e] = f2add(o[e], vpair<T>(b, e));
                 }
-                st_vec(p.y, row * nv + vid[k], vpack2<T>(o));
-                continue;
-            }
+            } else {
 #pragma unroll
-            for (int h = 0; h < H; ++h) {
-                const float4 g = pars[h * nv + vid[k]];
-                o[2 * h] = f2mul(f2mul(f2add(xf[k][2 * h], nm), rs), make_float2(g.x, g.y));
-                o[2 * h + 1] = f2mul(f2mul(f2add(xf[k][2 * h + 1], nm), rs), make_float2(g.z, g.w));
-                if constexpr (LN) {
-                    const float4 b = pars[(H + h) * nv + vid[k]];
-                    o[2 * h] = f2add(o[2 * h], make_float2(b.x, b.y));
-                    o[2 * h + 1] = f2add(o[2 * h + 1], make_float2(b.z, b.w));
+                for (int h = 0; h < H; ++h) {
+                    const float4 g = pars[h * nv + vid[k]];
+                    o[2 * h] = f2mul(f2mul(f2add(xf[k][2 * h], nm), rs), make_float2(g.x, g.y));
+                    o[2 * h + 1] = f2mul(f2mul(f2add(xf[k][2 * h + 1], nm), rs), make_float2(g.z, g.w));
+                    if constexpr (LN) {
+                        const float4 b = pars[(H + h) * nv + vid[k]];
+                        o[2 * h] = f2add(o[2 * h], make_float2(b.x, b.y));
+                        o[2 * h + 1] = f2add(o[2 * h + 1], make_float2(b.z, b.w));
+                    }
                 }
             }
             st_vec(p.y, row * nv + vid[k], vpack2<T>(o));

@@ -9,7 +9,7 @@ constants of fp32 arithmetic only; nothing measured on the GPU output enters a
 bound.  u = 2^-24 is the unit roundoff of fp32; ulp_T(v) is the spacing of
 dtype T at |v| with v first rounded to T (the smallest subnormal spacing at 0).
 
-Stated tolerances (the benchmark spec's figures) and how they are read:
+Stated tolerances (the target figures for this path) and how they are read:
   y      : 1 ulp_T of the oracle value (fp16 also 2e-3 relative);
   rstd   : 1e-5 relative; mean: 1e-5 (|mean| + sigma);
   dx     : 2 ulp_T of the oracle value;
