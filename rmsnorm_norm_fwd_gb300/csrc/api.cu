@@ -259,10 +259,10 @@ bool wider_geometry(const Variant &v, const CallShape &c, int dev, size_t *dyn_s
     const int64_t nv = c.N / v.elems_per_vec;
     const int64_t slice = (nv + v.cl - 1) / v.cl;
     if (slice > (int64_t)v.tpr * v.vpt) return false;
-    // gamma as fp32 planes; with db, gamma in its storage type and the dbeta
-    // sums as fp32 planes
+    // gamma as fp32 planes; with db 1, gamma in its storage type and the
+    // dbeta sums as fp32 planes; with db 2, the dbeta sums only
     const size_t planes = (size_t)(v.elems_per_vec / 4) * (size_t)v.tpr * v.vpt * 16u;
-    const size_t bytes = v.db ? (size_t)v.tpr * v.vpt * 16u + planes : planes;
+    const size_t bytes = v.db == 1 ? (size_t)v.tpr * v.vpt * 16u + planes : planes;
     if (bytes + 4096 > (size_t)g_dev[dev].smem_optin) return false;
     *dyn_smem = bytes;
     return true;

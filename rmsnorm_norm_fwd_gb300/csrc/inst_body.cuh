@@ -175,6 +175,10 @@ const VariantTable GBN_CAT(kFwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
     Variant{GBN_WIDER_VNAME(NT, K, CL, PF, MINB, F) "d",                                       \
             (const void *)&bwd_wider<GBN_T, true, NT, K, CL, PF, MINB, F, 1>, kWideR, NT, K, 1, CL, NT, \
             VecTraits<GBN_T>::E, MINB, 0, 0, 1},
+#define GBN_WIDER_DG(NT, K, CL, PF, MINB, F)                                                   \
+    Variant{GBN_WIDER_VNAME(NT, K, CL, PF, MINB, F) "g",                                       \
+            (const void *)&bwd_wider<GBN_T, true, NT, K, CL, PF, MINB, F, 2>, kWideR, NT, K, 1, CL, NT, \
+            VecTraits<GBN_T>::E, MINB, 0, 0, 2},
 #define GBN_WR_RMS(NT, K, CL, PF, MINB, F) GBN_WIDER(false, NT, K, CL, PF, MINB, F)
 #define GBN_WR_LN(NT, K, CL, PF, MINB, F) GBN_WIDER(true, NT, K, CL, PF, MINB, F)
 #define GBN_BWCS(LN, NT, VPT, CL)                                                              \
@@ -197,6 +201,7 @@ static const Variant rms_variants[] = {
 static const Variant ln_variants[] = {
     GBN_WCS_GEOMS(GBN_BWCS_LN)
     GBN_WIDER_DB_GEOMS(GBN_WIDER_DB)
+    GBN_WIDER_DG_GEOMS(GBN_WIDER_DG)
     GBN_WIDER_BWD_GEOMS(GBN_WR_LN)
     GBN_BWTMA_BWD_GEOMS(GBN_BWT_LN)
     GBN_TMA_BWD_GEOMS(GBN_T_LN)
@@ -223,6 +228,7 @@ const VariantTable GBN_CAT(kBwdLn_, GBN_SFX) = {ln_variants, (int)(sizeof(ln_var
 #undef GBN_WR_LN
 #undef GBN_BWCS
 #undef GBN_WIDER_DB
+#undef GBN_WIDER_DG
 #undef GBN_BWCS_RMS
 #undef GBN_BWCS_LN
 #undef GBN_SKTMA

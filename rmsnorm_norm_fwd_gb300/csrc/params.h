@@ -131,7 +131,7 @@ struct Variant {
     int ctas_per_sm;     // kTma: CTAs meant to share an SM (shared-memory budget split); kWide: launch bound
     int stage_target;    // kTma: bytes of one stage the host aims for
     int fused = 0;       // 1: the kernel also sums the partial rows (cooperative launch, no column reduce)
-    int db = 0;          // kWideR: 1 the dbeta sums (and gamma, in its storage type) in shared memory
+    int db = 0;          // kWideR: 1 the dbeta sums (and gamma, in its storage type) in shared memory; 2 the sums only
     int raw = 0;         // kRowsS: 1 gamma (and beta) staged in their storage type, not as fp32
 
     // Longest row (elements) this variant can hold.

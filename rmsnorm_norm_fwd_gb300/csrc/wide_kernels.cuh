@@ -665,7 +665,9 @@ namespace gbn {
 // DB (LayerNorm): 1 the dbeta sums in shared memory (each thread's own fp32
 // plane entries, a read-modify-write per vector) and gamma kept there in its
 // storage type, which frees K * E registers for a larger K or a second CTA
-// per SM; 0 both sums in registers, gamma widened to fp32.
+// per SM; 2 as 1 with gamma read from global memory (L1/L2) per use instead,
+// a third less shared memory per CTA (more L1 beside it for the loads in
+// flight); 0 both sums in registers, gamma widened to fp32.
 template <typename T, bool LN, int NT, int K, int CL, int PF, int MINB, int FUSE, int DB = 0>
 __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     pdl_launch_dependents();  // the column reduce waits for this grid's completion
@@ -699,13 +701,13 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     constexpr int KNT = K * NT;
 
     uint4 *graw = reinterpret_cast<uint4 *>(gsm);
-    float4 *dbs = gsm + KNT;  // DB: this slice's dbeta sums
+    float4 *dbs = gsm + (DB == 1 ? KNT : 0);  // DB: this slice's dbeta sums
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const int64_t lv = (int64_t)k * NT + t;
         const uint4 g = lv < cnt ? param_vec<T>(p.gamma, v0 + lv, true) : make_uint4(0, 0, 0, 0);
         if constexpr (DB) {
-            graw[lv] = g;
+            if constexpr (DB == 1) graw[lv] = g;
 #pragma unroll
             for (int h = 0; h < H; ++h) dbs[h * KNT + lv] = make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
@@ -748,7 +750,11 @@ __global__ void __launch_bounds__(NT, MINB) bwd_wider(const BwdParams p) {
     };
     auto gam = [&](int k, float2 (&g)[E / 2]) {
         const int64_t lv = (int64_t)k * NT + t;
-        if constexpr (DB) {
+        if constexpr (DB == 2) {
+            const uint4 q = lv < cnt ? param_vec<T>(p.gamma, v0 + lv, true) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) g[e] = vpair<T>(q, e);
+        } else if constexpr (DB) {
             const uint4 q = graw[lv];
 #pragma unroll
             for (int e = 0; e < E / 2; ++e) g[e] = vpair<T>(q, e);

@@ -99,7 +99,7 @@ def row_threads(variant: str):
         (r"bwide(\d+)u(\d+)c(\d+)p(\d+)f(\d+)m(\d+)", lambda g: (g[0], g[2])),  # wide backward
         (r"wtma(\d+)x(\d+)", lambda g: (32 * g[0], 1)),             # wide forward, bulk-copy ring
         (r"bwtma(\d+)x(\d+)", lambda g: (512, g[0])),               # wide backward, bulk-copy ring
-        (r"bwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)d?", lambda g: (g[0], g[2])),  # wide bwd, register sums
+        (r"bwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)[dg]?", lambda g: (g[0], g[2])),  # wide bwd, register sums
         (r"wcs(\d+)v(\d+)c(\d+)", lambda g: (g[0], g[2])),           # cluster slices in shared memory
         (r"fwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)", lambda g: (g[0], g[2])),  # wide fwd, cluster slices
     )

@@ -66,7 +66,7 @@ def _geom(name):
     if m:
         nt, vpt, cl = (int(v) for v in m.groups())
         return ("wcs", nt, vpt, cl)
-    m = re.fullmatch(r"bwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)d?", name)
+    m = re.fullmatch(r"bwr(\d+)k(\d+)c(\d+)p(\d+)m(\d+)f(\d+)[dg]?", name)
     if m:
         nt, k, cl, _, _, _ = (int(v) for v in m.groups())
         return ("bwtma", nt, k, cl)
@@ -565,14 +565,15 @@ def test_wide_forward_cluster_rows(op, variant, N, limit):
                                        ("bwr256k4c16p1m2f1", 131072), ("bwr256k8c8p1m2f0", 131072 - 24),
                                        ("bwr256k4c2p1m2f1", 3000), ("bwr512k4c1p1m1f1", 16384),
                                        ("bwr512k4c1p1m1f0", 16384), ("bwr256k8c8p1m2f0d", 131072),
-                                       ("bwr256k8c8p1m2f1d", 131072 - 24), ("bwr512k8c4p1m1f0d", 65536 + 8)])
+                                       ("bwr256k8c8p1m2f1d", 131072 - 24), ("bwr512k8c4p1m1f0d", 65536 + 8),
+                                       ("bwr256k8c8p1m2f0g", 131072 - 24), ("bwr256k8c4p1m2f0g", 65536)])
 @pytest.mark.parametrize("limit", [1, 3])
 def test_wide_backward_ring_wraps(op, variant, N, limit):
     """The bulk-copy wide backward under a grid cap (in clusters): each cluster
     walks many rows, so the ring stages, the pass order (pass 1 one row ahead
     of pass 2) and the four exchange slots go through many phases."""
     import rmsnorm_norm_fwd_gb300 as g
-    if variant.endswith("d") and op != "ln":
+    if variant.endswith(("d", "g")) and op != "ln":
         pytest.skip("dbeta-in-shared-memory variants exist for LayerNorm only")
     cl = int(re.match(r"bwtma(\d+)x", variant).group(1)) if variant.startswith("bwtma") else \
         int(re.search(r"c(\d+)p", variant).group(1))
