@@ -1,7 +1,8 @@
 """tune.py's table writer (CPU only): a partial sweep replaces exactly the
 rows it measured, keeps the fastest variant per (op, direction, dtype, M
 bucket, N), leaves every other row and the default rows as they were, and is
-stable; a small-M measurement gets a row of its own ahead of the any-M row."""
+stable; a small-M measurement gets a row of its own ahead of the any-M row;
+a near tie keeps the current variant."""
 import os
 import re
 import shutil
@@ -65,3 +66,23 @@ def test_small_m_row_precedes_any_m_row(tmp_path):
     assert i_small < i_big
     assert rows[i_small].startswith(f'{{0, 1, 2, {tune.SMALL_M}, 128, "small"}}')
     assert rows[i_big].startswith('{0, 1, 2, -1, 128, "big"}')
+
+
+def test_near_tie_keeps_the_current_variant(tmp_path):
+    """A measured row keeps its variant unless a challenger is faster by more
+    than KEEP_MARGIN (event timestamps step by about 2 us, so short calls tie)."""
+    path = tmp_path / "dispatch_table.inc"
+    shutil.copy(TABLE, path)
+    rows = _rows(path.read_text())
+    # the LayerNorm forward bf16 row at N = 131072 (16384 vectors), any M
+    row = next(r for r in rows if r.startswith("{1, 0, 2, -1, 16384,"))
+    current = re.search(r'"([^"]+)"', row).group(1)
+    base = {"op": "ln", "dir": 0, "dtype": "bf16", "M": 2048, "N": 131072}
+    near = 1000.0 * (1 + tune.KEEP_MARGIN / 2)
+    tune.emit([dict(base, variant=current, gbs=1000.0), dict(base, variant="challenger", gbs=near)], str(path))
+    row = next(r for r in _rows(path.read_text()) if r.startswith("{1, 0, 2, -1, 16384,"))
+    assert f'"{current}"' in row
+    far = 1000.0 * (1 + 2 * tune.KEEP_MARGIN)
+    tune.emit([dict(base, variant=current, gbs=1000.0), dict(base, variant="challenger", gbs=far)], str(path))
+    row = next(r for r in _rows(path.read_text()) if r.startswith("{1, 0, 2, -1, 16384,"))
+    assert '"challenger"' in row
