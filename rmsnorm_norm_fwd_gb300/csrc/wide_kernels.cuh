@@ -979,7 +979,10 @@ namespace gbn {
 // loads in flight together, KB = 4 vectors of each per batch); 2 one pass:
 // the slice stays in registers from its DRAM read to its y (no L2 re-read),
 // two rows per thread, the next row's loads issued before this row's
-// statistics.
+// statistics.  In every mode the four exchange slots are safe to reuse: a
+// peer sends row k + 4 only after it has received this CTA's row k + 2,
+// which this CTA sends after the CTA barrier in its statistics step, and
+// that barrier follows its reads of row k's slot.
 template <typename T, bool LN, int NT, int K, int CL, int PF, int MINB, int FUSE = 0>
 __global__ void __launch_bounds__(NT, MINB) fwd_wider(const FwdParams p) {
     constexpr int E = VecTraits<T>::E;
